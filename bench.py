@@ -1,0 +1,568 @@
+#!/usr/bin/env python3
+"""Benchmark: group-wise low-bit weight quantization hot path on GB300.
+
+One step = one pass of the whole hot path over one transformer layer's seven
+projections (hidden 4096, intermediate 14336, kv 1024; 218,103,808 bf16
+weights, N(0, 0.02) with 0.5% outlier input columns), all inputs resident in HBM:
+
+  GPTQ asym int4 quantize+pack (+ fused SNR)   gptq_quantize_asym   x7
+  GPTQ asym dequantize -> bf16 [N,K]           gptq_dequantize      x7
+  GPTQ sym  int4 quantize+pack (+ fused SNR)   gptq_quantize_sym    x7
+  GPTQ sym  dequantize -> bf16 [N,K]           gptq_dequantize      x7
+  MXFP4 quantize (half-even ties)              mxfp4_quantize       x7
+  MXFP4 dequantize -> bf16                     mxfp4_dequantize     x7
+  MXFP4 reconstruction SNR / rel. error        quant_snr            x7
+  uintx4 quantize + shard pack (group 64)      uintx_quantize       x7
+  uintx4 unpack + dequantize -> bf16           uintx_dequantize     x7
+  AWQ alpha search (gate||up, 2048 rows, 11 a) awq_search           x1
+
+metric value = weight GB/s: bf16 bytes of the weights every quantize and every
+dequantize kernel handles (8 passes x 436.2 MB per step) / step time.
+
+Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
+launching stream; L2 (129 MB) is flushed by a 256 MB write before every step
+(outside the events; the inputs, 436 MB, exceed L2 anyway); a barrier and
+torch.cuda.synchronize() on both sides of the K timed steps; max over ranks.
+Per-phase events give each kernel's average launch duration for the roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "weight GB/s quantized+packed (and dequantized) on 1 GB300; % of HBM roofline"
+UNIT = "GB/s"
+NBITS_UINTX = 4
+GROUP_GPTQ = 128
+GROUP_UINTX = 64
+THROTTLE_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+                 0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+                 0x100: "display_clock_setting"}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 4:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                mask = int(parts[3], 16)
+            except ValueError:
+                continue
+            for bit, name in THROTTLE_BITS.items():
+                if mask & bit and name != "gpu_idle":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload
+class Workload:
+    """The layer's tensors plus every preallocated output and workspace."""
+
+    def __init__(self, device, seed_offset=0):
+        import weight_only_bit_group_gb300 as wq
+        from weight_only_bit_group_gb300 import synth
+
+        self.wq = wq
+        self.dev = device
+        self.layer = synth.gptq_layer(seed=2 + seed_offset, device=device)
+        self.numel = sum(w.numel() for _, w in self.layer)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(4 + seed_offset)
+        gate = dict(self.layer)["gate_proj"]
+        up = dict(self.layer)["up_proj"]
+        self.gate_up = torch.cat([gate, up], 0)  # the page concatenates before searching
+        self.act = synth.awq_activation(gate.shape[1], seed=4 + seed_offset, device=device)
+        self.alphas = synth.ALPHAS
+        self.out = []
+        maxnumel = max(w.numel() for _, w in self.layer)
+        self.deq = torch.empty(maxnumel, dtype=torch.bfloat16, device=device)
+        for name, w in self.layer:
+            n, k = w.shape
+            g = k // GROUP_GPTQ
+            o = {}
+            for tag in ("asym", "sym"):
+                o[tag] = dict(qweight=torch.empty(k // 8, n, dtype=torch.int32, device=device),
+                              qzeros=torch.empty(g, n // 8, dtype=torch.int32, device=device),
+                              scales=torch.empty(g, n, dtype=torch.float16, device=device),
+                              g_idx=torch.empty(k, dtype=torch.int32, device=device),
+                              snr_db=torch.empty((), dtype=torch.float64, device=device),
+                              ws=wq.workspace(wq.WQ_OP_GPTQ_QUANTIZE, n, k, GROUP_GPTQ, device))
+            o["mx"] = dict(packed=torch.empty(n, k // 2, dtype=torch.uint8, device=device),
+                           e8m0=torch.empty(n, k // 32, dtype=torch.uint8, device=device))
+            o["snr"] = dict(snr_db=torch.empty((), dtype=torch.float64, device=device),
+                            rel_err=torch.empty((), dtype=torch.float64, device=device),
+                            ws=wq.workspace(wq.WQ_OP_QUANT_SNR, n, k, 0, device))
+            o["ux"] = dict(packed=torch.empty(wq.uintx_packed_bytes(n * k, NBITS_UINTX),
+                                              dtype=torch.uint8, device=device),
+                           scale=torch.empty(n, k // GROUP_UINTX, dtype=torch.bfloat16, device=device),
+                           zp=torch.empty(n, k // GROUP_UINTX, dtype=torch.uint8, device=device))
+            self.out.append(o)
+        n, k = self.gate_up.shape
+        self.awq_out = dict(best_s=torch.empty(k, dtype=torch.float32, device=device),
+                            best_idx=torch.empty((), dtype=torch.int32, device=device),
+                            best_alpha=torch.empty((), dtype=torch.float32, device=device),
+                            errs=torch.empty(len(self.alphas), dtype=torch.float64, device=device),
+                            ws=wq.workspace(wq.WQ_OP_AWQ_SEARCH, n, k, len(self.alphas), device))
+
+    # phases: (name, callable, algorithmic bytes, weight bytes counted in the metric, kernels)
+    def phases(self, inputs=None):
+        wq = self.wq
+        layer = inputs if inputs is not None else self.layer
+        P = []
+
+        def each(fn):
+            return lambda: [fn(i, w) for i, (_, w) in enumerate(layer)]
+
+        def deq_view(w):
+            return self.deq[: w.numel()].view(w.shape)
+
+        for tag, quant, sym in (("asym", wq.gptq_quantize_asym, False), ("sym", wq.gptq_quantize_sym, True)):
+            def q(i, w, quant=quant, tag=tag):
+                o = self.out[i][tag]
+                quant(w, GROUP_GPTQ, True, qweight=o["qweight"], qzeros=o["qzeros"],
+                      scales=o["scales"], g_idx=o["g_idx"], snr_db=o["snr_db"], ws=o["ws"])
+
+            def d(i, w, sym=sym, tag=tag):
+                o = self.out[i][tag]
+                n, k = w.shape
+                wq.gptq_dequantize(o["qweight"], o["qzeros"], o["scales"], n, k, GROUP_GPTQ, sym,
+                                   torch.bfloat16, "nk", out=deq_view(w))
+
+            qbytes = sum(2 * w.numel() + w.numel() // 2 + (w.numel() // GROUP_GPTQ) * (2 + 0.5)
+                         + 4 * w.shape[1] for _, w in layer)
+            dbytes = sum(w.numel() // 2 + (w.numel() // GROUP_GPTQ) * (2 + 0.5) + 2 * w.numel()
+                         for _, w in layer)
+            P.append((f"gptq_quantize_{tag}", each(q), qbytes, 2 * self.numel, 2 * len(layer)))
+            P.append((f"gptq_dequantize_{tag}", each(d), dbytes, 2 * self.numel, len(layer)))
+
+        def mq(i, w):
+            o = self.out[i]["mx"]
+            wq.mxfp4_quantize(w, 0, packed=o["packed"], e8m0=o["e8m0"])
+
+        def md(i, w):
+            o = self.out[i]["mx"]
+            wq.mxfp4_dequantize(o["packed"], o["e8m0"], torch.bfloat16, out=deq_view(w))
+            s = self.out[i]["snr"]
+            wq.quant_snr(w, deq_view(w), "nk", snr_db=s["snr_db"], rel_err=s["rel_err"], ws=s["ws"])
+
+        mx_q = sum(2 * w.numel() + w.numel() // 2 + w.numel() // 32 for _, w in layer)
+        mx_d = sum(w.numel() // 2 + w.numel() // 32 + 2 * w.numel() + 4 * w.numel() for _, w in layer)
+        P.append(("mxfp4_quantize", each(mq), mx_q, 2 * self.numel, len(layer)))
+        P.append(("mxfp4_dequantize+quant_snr", each(md), mx_d, 2 * self.numel, 3 * len(layer)))
+
+        def uq(i, w):
+            o = self.out[i]["ux"]
+            wq.uintx_quantize(w, NBITS_UINTX, GROUP_UINTX, packed=o["packed"], scale=o["scale"], zp=o["zp"])
+
+        def ud(i, w):
+            o = self.out[i]["ux"]
+            n, k = w.shape
+            wq.uintx_dequantize(o["packed"], o["scale"], o["zp"], n, k, NBITS_UINTX, GROUP_UINTX,
+                                torch.bfloat16, out=deq_view(w))
+
+        side = 3 / GROUP_UINTX
+        ux_q = sum(w.numel() * (2 + NBITS_UINTX / 8 + side) for _, w in layer)
+        ux_d = sum(w.numel() * (NBITS_UINTX / 8 + side + 2) for _, w in layer)
+        P.append(("uintx_quantize", each(uq), ux_q, 2 * self.numel, len(layer)))
+        P.append(("uintx_dequantize", each(ud), ux_d, 2 * self.numel, len(layer)))
+
+        def awq():
+            o = self.awq_out
+            wq.awq_search(self.gate_up, self.act, self.alphas, 2048, 0, best_s=o["best_s"],
+                          best_idx=o["best_idx"], best_alpha=o["best_alpha"], errs=o["errs"], ws=o["ws"])
+
+        awq_bytes = 2048 * self.gate_up.shape[1] * 2
+        P.append(("awq_search", awq, awq_bytes, 0, 3))
+        return P
+
+    def results(self):
+        """The step's products a caller takes home (quantized tensors + scalars)."""
+        outs = []
+        for o in self.out:
+            for tag in ("asym", "sym"):
+                outs += [o[tag]["qweight"], o[tag]["qzeros"], o[tag]["scales"], o[tag]["snr_db"]]
+            outs += [o["mx"]["packed"], o["mx"]["e8m0"], o["snr"]["snr_db"], o["snr"]["rel_err"]]
+            outs += [o["ux"]["packed"], o["ux"]["scale"], o["ux"]["zp"]]
+        outs += [self.awq_out["best_s"], self.awq_out["best_idx"], self.awq_out["errs"]]
+        return outs
+
+
+def source_sha(kernel_file: str) -> str:
+    path = os.path.join(ROOT, "weight_only_bit_group_gb300", "csrc", kernel_file)
+    h = hashlib.sha256()
+    for p in (path, os.path.join(ROOT, "weight_only_bit_group_gb300", "csrc", "wq_common.cuh")):
+        with open(p, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+PHASE_SOURCE = {"gptq_quantize_asym": "gptq.cu", "gptq_quantize_sym": "gptq.cu",
+                "gptq_dequantize_asym": "gptq.cu", "gptq_dequantize_sym": "gptq.cu",
+                "mxfp4_quantize": "mxfp4.cu", "mxfp4_dequantize+quant_snr": "mxfp4.cu",
+                "uintx_quantize": "uintx.cu", "uintx_dequantize": "uintx.cu", "awq_search": "awq.cu"}
+
+
+def ncu_traffic(phase: str, launches: int):
+    """dram bytes per launch of the phase's main kernel from the committed ncu
+    summary, or None when absent or taken on different kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        d = json.load(fh)
+    e = d.get(phase)
+    if not e or e.get("source_sha") != source_sha(PHASE_SOURCE[phase]):
+        return None
+    return e.get("dram_bytes_per_step") / launches if e.get("dram_bytes_per_step") else None
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, dist):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if dist is not None:
+        dist.barrier()
+    __graft_entry__.build()
+
+    wl = Workload(dev, seed_offset=100 * rank)
+    phases = wl.phases()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(record):
+        evs = []
+        for name, fn, *_ in phases:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((name, a, b))
+        return evs
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(False)
+    torch.cuda.synchronize(dev)
+
+    per_phase = {name: [] for name, *_ in phases}
+    step_ms = []
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        wall0 = time.perf_counter()
+        recs = []
+        for _ in range(args.steps):
+            flush.zero_()
+            evs = step(True)
+            recs.append(evs)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    for evs in recs:
+        tot = 0.0
+        for name, a, b in evs:
+            t = a.elapsed_time(b)
+            per_phase[name].append(t)
+            tot += t
+        step_ms.append(tot)
+    ms = statistics.mean(step_ms)
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    weight_bytes = sum(p[3] for p in phases)
+    value = world * weight_bytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    kernels = {}
+    for name, fn, alg_bytes, wbytes, nk in phases:
+        t = statistics.mean(per_phase[name])
+        gbs = alg_bytes / (t * 1e-3) / 1e9
+        kernels[name] = {"ms": round(t, 4), "share": None, "alg_GBps": round(gbs, 1),
+                         "frac_of_" + peak_kind: round(gbs / peak, 4)}
+    for name in kernels:
+        kernels[name]["share"] = round(kernels[name]["ms"] / ms, 4)
+    dom = max((p for p in phases if p[3] > 0), key=lambda p: statistics.mean(per_phase[p[0]]))
+    dom_t = statistics.mean(per_phase[dom[0]])
+    n_launch = len(wl.layer)
+    achieved = dom[2] / (dom_t * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom[0], "achieved": round(achieved, 1), "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": ncu_traffic(dom[0], n_launch),
+                "alg_bytes_per_launch": round(dom[2] / n_launch)}
+    launches = sum(p[4] for p in phases) * args.steps
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, dev, dist, world)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) bf16 with 0.5% outlier input columns x20; "
+                "LogNormal(0,1) activation means)",
+        "config": {"workload": "gptq_layer_7proj_h4096_i14336_kv1024 (218,103,808 weights) "
+                               "through every hot-path row",
+                   "weights_per_step": wl.numel, "weight_bytes_per_step": weight_bytes,
+                   "gptq_group": GROUP_GPTQ, "uintx_nbits": NBITS_UINTX, "uintx_group": GROUP_UINTX,
+                   "mxfp4_ties": "half_even", "awq": "gate||up [28672,4096] -> 2048 rows, 11 alphas",
+                   "l2": "flushed (256 MB write) before every step; inputs 436 MB > L2",
+                   "parallelism": f"replicas x{world} (one layer per GPU, no collective)"},
+        "roofline": roofline,
+        "kernels": kernels,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+    return line
+
+
+def run_e2e(args, wl, dev, dist, world):
+    """Same step through the public API with host-resident inputs: every step
+    copies the layer from pinned host memory to the device and copies the
+    quantized products back, inside the timed region."""
+    host_in = [w.cpu().pin_memory() for _, w in wl.layer]
+    dev_in = [torch.empty_like(w) for _, w in wl.layer]
+    outs = wl.results()
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    inputs = [(name, d) for (name, _), d in zip(wl.layer, dev_in)]
+    phases = wl.phases(inputs)
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        for _, fn, *_ in phases:
+            fn()
+        for o, h in zip(outs, host_out):
+            h.copy_(o, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    wbytes = sum(p[3] for p in phases)
+    return {"value": round(world * wbytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample_step(sample, alphas):
+    """One pass of the whole path through the CPU oracle on `sample` (list of
+    bf16 CPU tensors), tensors spread over host threads.  Returns weight bytes
+    (same definition as the GPU metric)."""
+    import concurrent.futures as cf
+
+    import oracle
+    from weight_only_bit_group_gb300 import synth
+
+    def one(w):
+        n, k = w.shape
+        for sym in (False, True):
+            qw, qz, sc, gi, snr = oracle.gptq_quantize(w, GROUP_GPTQ, sym)
+            oracle.gptq_dequantize(qw, qz, sc, n, k, GROUP_GPTQ, sym, out_kn=False)
+        p, e = oracle.mxfp4_quantize(w)
+        d = oracle.mxfp4_dequantize(p, e)
+        oracle.quant_snr(w, d)
+        p, s, z, _ = oracle.uintx_quantize(w, NBITS_UINTX, GROUP_UINTX)
+        oracle.uintx_dequantize(p, s, z, n, k, NBITS_UINTX, GROUP_UINTX)
+        return 8 * 2 * w.numel()
+
+    threads = min(len(sample), os.cpu_count() or 1)
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        futs = [ex.submit(one, w) for w in sample[:-1]]
+        gate_up = sample[-1]
+        a = synth.awq_activation(gate_up.shape[1]).numpy()
+        awq = ex.submit(oracle.awq_search, gate_up, a, alphas, 64)
+        wbytes = sum(f.result() for f in futs)
+        awq.result()
+    return wbytes, threads
+
+
+def cpu_sample(rows=256):
+    from weight_only_bit_group_gb300 import synth
+
+    layer = synth.gptq_layer(device="cpu")
+    sample = [w[:rows].contiguous() for _, w in layer]
+    gate_up = torch.cat([dict(layer)["gate_proj"][: 2 * rows], dict(layer)["up_proj"][: 2 * rows]])
+    return sample + [gate_up]
+
+
+def cpu_baseline(seconds=15.0):
+    import oracle
+
+    oracle.build()
+    from weight_only_bit_group_gb300 import synth
+
+    sample = cpu_sample()
+    t0 = time.perf_counter()
+    wbytes, threads = oracle_sample_step(sample, synth.ALPHAS)
+    dt = time.perf_counter() - t0
+    reps = 1
+    while time.perf_counter() - t0 < seconds * 0.5 and reps < 8:
+        oracle_sample_step(sample, synth.ALPHAS)
+        reps += 1
+    dt = (time.perf_counter() - t0) / reps
+    n = sum(w.numel() for w in sample[:-1])
+    return {"value": round(wbytes / dt / 1e9, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first 256 rows of each of the 7 projections ({n} weights) through every "
+                      f"quantize/dequantize/SNR row, plus AWQ on gate||up rows (64-row subsample); "
+                      f"{reps} passes, {dt:.2f} s each"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+
+    oracle.build()
+    from weight_only_bit_group_gb300 import synth
+
+    sample = cpu_sample()
+    for _ in range(args.warmup):
+        oracle_sample_step(sample, synth.ALPHAS)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        wbytes, threads = oracle_sample_step(sample, synth.ALPHAS)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = round(wbytes / dt / 1e9, 3)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded)",
+            "config": {"workload": "gptq_layer_7proj_h4096_i14336_kv1024 through every hot-path "
+                                   "row (bounded CPU sample: first 256 rows of each projection)",
+                       "parallelism": "host threads"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": "first 256 rows of each of the 7 projections"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as td
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        td.init_process_group(backend)
+        dist = td
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, dist)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

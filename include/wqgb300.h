@@ -1,0 +1,226 @@
+/*
+ * wqgb300.h -- C ABI of libwqgb300.so: group-wise low-bit weight quantization
+ * and its inverse on one NVIDIA GB300 (sm_103a).
+ *
+ * Formats (each restated from the page that defines it):
+ *   GPTQ int4   -- export_gptq_cpu.py: pack_int32, quantize_sym, quantize_asym and
+ *                  the module docstring (uint4b8: w = (code - 8) * scale).
+ *   OCP MXFP4   -- quantize_dflash_mxfp4.py: E2M1 table, quantize_mxfp4,
+ *                  dequantize_mxfp4, search_scale (AWQ alpha search).
+ *   uintx       -- uintx_quant.py: module docstring, _pack_shard, pack_uintx,
+ *                  unpack_uintx, UIntXQuantizer._quantize_impl, _dequantize_native.
+ *   SNR / rel.  -- export_gptq_cpu.py quantize_* (snr) and the relative-error
+ *                  report in quantize_dflash_mxfp4.py main().
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates or frees device memory.  Scratch space, where an operation
+ *     needs it, is the caller's `workspace` of at least wq_workspace_bytes(...).
+ *   - Matrices are dense row-major.  A weight is a torch Linear weight
+ *     [n = out_features, k = in_features].  bf16 and fp16 values are passed as
+ *     their 16-bit patterns (uint16_t).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *     is asynchronous on that stream; results, including scalars such as snr_db,
+ *     are written to device memory.
+ *   - Return value: WQ_OK, or an argument error detected on the host before any
+ *     launch (nothing is launched then), or WQ_ERR_CUDA when a launch failed
+ *     (wq_last_cuda_error() gives the CUDA error string).  No exception crosses
+ *     the ABI and nothing aborts the process.
+ *   - n == 0 or k == 0 is a valid empty input: nothing is launched, WQ_OK.
+ *   - Pointers to the main tensors must be 16-byte aligned (WQ_ERR_MISALIGNED
+ *     otherwise); side tensors (scales, zero points, g_idx) need only their
+ *     element alignment.
+ *   - Inputs must be finite; results for NaN/Inf inputs are unspecified (the
+ *     pages do not handle them either).
+ *   - The library is safe to call from several host threads on different
+ *     streams, provided their workspaces do not overlap.
+ */
+#ifndef WQGB300_H
+#define WQGB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int wq_status;
+
+#define WQ_OK 0
+#define WQ_ERR_NULL_PTR 1
+#define WQ_ERR_BAD_SHAPE 2
+#define WQ_ERR_BAD_DTYPE 3
+#define WQ_ERR_MISALIGNED 4
+#define WQ_ERR_UNSUPPORTED 5
+#define WQ_ERR_WORKSPACE_TOO_SMALL 6
+#define WQ_ERR_CUDA 7
+#define WQ_ERR_DEVICE_TIMEOUT 8 /* reserved: no kernel in this version waits */
+
+/* Output element types. */
+#define WQ_DTYPE_F32 0
+#define WQ_DTYPE_BF16 1
+
+/* Layout of a dequantized matrix. NK = [n, k] (the weight's own layout);
+ * KN = [k, n] (the transposed layout the GPTQ page computes its deq in). */
+#define WQ_LAYOUT_NK 0
+#define WQ_LAYOUT_KN 1
+
+/* MXFP4 rounding of exact e2m1 midpoints.
+ * HALF_EVEN: the even e2m1 index of the two neighbours (0.25->0, 0.75->1,
+ *   1.25->1, 1.75->2, 2.5->2, 3.5->4, 5->4) -- what the page's docstring,
+ *   comment and quark config ("round_method": "half_even") state.
+ * PAGE_LITERAL: the page's code as written, argmin (first of equal distances)
+ *   then (argmin // 2) * 2 on ties: 0.75->0, 1.75->1, 3.5->2, others as above. */
+#define WQ_TIE_HALF_EVEN 0
+#define WQ_TIE_PAGE_LITERAL 1
+
+/* Operations that take a workspace (first argument of wq_workspace_bytes). */
+#define WQ_OP_GPTQ_QUANTIZE 0 /* arg = group; only needed when snr_db != NULL */
+#define WQ_OP_QUANT_SNR 1     /* arg ignored */
+#define WQ_OP_AWQ_SEARCH 2    /* arg = n_alpha */
+
+/* Human-readable name of a status code (static string). */
+const char* wq_status_string(wq_status status);
+
+/* Text of the CUDA error behind the last WQ_ERR_CUDA returned on this host
+ * thread ("" if none). */
+const char* wq_last_cuda_error(void);
+
+/* Library version string. */
+const char* wq_version(void);
+
+/* Bytes of workspace `op` needs for an [n, k] weight (0 if none).  Pure host
+ * arithmetic: needs no GPU. */
+size_t wq_workspace_bytes(int op, int64_t n, int64_t k, int arg);
+
+/* ---------------------------------------------------------------- GPTQ int4
+ * gptq_quantize_sym  (export_gptq_cpu.py, quantize_sym)
+ * gptq_quantize_asym (export_gptq_cpu.py, quantize_asym)
+ *
+ * In:  w        bf16 [n, k], 16-byte aligned.
+ *      group    group size along k: 32, 64, 128 (the page's default) or 256;
+ *               k % group == 0, n % 8 == 0 (qzeros packs 8 columns per int32).
+ * Out: qweight  int32 [k/8, n]: word (r, c) holds the codes of w[c][8r .. 8r+7],
+ *               code of w[c][8r+i] in bits 4i..4i+3 (low nibble first).
+ *      qzeros   int32 [k/group, n/8] (may be NULL): sym stores 7 in every nibble
+ *               (the classic zp - 1 convention); asym packs the zero point zp
+ *               itself of columns 8c'..8c'+7, low nibble first (no "-1").
+ *      scales   fp16 [k/group, n] (bit patterns), round-to-nearest-even of the
+ *               binary32 scale.
+ *      g_idx    int32 [k] = kk / group (may be NULL).
+ *      snr_db   (may be NULL) one double: 20*log10(||w|| / max(||w - deq||, 1e-12))
+ *               over the whole tensor, deq = (code - zp) * binary32 scale.  Needs
+ *               workspace >= wq_workspace_bytes(WQ_OP_GPTQ_QUANTIZE, n, k, group).
+ * Math per (group g, column c), binary32 IEEE, round half to even:
+ *   sym : scale = max(amax / 8, 1e-9), code = clamp(round(x / scale) + 8, 0, 15)
+ *   asym: scale = max(wmax - wmin, 1e-9) / 15, zp = clamp(round(-wmin/scale), 0, 15),
+ *         code = clamp(round(x / scale) + zp, 0, 15)
+ * Bit-exact with a true IEEE division (the kernel uses a correctly rounded
+ * reciprocal plus one FMA correction step). */
+wq_status gptq_quantize_sym(const uint16_t* w, int64_t n, int64_t k, int group, int32_t* qweight,
+                            int32_t* qzeros, uint16_t* scales, int32_t* g_idx, double* snr_db,
+                            void* workspace, size_t workspace_bytes, void* stream);
+wq_status gptq_quantize_asym(const uint16_t* w, int64_t n, int64_t k, int group, int32_t* qweight,
+                             int32_t* qzeros, uint16_t* scales, int32_t* g_idx, double* snr_db,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* gptq_dequantize (export_gptq_cpu.py module docstring: uint4b8 w = (code-8)*scale;
+ * with real zero points w = (code - zp) * scale).
+ * In:  qweight, qzeros (ignored when sym != 0, may be NULL then), scales as
+ *      produced above; sym selects the rule.
+ * Out: out  [n, k] (out_layout WQ_LAYOUT_NK) or [k, n] (WQ_LAYOUT_KN), element
+ *      type out_dtype (WQ_DTYPE_F32: exact; WQ_DTYPE_BF16: round to nearest even
+ *      of the exact value), 16-byte aligned. */
+wq_status gptq_dequantize(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales,
+                          int64_t n, int64_t k, int group, int sym, int out_dtype, int out_layout,
+                          void* out, void* stream);
+
+/* ---------------------------------------------------------------- OCP MXFP4
+ * mxfp4_quantize (quantize_dflash_mxfp4.py, quantize_mxfp4)
+ * In:  w bf16 [n, k], k % 32 == 0, 16-byte aligned; tie_mode WQ_TIE_*.
+ * Out: packed  u8 [n, k/2]: byte j = code[2j] | code[2j+1] << 4, code = sign << 3 |
+ *              e2m1 magnitude index (0, .5, 1, 1.5, 2, 3, 4, 6).
+ *      e8m0    u8 [n, k/32] = exp + 127, exp = clamp(floor(log2 amax) - 2, -127,
+ *              127) (exp = 0 for an all-zero block).  floor(log2) is the exact
+ *              binary exponent.
+ * Each value v = w / 2^exp, magnitude clamped at 6, nearest grid magnitude,
+ * sign = signbit(v) (so -0.0 codes as 8). */
+wq_status mxfp4_quantize(const uint16_t* w, int64_t n, int64_t k, int tie_mode, uint8_t* packed,
+                         uint8_t* e8m0, void* stream);
+
+/* mxfp4_dequantize (quantize_dflash_mxfp4.py, dequantize_mxfp4)
+ * out[n][c] = +-E2M1[code & 7] * 2^(e8m0 - 127) as binary32 (WQ_DTYPE_F32) or bf16
+ * (WQ_DTYPE_BF16; exact, the value has at most 2 significant bits).  e8m0 = 255
+ * gives inf (or NaN for a zero code), as 2^128 does in binary32.  out 16-byte
+ * aligned. */
+wq_status mxfp4_dequantize(const uint8_t* packed, const uint8_t* e8m0, int64_t n, int64_t k,
+                           int out_dtype, void* out, void* stream);
+
+/* awq_search (quantize_dflash_mxfp4.py, search_scale)
+ * In:  W bf16 [n, k] (k % 32 == 0); a binary32 [k] per-channel mean |x| (device);
+ *      alphas: n_alpha (1..16) binary32 values on the HOST; max_rows (>= 1) rows
+ *      kept by the strided subsample (rows 0, s, 2s, ... with s = max(1, n /
+ *      max_rows), first max_rows of them, when n > max_rows); tie_mode as above.
+ * Out (device): best_s binary32 [k]; best_idx int32 [1]; best_alpha binary32 [1];
+ *      errs double [n_alpha]: err(alpha) = sum(((deq(quant(W*s))/s) - W) * a_c)^2
+ *      with a_c = max(a, 1e-8), s = t / exp(mean(log t)), t = clamp((a_c /
+ *      mean(a_c))^alpha, 1e-2, 1e2).  The first alpha with the strictly smallest
+ *      error wins.  Scale preparation: binary64 sums rounded once to binary32,
+ *      pow/log/exp in binary64 rounded once to binary32.
+ * workspace >= wq_workspace_bytes(WQ_OP_AWQ_SEARCH, n, k, n_alpha). */
+wq_status awq_search(const uint16_t* w, int64_t n, int64_t k, const float* a,
+                     const float* alphas_host, int n_alpha, int max_rows, int tie_mode,
+                     float* best_s, int32_t* best_idx, float* best_alpha, double* errs,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------- uintx
+ * uintx_packed_bytes: size of the packed buffer for numel codes of nbits bits:
+ * the sum over the power-of-two shards k in {4, 2, 1} present in nbits of
+ * ceil(numel / (8/k)).  Pure host arithmetic. */
+int64_t uintx_packed_bytes(int64_t numel, int nbits);
+
+/* uintx_quantize (uintx_quant.py, UIntXQuantizer._quantize_impl + pack_uintx)
+ * In:  w bf16 [n, k]; nbits in 2..7 (8 -> WQ_ERR_UNSUPPORTED, as the page's
+ *      can_quantize refuses uint8); group (the page's default 64; any multiple of
+ *      8 that divides k is accepted, 64 takes the single-pass kernel when
+ *      (n*k) % 512 == 0); w, packed 16-byte aligned.
+ * Out: packed u8 [uintx_packed_bytes(n*k, nbits)]: shards widest first; a k-bit
+ *      shard holds 8/k values per byte as 8/k contiguous chunks of
+ *      ceil(numel/(8/k)) values (chunk j in bits j*k .. j*k+k-1).
+ *      scale bf16 [n, k/group] (the page stores it as the u8 byte view of bf16);
+ *      zp u8 [n, k/group].
+ * Arithmetic in bf16: each step is the binary32 operation on bf16 operands,
+ * rounded once to bf16 (divisions are IEEE; "1.0 / scale" is a bf16 reciprocal):
+ *   scale = max((max(mx,0) - min(mn,0)) / qmax, 2^-23), zp = clamp(-round(min(mn,0)
+ *   / scale), 0, qmax), q = clamp(round(w * (1/scale)) + zp, 0, qmax). */
+wq_status uintx_quantize(const uint16_t* w, int64_t n, int64_t k, int nbits, int group,
+                         uint8_t* packed, uint16_t* scale, uint8_t* zp, void* stream);
+
+/* uintx_dequantize (uintx_quant.py, unpack_uintx + _dequantize_native)
+ * out = bf16(bf16(q - zp) * scale), as bf16 (WQ_DTYPE_BF16) or its exact binary32
+ * widening (WQ_DTYPE_F32, what dequantize() returns).  out [n, k], 16-byte
+ * aligned. */
+wq_status uintx_dequantize(const uint8_t* packed, const uint16_t* scale, const uint8_t* zp,
+                           int64_t n, int64_t k, int nbits, int group, int out_dtype, void* out,
+                           void* stream);
+
+/* ---------------------------------------------------------------- SNR
+ * quant_snr (export_gptq_cpu.py quantize_* snr; quantize_dflash_mxfp4.py main()
+ * relative error): over the whole tensor, Sw = sum w^2, Se = sum (w - deq)^2 with
+ * binary32 terms and binary64 sums;
+ *   snr_db = 20*log10(sqrt(Sw) / max(sqrt(Se), 1e-12)), rel_err = sqrt(Se)/sqrt(Sw).
+ * In:  w bf16 [n, k]; deq of dtype deq_dtype (WQ_DTYPE_F32 | WQ_DTYPE_BF16) in
+ *      layout deq_layout (WQ_LAYOUT_NK [n, k] | WQ_LAYOUT_KN [k, n]); both
+ *      16-byte aligned.
+ * Out: snr_db, rel_err: one double each on the device (either may be NULL).
+ * workspace >= wq_workspace_bytes(WQ_OP_QUANT_SNR, n, k, 0). */
+wq_status quant_snr(const uint16_t* w, const void* deq, int deq_dtype, int deq_layout, int64_t n,
+                    int64_t k, double* snr_db, double* rel_err, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WQGB300_H */

@@ -1,0 +1,91 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/wqgb300.h declares, and refuses bad arguments with the
+documented status codes before touching the GPU."""
+import ctypes
+
+import pytest
+
+import oracle
+
+wq = pytest.importorskip("weight_only_bit_group_gb300")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    return wq.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = wq.header_symbols()
+    assert len(names) >= 14
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for s in range(9):
+        assert L.wq_status_string(s)
+    assert b"sm_103a" in L.wq_version()
+
+
+def test_packed_bytes_matches_oracle(L):
+    for numel in (0, 1, 7, 8, 63, 64, 1000, 218103808):
+        for nbits in range(2, 8):
+            assert L.uintx_packed_bytes(numel, nbits) == oracle.uintx_packed_bytes(numel, nbits)
+    assert L.uintx_packed_bytes(10, 9) == -1
+
+
+def test_workspace_sizes(L):
+    assert L.wq_workspace_bytes(wq.WQ_OP_GPTQ_QUANTIZE, 4096, 4096, 128) >= 4096 * 16
+    assert L.wq_workspace_bytes(wq.WQ_OP_QUANT_SNR, 1, 1, 0) > 0
+    awq = L.wq_workspace_bytes(wq.WQ_OP_AWQ_SEARCH, 34816, 5120, 11)
+    assert awq >= 2 * 11 * 5120 * 4 + 5120 * 4
+    assert L.wq_workspace_bytes(99, 1, 1, 0) == 0
+
+
+def p(v):
+    return ctypes.c_void_p(v)
+
+
+BAD = p(0x1000)       # never dereferenced: every call below fails its checks first
+MIS = p(0x1002)       # misaligned
+
+
+def test_argument_errors_return_codes(L):
+    # shapes
+    assert L.mxfp4_quantize(BAD, 4, 48, 0, BAD, BAD, None) == 2
+    assert L.mxfp4_quantize(BAD, -1, 64, 0, BAD, BAD, None) == 2
+    assert L.gptq_quantize_sym(BAD, 12, 256, 128, BAD, BAD, BAD, BAD, None, None, 0, None) == 2
+    assert L.gptq_quantize_asym(BAD, 8, 200, 128, BAD, BAD, BAD, BAD, None, None, 0, None) == 2
+    assert L.uintx_quantize(BAD, 4, 100, 4, 64, BAD, BAD, BAD, None) == 2
+    # unsupported values (uint8 is refused as the page's can_quantize does)
+    assert L.uintx_quantize(BAD, 4, 64, 8, 64, BAD, BAD, BAD, None) == 5
+    assert L.uintx_quantize(BAD, 4, 64, 1, 64, BAD, BAD, BAD, None) == 5
+    assert L.gptq_quantize_sym(BAD, 8, 256, 96, BAD, BAD, BAD, BAD, None, None, 0, None) == 5
+    assert L.mxfp4_quantize(BAD, 4, 64, 7, BAD, BAD, None) == 5
+    # dtypes / layouts
+    assert L.mxfp4_dequantize(BAD, BAD, 4, 64, 5, BAD, None) == 3
+    assert L.quant_snr(BAD, BAD, 9, 0, 4, 64, BAD, BAD, BAD, 1 << 20, None) == 3
+    assert L.gptq_dequantize(BAD, BAD, BAD, 8, 128, 128, 1, 0, 7, BAD, None) == 5
+    # null pointers
+    assert L.mxfp4_quantize(None, 4, 64, 0, BAD, BAD, None) == 1
+    assert L.gptq_quantize_sym(BAD, 8, 128, 128, None, BAD, BAD, BAD, None, None, 0, None) == 1
+    assert L.gptq_quantize_sym(BAD, 8, 128, 128, BAD, BAD, BAD, BAD, BAD, None, 0, None) == 1
+    # misalignment
+    assert L.mxfp4_quantize(MIS, 4, 64, 0, BAD, BAD, None) == 4
+    assert L.uintx_quantize(BAD, 4, 64, 4, 64, MIS, BAD, BAD, None) == 4
+    # workspace too small
+    assert L.gptq_quantize_asym(BAD, 8, 128, 128, BAD, BAD, BAD, BAD, BAD, BAD, 16, None) == 6
+    assert L.quant_snr(BAD, BAD, 0, 0, 4, 64, BAD, BAD, BAD, 16, None) == 6
+    al = (ctypes.c_float * 2)(0.0, 1.0)
+    assert L.awq_search(BAD, 64, 64, BAD, al, 2, 16, 0, BAD, BAD, BAD, BAD, BAD, 16, None) == 6
+    assert L.awq_search(BAD, 64, 64, BAD, al, 17, 16, 0, BAD, BAD, BAD, BAD, BAD, 1 << 30, None) == 5
+
+
+def test_empty_inputs_are_ok_without_gpu(L):
+    assert L.mxfp4_quantize(None, 0, 64, 0, None, None, None) == 0
+    assert L.uintx_dequantize(None, None, None, 3, 0, 4, 64, 1, None, None) == 0
+    assert L.gptq_dequantize(None, None, None, 0, 128, 128, 1, 0, 0, None, None) == 0

@@ -1,0 +1,364 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle.
+
+Bit-exact on every packed code, zero point, E8M0 byte, fp16/bf16 scale and
+dequantized value; the SNR and the AWQ errors within 1e-4 relative; the chosen
+AWQ alpha identical.  Inputs come from the seeded generators in
+weight_only_bit_group_gb300.synth and are handed byte-identical to both sides.
+"""
+import concurrent.futures as cf
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import GOLDEN
+
+wq = pytest.importorskip("weight_only_bit_group_gb300")
+from weight_only_bit_group_gb300 import synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+REL = 1e-4  # SNR / AWQ error tolerance (relative)
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def npy(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy()
+
+
+def bf16_of_f32(a: np.ndarray) -> np.ndarray:
+    return u16(torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16))
+
+
+def pool_map(fn, items):
+    with cf.ThreadPoolExecutor(max_workers=min(len(items), os.cpu_count() or 4)) as ex:
+        return list(ex.map(fn, items))
+
+
+# ------------------------------------------------------------------ GPTQ
+def check_gptq(w: torch.Tensor, group: int, sym: bool, ref=None):
+    n, k = w.shape
+    fn = wq.gptq_quantize_sym if sym else wq.gptq_quantize_asym
+    r = fn(w.to(DEV), group=group, snr=True)
+    qw, qz, sc, gi, snr = ref if ref is not None else oracle.gptq_quantize(w, group, sym)
+    assert np.array_equal(npy(r["qweight"]), qw), "qweight"
+    assert np.array_equal(u16(r["scales"]), sc), "scales"
+    assert np.array_equal(npy(r["qzeros"]), qz), "qzeros"
+    assert np.array_equal(npy(r["g_idx"]), gi), "g_idx"
+    got = float(r["snr_db"])
+    assert abs(got - snr) <= REL * abs(snr), (got, snr)
+    return r
+
+
+@pytest.mark.parametrize("sym", [True, False])
+def test_gptq_small_config(sym):
+    """W [256, 512] ~ N(0, 0.02), group 128, plus dequant in both layouts/dtypes."""
+    w = synth.small_gptq()
+    r = check_gptq(w, 128, sym)
+    qw, qz, sc = npy(r["qweight"]), npy(r["qzeros"]), u16(r["scales"])
+    for layout in ("nk", "kn"):
+        want = oracle.gptq_dequantize(qw, qz, sc, 256, 512, 128, sym, out_kn=(layout == "kn"))
+        got = wq.gptq_dequantize(r["qweight"], r["qzeros"], r["scales"], 256, 512, 128, sym,
+                                 torch.float32, layout)
+        assert np.array_equal(npy(got), want)
+        got16 = wq.gptq_dequantize(r["qweight"], r["qzeros"], r["scales"], 256, 512, 128, sym,
+                                   torch.bfloat16, layout)
+        assert np.array_equal(u16(got16), bf16_of_f32(want))
+
+
+@pytest.mark.parametrize("group", [32, 64, 128, 256])
+@pytest.mark.parametrize("sym", [True, False])
+@pytest.mark.parametrize("shape", [(200, 768), (8, 256), (72, 1280)])
+def test_gptq_ragged_tiles(group, sym, shape):
+    """Row counts that are not multiples of the 64-row tile and K not a multiple of
+    the 256-wide tile; heavy-tailed values so groups differ widely in scale."""
+    n, k = shape
+    if k % group:
+        pytest.skip("k not a multiple of group")
+    g = torch.Generator().manual_seed(n * 7 + k + group)
+    w = (torch.randn(n, k, generator=g) * torch.exp(torch.randn(n, 1, generator=g) * 2)).to(torch.bfloat16)
+    check_gptq(w, group, sym)
+
+
+def test_gptq_hand_groups_on_gpu():
+    with open(os.path.join(GOLDEN, "gptq_hand_groups.json")) as fh:
+        cases = json.load(fh)["cases"]
+    for case in cases:
+        col = np.array(case["column"], np.float32)
+        w = torch.from_numpy(np.tile(col, (8, 1))).to(torch.bfloat16)
+        fn = wq.gptq_quantize_sym if case["sym"] else wq.gptq_quantize_asym
+        r = fn(w.to(DEV), group=case["group"], snr=False)
+        assert np.all(npy(r["qweight"]).view(np.uint32) == int(case["qweight_word"], 16)), case["name"]
+        assert np.all(u16(r["scales"]) == int(case["scale_f16"], 16)), case["name"]
+        assert np.all(npy(r["qzeros"]).view(np.uint32) == int(case["qzeros_word"], 16)), case["name"]
+
+
+def test_gptq_degenerate_groups():
+    """Constant, all-zero, single-outlier and tiny (subnormal-bf16) groups."""
+    rows = []
+    rows.append(np.zeros(256))
+    rows.append(np.full(256, 0.5))
+    rows.append(np.full(256, -0.25))
+    r = np.zeros(256); r[3] = 7.0; rows.append(r)
+    r = np.zeros(256); r[100] = -3.0; rows.append(r)
+    rows.append(np.full(256, 2.0 ** -130))
+    rows.append(np.linspace(-1e-8, 1e-8, 256))
+    rows.append(np.linspace(1e30, 2e30, 256))
+    w = torch.from_numpy(np.stack(rows).astype(np.float32)).to(torch.bfloat16)
+    for sym in (True, False):
+        fn = wq.gptq_quantize_sym if sym else wq.gptq_quantize_asym
+        res = fn(w.to(DEV), group=128, snr=False)
+        qw, qz, sc, gi, _ = oracle.gptq_quantize(w, 128, sym)
+        assert np.array_equal(npy(res["qweight"]), qw)
+        assert np.array_equal(u16(res["scales"]), sc)
+        assert np.array_equal(npy(res["qzeros"]), qz)
+
+
+def test_gptq_layer_full_size_asym():
+    """The seven projections of one layer (218,103,808 weights, outlier columns)
+    at full size, asym group 128 -- the configuration the benchmark times."""
+    layer = synth.gptq_layer(device="cpu")
+    refs = pool_map(lambda t: oracle.gptq_quantize(t[1], 128, False), layer)
+    for (name, w), ref in zip(layer, refs):
+        check_gptq(w, 128, False, ref)
+
+
+def test_gptq_layer_full_size_sym_sampled():
+    """Sym on the full layer: the GPU runs the whole tensors; the oracle checks a
+    sample of 64 output channels (columns of qweight) per tensor."""
+    layer = synth.gptq_layer(device="cpu")
+    rng = np.random.default_rng(0)
+    for name, w in layer:
+        n, k = w.shape
+        r = wq.gptq_quantize_sym(w.to(DEV), group=128, snr=True)
+        blocks = rng.choice(n // 8, size=8, replace=False)
+        cols = np.concatenate([np.arange(8 * b, 8 * b + 8) for b in blocks])
+        qw, qz, sc, gi, _ = oracle.gptq_quantize(w[cols], 128, True)
+        assert np.array_equal(npy(r["qweight"])[:, cols], qw), name
+        assert np.array_equal(u16(r["scales"])[:, cols], sc), name
+        assert np.all(npy(r["qzeros"]).view(np.uint32) == 0x77777777)
+        # whole-tensor SNR from the oracle's own dequant of the GPU's stored tensors
+        # is a different quantity (fp16 scales); the fused SNR is checked in the
+        # asym test and on the small configs.
+
+
+# ------------------------------------------------------------------ MXFP4
+def check_mxfp4(w: torch.Tensor, tie_mode: int, ref=None):
+    packed, e8 = wq.mxfp4_quantize(w.to(DEV), tie_mode)
+    p_ref, e_ref = ref if ref is not None else oracle.mxfp4_quantize(w, tie_mode)
+    assert np.array_equal(npy(e8), e_ref), "e8m0"
+    assert np.array_equal(npy(packed), p_ref), "packed"
+    return packed, e8, p_ref, e_ref
+
+
+@pytest.mark.parametrize("tie_mode", [0, 1])
+def test_mxfp4_tie_blocks(tie_mode):
+    w = synth.mxfp4_tie_rows()
+    packed, e8, p_ref, e_ref = check_mxfp4(w, tie_mode)
+    out = wq.mxfp4_dequantize(packed, e8, torch.float32)
+    assert np.array_equal(npy(out), oracle.mxfp4_dequantize(p_ref, e_ref))
+
+
+@pytest.mark.parametrize("tie_mode", [0, 1])
+def test_mxfp4_edge_blocks(tie_mode):
+    """Zero blocks, -0.0, bf16 subnormals (exponent clamp at -127), the largest
+    bf16 values, values on every grid point and every midpoint."""
+    rows = []
+    rows.append(np.zeros(64))
+    rows.append(-np.zeros(64))
+    rows.append(np.full(64, 2.0 ** -133) * np.arange(64))
+    rows.append(np.full(64, 3.0e38) * np.where(np.arange(64) % 2, 1, -1))
+    grid = np.array([0, .25, .5, .75, 1, 1.25, 1.5, 1.75, 2, 2.5, 3, 3.5, 4, 5, 6, 7.5])
+    rows.append(np.concatenate([grid, -grid, grid * 2.0 ** -100, -grid * 2.0 ** 100]))
+    w = torch.from_numpy(np.stack(rows).astype(np.float32)).to(torch.bfloat16)
+    check_mxfp4(w, tie_mode)
+
+
+def test_mxfp4_full_size_and_dequant():
+    """gate_up [34816, 5120] with 1% of blocks x50, full tensor, both dequant dtypes."""
+    w = synth.mxfp4_gate_up(device="cpu")
+    n, k = w.shape
+    chunks = [(i, min(i + 4352, n)) for i in range(0, n, 4352)]
+    refs = pool_map(lambda c: oracle.mxfp4_quantize(w[c[0]:c[1]]), chunks)
+    p_ref = np.concatenate([r[0] for r in refs])
+    e_ref = np.concatenate([r[1] for r in refs])
+    packed, e8, _, _ = check_mxfp4(w, 0, (p_ref, e_ref))
+    out32 = npy(wq.mxfp4_dequantize(packed, e8, torch.float32))
+    out16 = u16(wq.mxfp4_dequantize(packed, e8, torch.bfloat16))
+    for lo, hi in chunks[:: 3]:
+        want = oracle.mxfp4_dequantize(p_ref[lo:hi], e_ref[lo:hi])
+        assert np.array_equal(out32[lo:hi], want)
+        assert np.array_equal(out16[lo:hi], bf16_of_f32(want))
+
+
+def test_mxfp4_dequant_all_bytes():
+    """Every packed byte with every e8m0 value (255 included: inf, and NaN for
+    zero codes)."""
+    packed = np.tile(np.arange(256, dtype=np.uint8), (256, 1))  # [256, 256] -> k = 512
+    e8 = np.repeat(np.arange(256, dtype=np.uint8)[:, None], 16, axis=1)
+    want = oracle.mxfp4_dequantize(packed, e8)
+    got = npy(wq.mxfp4_dequantize(torch.from_numpy(packed).to(DEV), torch.from_numpy(e8).to(DEV),
+                                  torch.float32))
+    same = (got.view(np.uint32) == want.view(np.uint32)) | (np.isnan(got) & np.isnan(want))
+    assert same.all()
+    got16 = u16(wq.mxfp4_dequantize(torch.from_numpy(packed).to(DEV), torch.from_numpy(e8).to(DEV),
+                                    torch.bfloat16))
+    w16 = oracle.bf16_bits_to_f32(got16)
+    same = (w16.view(np.uint32) == want.view(np.uint32)) | (np.isnan(w16) & np.isnan(want))
+    assert same.all()
+
+
+# ------------------------------------------------------------------ uintx
+def check_uintx(w: torch.Tensor, nbits: int, group: int = 64, ref=None):
+    n, k = w.shape
+    packed, scale, zp = wq.uintx_quantize(w.to(DEV), nbits, group)
+    p_ref, s_ref, z_ref, _ = ref if ref is not None else oracle.uintx_quantize(w, nbits, group)
+    assert np.array_equal(u16(scale), s_ref), "scale"
+    assert np.array_equal(npy(zp), z_ref), "zp"
+    assert np.array_equal(npy(packed), p_ref), "packed"
+    return packed, scale, zp, p_ref, s_ref, z_ref
+
+
+@pytest.mark.parametrize("nbits", [2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("shape,group", [((64, 512), 64), ((9, 192), 64), ((3, 64), 64),
+                                         ((40, 96), 32), ((5, 24), 8)])
+def test_uintx_shapes(nbits, shape, group):
+    """Fused single-pass path (numel % 512 == 0, group 64) and the general path
+    (ragged numel, other groups), quantize and dequantize in both dtypes."""
+    n, k = shape
+    g = torch.Generator().manual_seed(nbits * 1000 + n + k)
+    w = (torch.randn(n, k, generator=g) * 0.02 * torch.exp(torch.randn(n, 1, generator=g))).to(torch.bfloat16)
+    packed, scale, zp, p_ref, s_ref, z_ref = check_uintx(w, nbits, group)
+    want = oracle.uintx_dequantize(p_ref, s_ref, z_ref, n, k, nbits, group)
+    got = wq.uintx_dequantize(packed, scale, zp, n, k, nbits, group, torch.bfloat16)
+    assert np.array_equal(u16(got), want)
+    got32 = wq.uintx_dequantize(packed, scale, zp, n, k, nbits, group, torch.float32)
+    assert np.array_equal(npy(got32), oracle.bf16_bits_to_f32(want))
+
+
+def test_uintx_hand_groups_on_gpu():
+    with open(os.path.join(GOLDEN, "uintx_hand.json")) as fh:
+        g = json.load(fh)
+    cases = [g["quant_case"]] + g["rounding_point_cases"]
+    for c in cases:
+        vals = c["values_first"] + [c["rest_of_group"]] * (c["group"] - len(c["values_first"]))
+        w = torch.tensor([vals] * 8, dtype=torch.float32).to(torch.bfloat16)  # 512 values: fused path
+        packed, scale, zp = wq.uintx_quantize(w.to(DEV), c["nbits"], c["group"])
+        assert np.all(u16(scale) == int(c["scale_bits"], 16))
+        assert np.all(npy(zp) == c["zp"])
+        codes = oracle.uintx_unpack(npy(packed), c["nbits"], 8 * c["group"]).reshape(8, -1)
+        want = c["codes_first"] + [c["code_rest"]] * (c["group"] - len(c["codes_first"]))
+        assert np.all(codes == np.array(want, np.uint8))
+
+
+def test_uintx_degenerate_groups():
+    rows = [np.zeros(64), np.linspace(0.01, 0.5, 64), -np.linspace(0.01, 0.5, 64),
+            np.full(64, 1e-30), np.linspace(-3e38, 3e38, 64), np.full(64, 2.0 ** -133)]
+    general = torch.from_numpy(np.stack(rows * 2).astype(np.float32)).to(torch.bfloat16)  # 768 values
+    fused = torch.from_numpy(np.stack(rows + rows[:2]).astype(np.float32)).to(torch.bfloat16)  # 512
+    for nbits in (2, 5, 7):
+        check_uintx(general, nbits)
+        check_uintx(fused, nbits)
+
+
+@pytest.mark.parametrize("nbits", [2, 3, 4, 5, 6, 7])
+def test_uintx_layer_full_size(nbits):
+    """One full layer of the 8-layer uintx workload per nbits (218 M weights)."""
+    layer = synth.uintx_layers(n_layers=1, seed=5 + nbits)
+    refs = pool_map(lambda t: oracle.uintx_quantize(t[1], nbits), layer)
+    for (name, w), ref in zip(layer, refs):
+        n, k = w.shape
+        packed, scale, zp, p_ref, s_ref, z_ref = check_uintx(w, nbits, 64, ref)
+        if name.endswith(("k_proj", "down_proj")):
+            want = oracle.uintx_dequantize(p_ref, s_ref, z_ref, n, k, nbits)
+            got = wq.uintx_dequantize(packed, scale, zp, n, k, nbits)
+            assert np.array_equal(u16(got), want), name
+
+
+# ------------------------------------------------------------------ SNR
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_quant_snr(layout, dtype):
+    g = torch.Generator().manual_seed(3)
+    for n, k in ((256, 512), (200, 328), (8, 8)):
+        w = (torch.randn(n, k, generator=g) * 0.02).to(torch.bfloat16)
+        deq = (w.float() + torch.randn(n, k, generator=g) * 1e-3)
+        deq = deq.to(dtype)
+        d = deq if layout == "nk" else deq.t().contiguous()
+        snr, rel = wq.quant_snr(w.to(DEV), d.to(DEV), layout)
+        dn = u16(d) if dtype == torch.bfloat16 else npy(d)
+        s_ref, r_ref = oracle.quant_snr(w, dn, deq_kn=(layout == "kn"))
+        assert abs(float(snr) - s_ref) <= REL * abs(s_ref)
+        assert abs(float(rel) - r_ref) <= REL * abs(r_ref)
+
+
+def test_quant_snr_full_layer_gptq_pipeline():
+    """Stored-tensor SNR: quant_snr(w, gptq_dequantize(...)) on the down projection."""
+    name, w = synth.gptq_layer(device="cpu")[-1]
+    n, k = w.shape
+    r = wq.gptq_quantize_asym(w.to(DEV), 128, snr=False)
+    deq = wq.gptq_dequantize(r["qweight"], r["qzeros"], r["scales"], n, k, 128, False,
+                             torch.float32, "kn")
+    snr, rel = wq.quant_snr(w.to(DEV), deq, "kn")
+    s_ref, r_ref = oracle.quant_snr(w, npy(deq), deq_kn=True)
+    assert abs(float(snr) - s_ref) <= REL * abs(s_ref)
+    assert abs(float(rel) - r_ref) <= REL * abs(r_ref)
+
+
+# ------------------------------------------------------------------ AWQ
+def check_awq(w, a, alphas, max_rows, tie_mode=0):
+    best_s, bi, ba, errs = wq.awq_search(w.to(DEV), a.to(DEV), alphas, max_rows, tie_mode)
+    s_ref, bi_ref, ba_ref, e_ref = oracle.awq_search(w, a.numpy(), alphas, max_rows, tie_mode)
+    e = npy(errs)
+    np.testing.assert_allclose(e, e_ref, rtol=REL, atol=0)
+    order = np.sort(e_ref)
+    margin = (order[1] - order[0]) / order[0] if len(order) > 1 and order[0] > 0 else 1.0
+    if margin > 1e-6:  # a near-tie between the two best alphas is reported, not failed
+        assert int(bi) == bi_ref and float(ba) == ba_ref
+        np.testing.assert_allclose(npy(best_s), s_ref, rtol=2e-7, atol=0)
+    return int(bi), margin
+
+
+def test_awq_small_and_literal_ties():
+    g = torch.Generator().manual_seed(9)
+    w = (torch.randn(300, 256, generator=g) * 0.02).to(torch.bfloat16)
+    a = torch.randn(256, generator=g).exp()
+    check_awq(w, a, synth.ALPHAS, 64, 0)
+    check_awq(w, a, synth.ALPHAS, 64, 1)
+    check_awq(w, torch.full((256,), 0.7), synth.ALPHAS, 64, 0)  # all errors equal -> alpha 0
+
+
+def test_awq_full_size():
+    """W = the gate_up tensor [34816, 5120], LogNormal(0,1) activations,
+    alpha grid 0.0..1.0 -> strided subsample of 2048 rows (stride 17)."""
+    w = synth.mxfp4_gate_up(device="cpu")
+    a = synth.awq_activation()
+    bi, margin = check_awq(w, a, synth.ALPHAS, 2048, 0)
+    print(f"awq best alpha index {bi}, relative margin to the runner-up {margin:.3e}")
+
+
+# ------------------------------------------------------------------ ABI edge cases
+def test_empty_inputs_launch_nothing():
+    L = wq.lib()
+    assert L.mxfp4_quantize(None, 0, 64, 0, None, None, None) == 0
+    assert L.uintx_quantize(None, 0, 64, 4, 64, None, None, None, None) == 0
+    assert L.gptq_quantize_sym(None, 0, 128, 128, None, None, None, None, None, None, 0, None) == 0
+    assert L.gptq_dequantize(None, None, None, 8, 0, 128, 1, 0, 0, None, None) == 0
+
+
+def test_misaligned_pointer_is_refused():
+    w = torch.zeros(1, 72, dtype=torch.bfloat16, device=DEV)
+    out = torch.zeros(64, dtype=torch.uint8, device=DEV)
+    e8 = torch.zeros(2, dtype=torch.uint8, device=DEV)
+    L = wq.lib()
+    import ctypes
+    st = L.mxfp4_quantize(ctypes.c_void_p(w.data_ptr() + 2), 1, 64, 0, ctypes.c_void_p(out.data_ptr()),
+                          ctypes.c_void_p(e8.data_ptr()), None)
+    assert st == 4  # WQ_ERR_MISALIGNED, nothing launched

@@ -1,0 +1,188 @@
+// mxfp4.cu -- OCP MXFP4 quantize / dequantize (quantize_dflash_mxfp4.py:
+// E2M1 table, GROUP = 32, quantize_mxfp4, dequantize_mxfp4).
+//
+// Layout: k % 32 == 0, so the 32-value blocks of a row-major [n, k] matrix are
+// consecutive in memory and the whole matrix is a flat stream of blocks.  One
+// thread takes one 16-byte chunk (8 bf16 values), four lanes make one block:
+//   load   uint4 (8 bf16)                -> 16 B per lane, 512 B per warp
+//   amax   16-bit SIMD max of |bf16| bit patterns, 2 shuffles over 4 lanes
+//   code   v = w * 2^-exp (exact), hardware cvt to e2m1x2 (round half even,
+//          saturate at 6) -- the e2m1 encoding IS the page's magnitude index
+//   store  one uint32 of 8 nibbles per lane (128 B per warp), one e8m0 byte per
+//          block.
+// HBM bound: 2 B read + 0.53 B written per weight.
+#include "wq_common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;  // independent 16-byte chunks in flight per thread
+
+// exp = clamp(floor(log2(amax)) - 2, -127, 127), 0 for amax == 0, from the
+// 15-bit magnitude pattern of a bf16 amax.  A bf16 subnormal has
+// floor(log2) <= -127 so it always clamps.
+__device__ __forceinline__ int exp_from_bf16_mag(uint32_t a) {
+    uint32_t ef = a >> 7;
+    if (ef == 0) return a == 0 ? 0 : -127;
+    int e = (int)ef - 129;
+    return e < -127 ? -127 : e;
+}
+
+// Two binary32 -> two e2m1 nibbles, round to nearest even, saturating at +-6.
+// `lo` lands in bits 0..3, `hi` in bits 4..7 (the first source operand of the
+// cvt goes to the upper nibble).
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+    uint16_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+        : "=h"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Page-literal tie rewrite: exact midpoints 0.75, 1.75 and 3.5 go two grid steps
+// down from the half-even choice ((argmin // 2) * 2 with argmin the lower
+// neighbour); the other midpoints already agree with half-even.
+__device__ __forceinline__ uint32_t page_tie(uint32_t nib, float v) {
+    float m = fabsf(v);
+    return (m == 0.75f || m == 1.75f || m == 3.5f) ? nib - 2u : nib;
+}
+
+template <int TIE>
+__device__ __forceinline__ uint32_t code_pair(float x0, float x1, float inv) {
+    float a0 = __fmul_rn(x0, inv), a1 = __fmul_rn(x1, inv);
+    uint32_t b = e2m1x2(a0, a1);
+    if (TIE == WQ_TIE_PAGE_LITERAL) b = page_tie(b & 15u, a0) | (page_tie(b >> 4, a1) << 4);
+    return b;
+}
+
+template <int TIE>
+__global__ void __launch_bounds__(kThreads) mxfp4_quant_kernel(const uint4* __restrict__ w,
+                                                               int64_t nchunks,
+                                                               uint32_t* __restrict__ packed,
+                                                               uint8_t* __restrict__ e8m0) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+    // Every lane of a warp runs the same trip count (shuffles below); lanes past
+    // the end compute on zeros and store nothing.  nchunks % 4 == 0 and chunk
+    // indices are 4-aligned per lane quad, so a quad is all-valid or all-invalid.
+    for (int64_t wb = warp * 32; wb < nchunks; wb += nwarps * 32 * kUnroll) {
+        uint4 v[kUnroll];
+        int64_t ch[kUnroll];
+#pragma unroll
+        for (int j = 0; j < kUnroll; ++j) {
+            ch[j] = wb + (int64_t)j * nwarps * 32 + lane;
+            v[j] = ch[j] < nchunks ? wq::ld_stream(w + ch[j]) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < kUnroll; ++j) {
+            const uint32_t M = 0x7fff7fffu;
+            uint32_t m2 = __vmaxu2(__vmaxu2(v[j].x & M, v[j].y & M), __vmaxu2(v[j].z & M, v[j].w & M));
+            uint32_t a = max(m2 & 0xffffu, m2 >> 16);
+            a = max(a, wq::shfl_xor(a, 1));
+            a = max(a, wq::shfl_xor(a, 2));
+            const int ex = exp_from_bf16_mag(a);
+            const float inv = __uint_as_float((uint32_t)(127 - ex) << 23);  // 2^-exp, normal
+            uint32_t word = code_pair<TIE>(wq::bf_lo(v[j].x), wq::bf_hi(v[j].x), inv);
+            word |= code_pair<TIE>(wq::bf_lo(v[j].y), wq::bf_hi(v[j].y), inv) << 8;
+            word |= code_pair<TIE>(wq::bf_lo(v[j].z), wq::bf_hi(v[j].z), inv) << 16;
+            word |= code_pair<TIE>(wq::bf_lo(v[j].w), wq::bf_hi(v[j].w), inv) << 24;
+            if (ch[j] < nchunks) {
+                packed[ch[j]] = word;
+                if ((lane & 3) == 0) e8m0[ch[j] >> 2] = (uint8_t)(ex + 127);
+            }
+        }
+    }
+}
+
+// Two e2m1 nibbles of one byte -> two binary32 magnitudes with sign (exact).
+__device__ __forceinline__ void e2m1x2_to_f(uint32_t byte, float& lo, float& hi) {
+    uint32_t h2;
+    uint16_t in = (uint16_t)byte;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "h"(in));
+    lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+    hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+}
+
+// 2^(e - 127) in binary32: e = 0 is the subnormal 2^-127, e = 255 is inf
+// (as exp2(128.0) is in binary32).
+__device__ __forceinline__ float e8m0_scale(uint32_t e) {
+    return __uint_as_float(e == 0 ? 0x00400000u : (e << 23));
+}
+
+template <int OUT_BF16>
+__global__ void __launch_bounds__(kThreads) mxfp4_dequant_kernel(const uint32_t* __restrict__ packed,
+                                                                 const uint8_t* __restrict__ e8m0,
+                                                                 int64_t nchunks, void* __restrict__ out) {
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t c = (int64_t)blockIdx.x * kThreads + threadIdx.x; c < nchunks; c += stride) {
+        const uint32_t word = __ldg(packed + c);
+        const float s = e8m0_scale(__ldg(e8m0 + (c >> 2)));
+        float f[8];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            float lo, hi;
+            e2m1x2_to_f((word >> (8 * p)) & 0xffu, lo, hi);
+            f[2 * p] = __fmul_rn(lo, s);
+            f[2 * p + 1] = __fmul_rn(hi, s);
+        }
+        if (OUT_BF16) {
+            uint4 o;
+            o.x = wq::f2_to_bf2(f[0], f[1]);
+            o.y = wq::f2_to_bf2(f[2], f[3]);
+            o.z = wq::f2_to_bf2(f[4], f[5]);
+            o.w = wq::f2_to_bf2(f[6], f[7]);
+            reinterpret_cast<uint4*>(out)[c] = o;
+        } else {
+            float4* o = reinterpret_cast<float4*>(out) + 2 * c;
+            o[0] = make_float4(f[0], f[1], f[2], f[3]);
+            o[1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
+    }
+}
+
+}  // namespace
+
+extern "C" wq_status mxfp4_quantize(const uint16_t* w, int64_t n, int64_t k, int tie_mode,
+                                    uint8_t* packed, uint8_t* e8m0, void* stream) {
+    if (n < 0 || k < 0 || k % 32 != 0) return WQ_ERR_BAD_SHAPE;
+    if (tie_mode != WQ_TIE_HALF_EVEN && tie_mode != WQ_TIE_PAGE_LITERAL) return WQ_ERR_UNSUPPORTED;
+    if (n == 0 || k == 0) return WQ_OK;
+    if (!w || !packed || !e8m0) return WQ_ERR_NULL_PTR;
+    if (!wqh::aligned16(w) || !wqh::aligned16(packed)) return WQ_ERR_MISALIGNED;
+    const int64_t nchunks = n * k / 8;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (tie_mode == WQ_TIE_HALF_EVEN) {
+        int grid = wqh::grid_for((const void*)mxfp4_quant_kernel<WQ_TIE_HALF_EVEN>, kThreads, 0,
+                                 (nchunks + kThreads - 1) / kThreads, 1 << 30);
+        mxfp4_quant_kernel<WQ_TIE_HALF_EVEN><<<grid, kThreads, 0, st>>>(
+            (const uint4*)w, nchunks, (uint32_t*)packed, e8m0);
+    } else {
+        int grid = wqh::grid_for((const void*)mxfp4_quant_kernel<WQ_TIE_PAGE_LITERAL>, kThreads, 0,
+                                 (nchunks + kThreads - 1) / kThreads, 1 << 30);
+        mxfp4_quant_kernel<WQ_TIE_PAGE_LITERAL><<<grid, kThreads, 0, st>>>(
+            (const uint4*)w, nchunks, (uint32_t*)packed, e8m0);
+    }
+    return wqh::check_launch();
+}
+
+extern "C" wq_status mxfp4_dequantize(const uint8_t* packed, const uint8_t* e8m0, int64_t n,
+                                      int64_t k, int out_dtype, void* out, void* stream) {
+    if (n < 0 || k < 0 || k % 32 != 0) return WQ_ERR_BAD_SHAPE;
+    if (out_dtype != WQ_DTYPE_F32 && out_dtype != WQ_DTYPE_BF16) return WQ_ERR_BAD_DTYPE;
+    if (n == 0 || k == 0) return WQ_OK;
+    if (!packed || !e8m0 || !out) return WQ_ERR_NULL_PTR;
+    if (!wqh::aligned16(packed) || !wqh::aligned16(out)) return WQ_ERR_MISALIGNED;
+    const int64_t nchunks = n * k / 8;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (out_dtype == WQ_DTYPE_BF16) {
+        int grid = wqh::grid_for((const void*)mxfp4_dequant_kernel<1>, kThreads, 0,
+                                 (nchunks + kThreads - 1) / kThreads, 1 << 30);
+        mxfp4_dequant_kernel<1><<<grid, kThreads, 0, st>>>((const uint32_t*)packed, e8m0, nchunks, out);
+    } else {
+        int grid = wqh::grid_for((const void*)mxfp4_dequant_kernel<0>, kThreads, 0,
+                                 (nchunks + kThreads - 1) / kThreads, 1 << 30);
+        mxfp4_dequant_kernel<0><<<grid, kThreads, 0, st>>>((const uint32_t*)packed, e8m0, nchunks, out);
+    }
+    return wqh::check_launch();
+}

@@ -1,0 +1,510 @@
+// uintx.cu -- affine uintx quantization with power-of-two bit-shard packing and
+// its inverse (uintx_quant.py: module docstring, _pack_shard, pack_uintx,
+// unpack_uintx, UIntXQuantizer._quantize_impl, _dequantize_native).
+//
+// Shard geometry.  numel = n*k is a multiple of 8 (group % 8 == 0 divides k), so
+// with L1 = numel/8 the 1-bit shard has L1 bytes, the 2-bit shard 2*L1 and the
+// 4-bit shard 4*L1.  Byte i of the 1-bit shard takes element i + j*L1 (j < 8) as
+// bit j; byte h*L1 + d of the 2-bit shard takes elements (2jj + h)*L1 + d (jj < 4)
+// at bits 2jj; byte m*L1 + d of the 4-bit shard takes elements m*L1 + d and
+// (m+4)*L1 + d.  Hence one thread that holds, for 8 consecutive positions d, the
+// codes of all 8 "segments" m*L1 + d (m < 8) completes every shard byte of those
+// positions in registers: one read of w, no atomics, 8-byte coalesced stores.
+//
+// Fused path (group 64, numel % 512 == 0, so segment starts are group-aligned):
+// a warp takes 256 consecutive positions d; lane l holds d = d0 + 8l .. 8l+7 of
+// all 8 segments (8 coalesced 16-byte loads).  The 8 lanes of an octet together
+// hold 8 whole groups (one per segment): a 3-round reduce-scatter leaves lane c
+// with the min/max of segment c's group, lane c derives that group's bf16
+// qparams (once per group) and an 8-shuffle all-gather hands every lane the
+// (1/scale, zp) of all 8 groups.
+//
+// bf16 arithmetic: every page step is the binary32 operation on bf16 operands
+// rounded once to bf16 (cvt.rn).  w * (1/scale) is an exact binary32 product of
+// two bf16 values, so rounding it with cvt.rn.bf16 reproduces the bf16 multiply.
+#include "wq_common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+
+struct QParams {
+    uint32_t scale_bits;  // bf16 bits of the scale
+    uint32_t inv_bits;    // bf16 bits of 1/scale
+    uint32_t zp;
+};
+
+// choose_qparams_affine as the page states it, in bf16 (preserve_zero, eps =
+// binary32 eps, integer zero point).
+template <int QMAX>
+__device__ __forceinline__ QParams qparams(float mn, float mx) {
+    const float mnn = fminf(mn, 0.0f), mxp = fmaxf(mx, 0.0f);
+    float sc = wq::bfr(__fsub_rn(mxp, mnn));
+    sc = wq::bfr(__fdiv_rn(sc, (float)QMAX));
+    sc = fmaxf(sc, 0x1p-23f);
+    const float ratio = wq::bfr(__fdiv_rn(mnn, sc));
+    float zpf = wq::bfr(__fsub_rn(0.0f, rintf(ratio)));
+    zpf = fminf(fmaxf(zpf, 0.0f), (float)QMAX);
+    QParams p;
+    p.scale_bits = wq::f_to_bf(sc);
+    p.inv_bits = wq::f_to_bf(__fdiv_rn(1.0f, sc));
+    p.zp = (uint32_t)zpf;
+    return p;
+}
+
+// Codes of two bf16 weights (packed in u) for one group: q = clamp(round(bf16(w *
+// inv)) + zp, 0, qmax); the clamp is applied before rounding (integer bounds).
+template <int QMAX>
+__device__ __forceinline__ uint32_t code2(uint32_t u, float inv, float lo, float hi, uint32_t zp) {
+    const uint32_t p2 = wq::f2_to_bf2(__fmul_rn(wq::bf_lo(u), inv), __fmul_rn(wq::bf_hi(u), inv));
+    const float p0 = fminf(fmaxf(wq::bf_lo(p2), lo), hi);
+    const float p1 = fminf(fmaxf(wq::bf_hi(p2), lo), hi);
+    const uint32_t c0 = (uint32_t)(__float_as_int(__fadd_rn(p0, kMagic)) - 0x4B400000) + zp;
+    const uint32_t c1 = (uint32_t)(__float_as_int(__fadd_rn(p1, kMagic)) - 0x4B400000) + zp;
+    return c0 | (c1 << 8);  // two code bytes
+}
+
+template <int NBITS>
+struct Shards {
+    static constexpr bool has4 = (NBITS & 4) != 0;
+    static constexpr bool has2 = (NBITS & 2) != 0;
+    static constexpr bool has1 = (NBITS & 1) != 0;
+    static constexpr int off2 = has4 ? 4 : 0;
+    static constexpr int off1 = (has4 ? 4 : 0) + (has2 ? 2 : 0);
+};
+
+// Build and store every shard byte of 8 positions d .. d+7 from the code bytes
+// B[m] (8 bytes: codes of elements m*L1 + d .. d+7).
+template <int NBITS>
+__device__ __forceinline__ void store_shards(const uint32_t (&blo)[8], const uint32_t (&bhi)[8],
+                                             uint8_t* __restrict__ packed, int64_t numel,
+                                             int64_t L1, int64_t d) {
+    using S = Shards<NBITS>;
+    const int64_t base2 = S::has4 ? numel / 2 : 0;
+    const int64_t base1 = base2 + (S::has2 ? numel / 4 : 0);
+    if (S::has4) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            uint2 o;
+            o.x = (blo[m] & 0x0F0F0F0Fu) | ((blo[m + 4] & 0x0F0F0F0Fu) << 4);
+            o.y = (bhi[m] & 0x0F0F0F0Fu) | ((bhi[m + 4] & 0x0F0F0F0Fu) << 4);
+            *reinterpret_cast<uint2*>(packed + m * L1 + d) = o;
+        }
+    }
+    if (S::has2) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint2 o = make_uint2(0, 0);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                o.x |= ((blo[2 * jj + h] >> S::off2) & 0x03030303u) << (2 * jj);
+                o.y |= ((bhi[2 * jj + h] >> S::off2) & 0x03030303u) << (2 * jj);
+            }
+            *reinterpret_cast<uint2*>(packed + base2 + h * L1 + d) = o;
+        }
+    }
+    if (S::has1) {
+        uint2 o = make_uint2(0, 0);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            o.x |= ((blo[m] >> S::off1) & 0x01010101u) << m;
+            o.y |= ((bhi[m] >> S::off1) & 0x01010101u) << m;
+        }
+        *reinterpret_cast<uint2*>(packed + base1 + d) = o;
+    }
+}
+
+template <int NBITS>
+__global__ void __launch_bounds__(kThreads) uintx_quant_fused(const uint16_t* __restrict__ w,
+                                                              int64_t numel, uint8_t* __restrict__ packed,
+                                                              uint16_t* __restrict__ scale,
+                                                              uint8_t* __restrict__ zp) {
+    constexpr int QMAX = (1 << NBITS) - 1;
+    const int64_t L1 = numel / 8;  // multiple of 64
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+    const int64_t items = (L1 + 255) / 256;
+
+    for (int64_t it = warp; it < items; it += nwarps) {
+        const int64_t d0 = it * 256, d = d0 + 8 * lane;
+        const bool valid = d < L1;  // uniform over an octet (64 positions)
+        uint4 v[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+            v[m] = valid ? wq::ld_stream(w + m * L1 + d) : make_uint4(0, 0, 0, 0);
+
+        float mn[8], mx[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            float x[8] = {wq::bf_lo(v[m].x), wq::bf_hi(v[m].x), wq::bf_lo(v[m].y), wq::bf_hi(v[m].y),
+                          wq::bf_lo(v[m].z), wq::bf_hi(v[m].z), wq::bf_lo(v[m].w), wq::bf_hi(v[m].w)};
+            float a = x[0], b = x[0];
+#pragma unroll
+            for (int j = 1; j < 8; ++j) { a = fminf(a, x[j]); b = fmaxf(b, x[j]); }
+            mn[m] = a;
+            mx[m] = b;
+        }
+        // reduce-scatter over the octet: lane c ends with segment c's group
+        float k4n[4], k4x[4];
+        {
+            const bool hb = lane & 4;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float sn = hb ? mn[j] : mn[j + 4], sx = hb ? mx[j] : mx[j + 4];
+                const float rn = wq::shfl_xor(sn, 4), rx = wq::shfl_xor(sx, 4);
+                k4n[j] = fminf(hb ? mn[j + 4] : mn[j], rn);
+                k4x[j] = fmaxf(hb ? mx[j + 4] : mx[j], rx);
+            }
+        }
+        float k2n[2], k2x[2];
+        {
+            const bool hb = lane & 2;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float sn = hb ? k4n[j] : k4n[j + 2], sx = hb ? k4x[j] : k4x[j + 2];
+                const float rn = wq::shfl_xor(sn, 2), rx = wq::shfl_xor(sx, 2);
+                k2n[j] = fminf(hb ? k4n[j + 2] : k4n[j], rn);
+                k2x[j] = fmaxf(hb ? k4x[j + 2] : k4x[j], rx);
+            }
+        }
+        float gmn, gmx;
+        {
+            const bool hb = lane & 1;
+            const float sn = hb ? k2n[0] : k2n[1], sx = hb ? k2x[0] : k2x[1];
+            const float rn = wq::shfl_xor(sn, 1), rx = wq::shfl_xor(sx, 1);
+            gmn = fminf(hb ? k2n[1] : k2n[0], rn);
+            gmx = fmaxf(hb ? k2x[1] : k2x[0], rx);
+        }
+        const int c = lane & 7;
+        const QParams qp = qparams<QMAX>(gmn, gmx);
+        if (valid) {
+            const int64_t g = (c * L1 + d0) / 64 + (lane >> 3);
+            scale[g] = (uint16_t)qp.scale_bits;
+            zp[g] = (uint8_t)qp.zp;
+        }
+        const uint32_t mine = qp.inv_bits | (qp.zp << 16);
+
+        uint32_t blo[8], bhi[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const uint32_t P = __shfl_sync(0xffffffffu, mine, (lane & ~7) | m);
+            const float inv = wq::bf_to_f(P & 0xffffu);
+            const uint32_t z = P >> 16;
+            const float lo = -(float)z, hi = (float)(QMAX - (int)z);
+            const uint32_t c01 = code2<QMAX>(v[m].x, inv, lo, hi, z);
+            const uint32_t c23 = code2<QMAX>(v[m].y, inv, lo, hi, z);
+            const uint32_t c45 = code2<QMAX>(v[m].z, inv, lo, hi, z);
+            const uint32_t c67 = code2<QMAX>(v[m].w, inv, lo, hi, z);
+            blo[m] = c01 | (c23 << 16);
+            bhi[m] = c45 | (c67 << 16);
+        }
+        if (valid) store_shards<NBITS>(blo, bhi, packed, numel, L1, d);
+    }
+}
+
+// ----------------------------------------------------------- general path
+// (any group % 8 == 0 dividing k; numel % 8 == 0)
+
+template <int QMAX>
+__global__ void __launch_bounds__(kThreads) uintx_qparams_kernel(const uint16_t* __restrict__ w,
+                                                                 int64_t ngroups, int group,
+                                                                 uint16_t* __restrict__ scale,
+                                                                 uint8_t* __restrict__ zp) {
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < ngroups; g += stride) {
+        const uint4* p = reinterpret_cast<const uint4*>(w + g * group);
+        float a = INFINITY, b = -INFINITY;
+        for (int i = 0; i < group / 8; ++i) {
+            const uint4 u = __ldg(p + i);
+            const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                a = fminf(a, fminf(wq::bf_lo(q[j]), wq::bf_hi(q[j])));
+                b = fmaxf(b, fmaxf(wq::bf_lo(q[j]), wq::bf_hi(q[j])));
+            }
+        }
+        const QParams qp = qparams<QMAX>(a, b);
+        scale[g] = (uint16_t)qp.scale_bits;
+        zp[g] = (uint8_t)qp.zp;
+    }
+}
+
+template <int NBITS>
+__global__ void __launch_bounds__(kThreads) uintx_pack_general(const uint16_t* __restrict__ w,
+                                                               int64_t numel, int group,
+                                                               const uint16_t* __restrict__ scale,
+                                                               const uint8_t* __restrict__ zp,
+                                                               uint8_t* __restrict__ packed) {
+    using S = Shards<NBITS>;
+    constexpr int QMAX = (1 << NBITS) - 1;
+    const int64_t L1 = numel / 8;
+    const int64_t base2 = S::has4 ? numel / 2 : 0;
+    const int64_t base1 = base2 + (S::has2 ? numel / 4 : 0);
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t d = (int64_t)blockIdx.x * kThreads + threadIdx.x; d < L1; d += stride) {
+        uint32_t c[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int64_t e = m * L1 + d, g = e / group;
+            const float sc = wq::bf_to_f(__ldg(scale + g));
+            const uint32_t z = __ldg(zp + g);
+            const float inv = wq::bfr(__fdiv_rn(1.0f, sc));
+            const float p = wq::bfr(__fmul_rn(wq::bf_to_f(__ldg(w + e)), inv));
+            const float pc = fminf(fmaxf(p, -(float)z), (float)(QMAX - (int)z));
+            c[m] = (uint32_t)(__float_as_int(__fadd_rn(pc, kMagic)) - 0x4B400000) + z;
+        }
+        if (S::has4) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) packed[m * L1 + d] = (uint8_t)((c[m] & 15u) | ((c[m + 4] & 15u) << 4));
+        }
+        if (S::has2) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t b = 0;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) b |= ((c[2 * jj + h] >> S::off2) & 3u) << (2 * jj);
+                packed[base2 + h * L1 + d] = (uint8_t)b;
+            }
+        }
+        if (S::has1) {
+            uint32_t b = 0;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) b |= ((c[m] >> S::off1) & 1u) << m;
+            packed[base1 + d] = (uint8_t)b;
+        }
+    }
+}
+
+// ----------------------------------------------------------- dequant
+// Codes of positions d .. d+7 of all 8 segments from the shard bytes, then
+// out = bf16(bf16(q - zp) * scale): q - zp is an exact small integer and the
+// product of two bf16 values is exact in binary32, so one cvt.rn gives the page's
+// bf16 result.
+template <int NBITS>
+__device__ __forceinline__ void load_codes(const uint8_t* __restrict__ packed, int64_t numel,
+                                           int64_t L1, int64_t d, uint32_t (&blo)[8],
+                                           uint32_t (&bhi)[8]) {
+    using S = Shards<NBITS>;
+    const int64_t base2 = S::has4 ? numel / 2 : 0;
+    const int64_t base1 = base2 + (S::has2 ? numel / 4 : 0);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) { blo[m] = 0; bhi[m] = 0; }
+    if (S::has4) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const uint2 s = wq::ld_stream2(packed + m * L1 + d);
+            blo[m] |= s.x & 0x0F0F0F0Fu;
+            bhi[m] |= s.y & 0x0F0F0F0Fu;
+            blo[m + 4] |= (s.x >> 4) & 0x0F0F0F0Fu;
+            bhi[m + 4] |= (s.y >> 4) & 0x0F0F0F0Fu;
+        }
+    }
+    if (S::has2) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint2 s = wq::ld_stream2(packed + base2 + h * L1 + d);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                blo[2 * jj + h] |= ((s.x >> (2 * jj)) & 0x03030303u) << S::off2;
+                bhi[2 * jj + h] |= ((s.y >> (2 * jj)) & 0x03030303u) << S::off2;
+            }
+        }
+    }
+    if (S::has1) {
+        const uint2 s = wq::ld_stream2(packed + base1 + d);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            blo[m] |= ((s.x >> m) & 0x01010101u) << S::off1;
+            bhi[m] |= ((s.y >> m) & 0x01010101u) << S::off1;
+        }
+    }
+}
+
+__device__ __forceinline__ float deq1(uint32_t q, float zf, float sc) {
+    return __fmul_rn(__fsub_rn((float)q, zf), sc);
+}
+
+// numel % 64 == 0: 8 positions per thread, 16-byte output stores.
+template <int NBITS, bool BF16>
+__global__ void __launch_bounds__(kThreads) uintx_dequant_vec(const uint8_t* __restrict__ packed,
+                                                              const uint16_t* __restrict__ scale,
+                                                              const uint8_t* __restrict__ zp,
+                                                              int64_t numel, int group,
+                                                              void* __restrict__ out) {
+    const int64_t L1 = numel / 8, items = L1 / 8;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x; t < items; t += stride) {
+        const int64_t d = 8 * t;
+        uint32_t blo[8], bhi[8];
+        load_codes<NBITS>(packed, numel, L1, d, blo, bhi);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int64_t e = m * L1 + d, g = e / group;  // 8 | group: one group
+            const float sc = wq::bf_to_f(__ldg(scale + g));
+            const float zf = (float)__ldg(zp + g);
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[j] = deq1((blo[m] >> (8 * j)) & 0xffu, zf, sc);
+                f[j + 4] = deq1((bhi[m] >> (8 * j)) & 0xffu, zf, sc);
+            }
+            const uint4 o = make_uint4(wq::f2_to_bf2(f[0], f[1]), wq::f2_to_bf2(f[2], f[3]),
+                                       wq::f2_to_bf2(f[4], f[5]), wq::f2_to_bf2(f[6], f[7]));
+            if (BF16) {
+                reinterpret_cast<uint4*>(out)[e / 8] = o;
+            } else {
+                float4* p = reinterpret_cast<float4*>(out) + e / 4;
+                p[0] = make_float4(wq::bf_lo(o.x), wq::bf_hi(o.x), wq::bf_lo(o.y), wq::bf_hi(o.y));
+                p[1] = make_float4(wq::bf_lo(o.z), wq::bf_hi(o.z), wq::bf_lo(o.w), wq::bf_hi(o.w));
+            }
+        }
+    }
+}
+
+// any numel % 8 == 0: one position per thread, byte loads.
+template <int NBITS, bool BF16>
+__global__ void __launch_bounds__(kThreads) uintx_dequant_general(const uint8_t* __restrict__ packed,
+                                                                  const uint16_t* __restrict__ scale,
+                                                                  const uint8_t* __restrict__ zp,
+                                                                  int64_t numel, int group,
+                                                                  void* __restrict__ out) {
+    using S = Shards<NBITS>;
+    const int64_t L1 = numel / 8;
+    const int64_t base2 = S::has4 ? numel / 2 : 0;
+    const int64_t base1 = base2 + (S::has2 ? numel / 4 : 0);
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t d = (int64_t)blockIdx.x * kThreads + threadIdx.x; d < L1; d += stride) {
+        uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (S::has4) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t b = __ldg(packed + m * L1 + d);
+                c[m] |= b & 15u;
+                c[m + 4] |= b >> 4;
+            }
+        }
+        if (S::has2) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t b = __ldg(packed + base2 + h * L1 + d);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) c[2 * jj + h] |= ((b >> (2 * jj)) & 3u) << S::off2;
+            }
+        }
+        if (S::has1) {
+            const uint32_t b = __ldg(packed + base1 + d);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) c[m] |= ((b >> m) & 1u) << S::off1;
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int64_t e = m * L1 + d, g = e / group;
+            const float v = deq1(c[m], (float)__ldg(zp + g), wq::bf_to_f(__ldg(scale + g)));
+            const uint32_t h = wq::f_to_bf(v);
+            if (BF16) reinterpret_cast<uint16_t*>(out)[e] = (uint16_t)h;
+            else reinterpret_cast<float*>(out)[e] = wq::bf_to_f(h);
+        }
+    }
+}
+
+template <int NBITS>
+wq_status quant_nbits(const uint16_t* w, int64_t numel, int group, uint8_t* packed, uint16_t* scale,
+                      uint8_t* zp, cudaStream_t st) {
+    constexpr int QMAX = (1 << NBITS) - 1;
+    if (group == 64 && numel % 512 == 0) {
+        const int64_t items = (numel / 8 + 255) / 256;  // one per warp
+        const void* fn = (const void*)uintx_quant_fused<NBITS>;
+        const int grid = wqh::grid_for(fn, kThreads, 0, (items + 7) / 8, 1 << 30);
+        uintx_quant_fused<NBITS><<<grid, kThreads, 0, st>>>(w, numel, packed, scale, zp);
+        return wqh::check_launch();
+    }
+    const int64_t ngroups = numel / group;
+    int grid = wqh::grid_for((const void*)uintx_qparams_kernel<QMAX>, kThreads, 0,
+                             (ngroups + kThreads - 1) / kThreads, 1 << 30);
+    uintx_qparams_kernel<QMAX><<<grid, kThreads, 0, st>>>(w, ngroups, group, scale, zp);
+    wq_status s = wqh::check_launch();
+    if (s != WQ_OK) return s;
+    const int64_t L1 = numel / 8;
+    grid = wqh::grid_for((const void*)uintx_pack_general<NBITS>, kThreads, 0,
+                         (L1 + kThreads - 1) / kThreads, 1 << 30);
+    uintx_pack_general<NBITS><<<grid, kThreads, 0, st>>>(w, numel, group, scale, zp, packed);
+    return wqh::check_launch();
+}
+
+template <int NBITS, bool BF16>
+wq_status dequant_nbits(const uint8_t* packed, const uint16_t* scale, const uint8_t* zp,
+                        int64_t numel, int group, void* out, cudaStream_t st) {
+    if (numel % 64 == 0) {
+        const int64_t items = numel / 64;
+        const int grid = wqh::grid_for((const void*)uintx_dequant_vec<NBITS, BF16>, kThreads, 0,
+                                       (items + kThreads - 1) / kThreads, 1 << 30);
+        uintx_dequant_vec<NBITS, BF16><<<grid, kThreads, 0, st>>>(packed, scale, zp, numel, group, out);
+    } else {
+        const int64_t L1 = numel / 8;
+        const int grid = wqh::grid_for((const void*)uintx_dequant_general<NBITS, BF16>, kThreads, 0,
+                                       (L1 + kThreads - 1) / kThreads, 1 << 30);
+        uintx_dequant_general<NBITS, BF16><<<grid, kThreads, 0, st>>>(packed, scale, zp, numel, group, out);
+    }
+    return wqh::check_launch();
+}
+
+wq_status check_common(int64_t n, int64_t k, int nbits, int group) {
+    if (n < 0 || k < 0) return WQ_ERR_BAD_SHAPE;
+    if (nbits < 2 || nbits > 7) return WQ_ERR_UNSUPPORTED;  // uint8 is refused, as the page does
+    if (group <= 0 || group % 8 != 0) return WQ_ERR_UNSUPPORTED;
+    if (k % group != 0) return WQ_ERR_BAD_SHAPE;
+    return WQ_OK;
+}
+
+}  // namespace
+
+extern "C" wq_status uintx_quantize(const uint16_t* w, int64_t n, int64_t k, int nbits, int group,
+                                    uint8_t* packed, uint16_t* scale, uint8_t* zp, void* stream) {
+    wq_status s = check_common(n, k, nbits, group);
+    if (s != WQ_OK) return s;
+    if (n == 0 || k == 0) return WQ_OK;
+    if (!w || !packed || !scale || !zp) return WQ_ERR_NULL_PTR;
+    if (!wqh::aligned16(w) || !wqh::aligned16(packed) || !wqh::aligned_to(scale, 2))
+        return WQ_ERR_MISALIGNED;
+    const int64_t numel = n * k;
+    cudaStream_t st = (cudaStream_t)stream;
+    switch (nbits) {
+        case 2: return quant_nbits<2>(w, numel, group, packed, scale, zp, st);
+        case 3: return quant_nbits<3>(w, numel, group, packed, scale, zp, st);
+        case 4: return quant_nbits<4>(w, numel, group, packed, scale, zp, st);
+        case 5: return quant_nbits<5>(w, numel, group, packed, scale, zp, st);
+        case 6: return quant_nbits<6>(w, numel, group, packed, scale, zp, st);
+        case 7: return quant_nbits<7>(w, numel, group, packed, scale, zp, st);
+        default: return WQ_ERR_UNSUPPORTED;
+    }
+}
+
+extern "C" wq_status uintx_dequantize(const uint8_t* packed, const uint16_t* scale, const uint8_t* zp,
+                                      int64_t n, int64_t k, int nbits, int group, int out_dtype,
+                                      void* out, void* stream) {
+    wq_status s = check_common(n, k, nbits, group);
+    if (s != WQ_OK) return s;
+    if (out_dtype != WQ_DTYPE_F32 && out_dtype != WQ_DTYPE_BF16) return WQ_ERR_BAD_DTYPE;
+    if (n == 0 || k == 0) return WQ_OK;
+    if (!packed || !scale || !zp || !out) return WQ_ERR_NULL_PTR;
+    if (!wqh::aligned16(packed) || !wqh::aligned16(out) || !wqh::aligned_to(scale, 2))
+        return WQ_ERR_MISALIGNED;
+    const int64_t numel = n * k;
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool bf = out_dtype == WQ_DTYPE_BF16;
+#define WQ_UX_DQ(NB) \
+    case NB: return bf ? dequant_nbits<NB, true>(packed, scale, zp, numel, group, out, st) \
+                       : dequant_nbits<NB, false>(packed, scale, zp, numel, group, out, st);
+    switch (nbits) {
+        WQ_UX_DQ(2)
+        WQ_UX_DQ(3)
+        WQ_UX_DQ(4)
+        WQ_UX_DQ(5)
+        WQ_UX_DQ(6)
+        WQ_UX_DQ(7)
+        default: return WQ_ERR_UNSUPPORTED;
+    }
+#undef WQ_UX_DQ
+}
