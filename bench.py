@@ -77,7 +77,7 @@ class ClockSampler:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index),
                  "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -529,16 +529,95 @@ def run_reference(args, rank, world):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_single(args):
+    """One kernel on one synthetic tensor (for ncu captures and quick timing):
+    prints the mean CUDA-event time per launch and the algorithmic GB/s."""
+    import weight_only_bit_group_gb300 as wq
+    from weight_only_bit_group_gb300 import synth
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    n, k = (int(x) for x in args.shape.split("x"))
+    w = synth.outlier_columns_bf16(n, k, 0.02, 0.005, 20.0, 11, device=dev)
+    name = args.kernel
+    ws = wq.workspace(wq.WQ_OP_GPTQ_QUANTIZE, n, k, GROUP_GPTQ, dev)
+    if name.startswith("gptq_quantize"):
+        fn = wq.gptq_quantize_asym if name.endswith("asym") else wq.gptq_quantize_sym
+        out = fn(w, GROUP_GPTQ, True, ws=ws)
+        call = lambda: fn(w, GROUP_GPTQ, True, qweight=out["qweight"], qzeros=out["qzeros"],
+                          scales=out["scales"], g_idx=out["g_idx"], snr_db=out["snr_db"], ws=ws)
+        alg = n * k * (2 + 0.5) + (n * k // GROUP_GPTQ) * 2.5 + 4 * k
+    elif name.startswith("gptq_dequantize"):
+        sym = name.endswith("sym")
+        r = (wq.gptq_quantize_sym if sym else wq.gptq_quantize_asym)(w, GROUP_GPTQ, False)
+        out = torch.empty(n, k, dtype=torch.bfloat16, device=dev)
+        call = lambda: wq.gptq_dequantize(r["qweight"], r["qzeros"], r["scales"], n, k, GROUP_GPTQ,
+                                          sym, torch.bfloat16, "nk", out=out)
+        alg = n * k * (0.5 + 2) + (n * k // GROUP_GPTQ) * 2.5
+    elif name == "mxfp4_quantize":
+        p, e = wq.mxfp4_quantize(w)
+        call = lambda: wq.mxfp4_quantize(w, 0, packed=p, e8m0=e)
+        alg = n * k * (2 + 0.5 + 1 / 32)
+    elif name == "mxfp4_dequantize":
+        p, e = wq.mxfp4_quantize(w)
+        out = torch.empty(n, k, dtype=torch.bfloat16, device=dev)
+        call = lambda: wq.mxfp4_dequantize(p, e, torch.bfloat16, out=out)
+        alg = n * k * (0.5 + 1 / 32 + 2)
+    elif name == "uintx_quantize":
+        p, sc, z = wq.uintx_quantize(w, NBITS_UINTX)
+        call = lambda: wq.uintx_quantize(w, NBITS_UINTX, packed=p, scale=sc, zp=z)
+        alg = n * k * (2 + NBITS_UINTX / 8 + 3 / 64)
+    elif name == "uintx_dequantize":
+        p, sc, z = wq.uintx_quantize(w, NBITS_UINTX)
+        out = torch.empty(n, k, dtype=torch.bfloat16, device=dev)
+        call = lambda: wq.uintx_dequantize(p, sc, z, n, k, NBITS_UINTX, out=out)
+        alg = n * k * (NBITS_UINTX / 8 + 3 / 64 + 2)
+    elif name == "quant_snr":
+        d = w.clone()
+        sn = torch.empty((), dtype=torch.float64, device=dev)
+        re = torch.empty((), dtype=torch.float64, device=dev)
+        call = lambda: wq.quant_snr(w, d, "nk", snr_db=sn, rel_err=re, ws=ws)
+        alg = n * k * 4
+    elif name == "awq_search":
+        a = synth.awq_activation(k, device=dev)
+        call = lambda: wq.awq_search(w, a, synth.ALPHAS, 2048)
+        alg = min(n, 2048) * k * 2
+    else:
+        raise SystemExit(f"unknown kernel {name}")
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    times = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a_ = torch.cuda.Event(enable_timing=True)
+        b_ = torch.cuda.Event(enable_timing=True)
+        a_.record()
+        call()
+        b_.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(a_.elapsed_time(b_))
+    t = statistics.mean(times)
+    peak, kind = peaks()
+    print(json.dumps({"kernel": name, "shape": [n, k], "ms": round(t, 4),
+                      "alg_GBps": round(alg / t / 1e6, 1), "frac_of_" + kind: round(alg / t / 1e6 / peak, 4)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--kernel", default=None, help="time one kernel alone (see run_single)")
+    ap.add_argument("--shape", default="16384x8192")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
+    if args.kernel:
+        return run_single(args)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
 

@@ -91,10 +91,13 @@ def test_gptq_hand_groups_on_gpu():
     with open(os.path.join(GOLDEN, "gptq_hand_groups.json")) as fh:
         cases = json.load(fh)["cases"]
     for case in cases:
-        col = np.array(case["column"], np.float32)
+        # the GPU kernel supports groups of 32..256: repeating the 8-value hand group
+        # four times leaves its min/max/amax (hence every code) unchanged, so each
+        # of the four qweight words per column must equal the hand-derived word
+        col = np.tile(np.array(case["column"], np.float32), 4)
         w = torch.from_numpy(np.tile(col, (8, 1))).to(torch.bfloat16)
         fn = wq.gptq_quantize_sym if case["sym"] else wq.gptq_quantize_asym
-        r = fn(w.to(DEV), group=case["group"], snr=False)
+        r = fn(w.to(DEV), group=4 * case["group"], snr=False)
         assert np.all(npy(r["qweight"]).view(np.uint32) == int(case["qweight_word"], 16)), case["name"]
         assert np.all(u16(r["scales"]) == int(case["scale_f16"], 16)), case["name"]
         assert np.all(npy(r["qzeros"]).view(np.uint32) == int(case["qzeros_word"], 16)), case["name"]

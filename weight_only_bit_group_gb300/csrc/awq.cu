@@ -6,10 +6,13 @@
 //                   err = sum over the row subsample of ((deq(quant(W*s)) / s - W) * a_c)^2
 //   best = first alpha with the strictly smallest err
 //
-// Three kernels on the caller's stream:
-//   awq_prep      one CTA: the s and 1/s tables [n_alpha][k] (binary64 sums in a
-//                 fixed order rounded once to binary32; pow/log/exp in binary64
-//                 rounded once to binary32), a_c [k].
+// Four kernels on the caller's stream:
+//   awq_tables    grid (k/256, n_alpha): t = clamp(an^alpha, 1e-2, 1e2) and log t
+//                 per column and alpha (pow/log in binary64 rounded once to
+//                 binary32; mean(a_c) as a binary64 sum in a fixed order, the
+//                 same in every CTA), a_c [k].
+//   awq_norm      one CTA per alpha: exp(mean(log t)) (fixed-order binary64
+//                 sum), s = t / gm and RN(1/s).
 //   awq_err       every subsampled weight is read once; all alphas are evaluated
 //                 in registers (4 rows x 8 columns per lane, s/1-s loaded once per
 //                 alpha for those 4 rows).  Per element and alpha: W*s, the
@@ -23,7 +26,6 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kPrepThreads = 1024;
 constexpr int kMaxAlpha = 16;
 constexpr int kRowsPerLane = 4;
 
@@ -31,7 +33,8 @@ struct AlphaList {
     float v[kMaxAlpha];
 };
 
-__device__ double block_sum_1024(double v, double* red) {
+// Fixed-order sum over a 256-thread CTA (every thread gets the result).
+__device__ double block_sum_256(double v, double* red) {
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
     __syncthreads();
@@ -39,43 +42,54 @@ __device__ double block_sum_1024(double v, double* red) {
     __syncthreads();
     if (threadIdx.x == 0) {
         double t = 0.0;
-        for (int i = 0; i < kPrepThreads / 32; ++i) t += red[i];
-        red[32] = t;
+        for (int i = 0; i < kThreads / 32; ++i) t += red[i];
+        red[kThreads / 32] = t;
     }
     __syncthreads();
-    return red[32];
+    return red[kThreads / 32];
 }
 
-__global__ void __launch_bounds__(kPrepThreads) awq_prep(const float* __restrict__ a, int64_t k,
-                                                         AlphaList al, int n_alpha,
-                                                         float* __restrict__ s_tab,
-                                                         float* __restrict__ r_tab,
-                                                         float* __restrict__ a_c) {
-    __shared__ double red[33];
+// Grid (ceil(k/256), n_alpha).  Every CTA forms mean(a_c) in the same fixed
+// order (so all agree bit for bit), then for its 256 columns and its alpha:
+// t = clamp(an^alpha, 1e-2, 1e2) -> t_tab, log(t) rounded to binary32 -> l_tab.
+__global__ void __launch_bounds__(kThreads) awq_tables(const float* __restrict__ a, int64_t k,
+                                                       AlphaList al, float* __restrict__ t_tab,
+                                                       float* __restrict__ l_tab,
+                                                       float* __restrict__ a_c) {
+    __shared__ double red[kThreads / 32 + 1];
     double part = 0.0;
-    for (int64_t c = threadIdx.x; c < k; c += kPrepThreads) {
-        const float ac = fmaxf(a[c], 1e-8f);
-        a_c[c] = ac;
-        part += (double)ac;
+    for (int64_t c = threadIdx.x; c < k; c += kThreads) part += (double)fmaxf(__ldg(a + c), 1e-8f);
+    const float mean = (float)(block_sum_256(part, red) / (double)k);
+    const int64_t c = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int i = blockIdx.y;
+    if (c < k) {
+        const float ac = fmaxf(__ldg(a + c), 1e-8f);
+        if (i == 0) a_c[c] = ac;
+        const float an = __fdiv_rn(ac, mean);
+        float t = (float)pow((double)an, (double)al.v[i]);
+        t = fminf(fmaxf(t, 1e-2f), 1e2f);
+        t_tab[(int64_t)i * k + c] = t;
+        l_tab[(int64_t)i * k + c] = (float)log((double)t);
     }
-    const float mean = (float)(block_sum_1024(part, red) / (double)k);
-    for (int i = 0; i < n_alpha; ++i) {
-        float* s = s_tab + (int64_t)i * k;
-        double lp = 0.0;
-        for (int64_t c = threadIdx.x; c < k; c += kPrepThreads) {
-            const float an = __fdiv_rn(a_c[c], mean);
-            float t = (float)pow((double)an, (double)al.v[i]);
-            t = fminf(fmaxf(t, 1e-2f), 1e2f);
-            s[c] = t;
-            lp += (double)(float)log((double)t);
-        }
-        const float lmean = (float)(block_sum_1024(lp, red) / (double)k);
-        const float gm = (float)exp((double)lmean);
-        for (int64_t c = threadIdx.x; c < k; c += kPrepThreads) {
-            const float sv = __fdiv_rn(s[c], gm);
-            s[c] = sv;
-            r_tab[(int64_t)i * k + c] = __frcp_rn(sv);
-        }
+}
+
+// One CTA per alpha: gm = exp(mean(log t)) from the binary32 logs (binary64 sum
+// in a fixed order), then s = t / gm and r = RN(1/s).  r_tab holds the logs on
+// entry (all read before any is overwritten).
+__global__ void __launch_bounds__(kThreads) awq_norm(int64_t k, float* __restrict__ s_tab,
+                                                     float* __restrict__ r_tab) {
+    __shared__ double red[kThreads / 32 + 1];
+    const int i = blockIdx.x;
+    float* s = s_tab + (int64_t)i * k;
+    float* r = r_tab + (int64_t)i * k;
+    double part = 0.0;
+    for (int64_t c = threadIdx.x; c < k; c += kThreads) part += (double)r[c];
+    const float lmean = (float)(block_sum_256(part, red) / (double)k);
+    const float gm = (float)exp((double)lmean);
+    for (int64_t c = threadIdx.x; c < k; c += kThreads) {
+        const float sv = __fdiv_rn(s[c], gm);
+        s[c] = sv;
+        r[c] = __frcp_rn(sv);
     }
 }
 
@@ -224,10 +238,14 @@ __global__ void __launch_bounds__(kThreads) awq_finalize(const double* __restric
                                                          double* __restrict__ errs) {
     __shared__ double e[kMaxAlpha];
     __shared__ int best;
-    if (threadIdx.x < n_alpha) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // warp w sums alphas w, w + 8: lane-strided slots, then a fixed shuffle tree
+    for (int i = warp; i < n_alpha; i += kThreads / 32) {
         double t = 0.0;
-        for (int b = 0; b < nslots; ++b) t += slots[(int64_t)b * n_alpha + threadIdx.x];
-        e[threadIdx.x] = t;
+        for (int b = lane; b < nslots; b += 32) t += slots[(int64_t)b * n_alpha + i];
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
+        if (lane == 0) e[i] = t;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -271,15 +289,19 @@ extern "C" wq_status awq_search(const uint16_t* w, int64_t n, int64_t k, const f
     for (int i = 0; i < kMaxAlpha; ++i) al.v[i] = i < n_alpha ? alphas_host[i] : 0.0f;
 
     auto up = [](size_t b) { return (b + 255) & ~(size_t)255; };
-    char* ws = (char*)workspace;
+    char* ws = (char*)workspace + wqh::kCtrlBytes;
     float* s_tab = (float*)ws;
     float* r_tab = (float*)(ws + up((size_t)n_alpha * k * sizeof(float)));
     float* a_c = (float*)(ws + 2 * up((size_t)n_alpha * k * sizeof(float)));
     double* slots = (double*)(ws + 2 * up((size_t)n_alpha * k * sizeof(float)) + up((size_t)k * sizeof(float)));
 
     cudaStream_t st = (cudaStream_t)stream;
-    awq_prep<<<1, kPrepThreads, 0, st>>>(a, k, al, n_alpha, s_tab, r_tab, a_c);
+    awq_tables<<<dim3((unsigned)((k + kThreads - 1) / kThreads), (unsigned)n_alpha), kThreads, 0, st>>>(
+        a, k, al, s_tab, r_tab, a_c);
     wq_status s = wqh::check_launch();
+    if (s != WQ_OK) return s;
+    awq_norm<<<n_alpha, kThreads, 0, st>>>(k, s_tab, r_tab);
+    s = wqh::check_launch();
     if (s != WQ_OK) return s;
 
     const int64_t items = ((k + 255) / 256) * ((rows + kRowsPerLane - 1) / kRowsPerLane);

@@ -2,224 +2,210 @@
 // (export_gptq_cpu.py: pack_int32, quantize_sym, quantize_asym; module docstring
 // for the uint4b8 dequant rule).
 //
-// Quantize tile: 64 output channels (rows of w) x 256 input channels.  Lane l of
-// a warp reads w[row][k0 + 8l .. 8l+7] (one 16-byte load); warp j owns rows
-// j, j+8, ..., j+56, so a CTA keeps 32 KB of loads in flight.  The eight codes of
-// a lane are one qweight word (row r = (k0 + 8l)/8, column = row of w); words go
-// through shared memory so that each qweight row segment [r][n0 .. n0+63] leaves
-// as 256 contiguous bytes.  Per (group, column) parameters: the max/min is a
-// shuffle reduction over the group's G/8 lanes; the divisions are then done once
-// per group (not once per lane) and broadcast back by shuffle.  Per element the
-// quotient x / scale uses a correctly rounded reciprocal and one FMA correction
-// (bit-identical to IEEE division), round-half-even comes from the binary32
-// adder, and the clamp to [0, 15] is applied before rounding (exact because the
-// bounds are integers).
+// Quantize: a warp owns a tile of 32 output channels (rows of w) x KT input
+// channels (KT = 128, or the group when it is larger) and lane l owns row
+// n0 + l.  The tile arrives in shared memory through a two-stage per-warp
+// cp.async pipeline (each copy instruction moves two whole 256-byte row
+// segments, fully coalesced; rows are padded to 272 bytes so the per-lane
+// reads are bank-conflict free) while the previous tile is computed.  A lane
+// holds whole groups of its row, so the group max/min is an in-thread bf16x2
+// reduction and the scale / zero point are computed once per group with true
+// IEEE divisions.  Per element: the quotient by the scale from a correctly
+// rounded reciprocal plus one FMA correction (bit-identical to IEEE division),
+// the clamp to [-zp, 15-zp] (exact before rounding, the bounds are integers),
+// round-half-even by the binary32 adder (x + 1.5*2^23), and the nibble pack as
+// one IMAD per element.  The eight codes along k of one row are one qweight
+// word, so the 32 lanes store 32 consecutive qweight columns (128 bytes) per
+// word row -- the [K/8, N] transpose costs nothing.  Packed-pair (f32x2) math
+// halves the issue slots of the arithmetic.  The optional reconstruction SNR
+// is accumulated from the same registers and reduced by the last CTA.
 #include "wq_common.cuh"
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kNT = 64;   // rows of w (columns of qweight) per tile
-constexpr int kKT = 256;  // input channels per tile
+constexpr int kThreads = 256;  // dequant kernels
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
 
-struct GroupParams {
-    float s;   // binary32 scale
-    float r;   // RN(1 / s)
-    float zp;  // zero point as a float (8 for sym)
+template <int G>
+struct QTile {
+    static constexpr int KT = G < 128 ? 128 : G;     // input channels per warp tile
+    static constexpr int CH = KT / 8;                 // 16-byte chunks per row
+    static constexpr int ROWB = KT * 2 + 16;          // padded shared-memory row
+    static constexpr int STAGE = 32 * ROWB;           // one stage of one warp
+    static constexpr int NS = 2;                      // pipeline stages
+    static constexpr int WARPS = KT > 128 ? 2 : 4;    // warps per CTA
+    static constexpr int THREADS = 32 * WARPS;
+    static constexpr int SMEM = NS * WARPS * STAGE;
 };
 
-template <bool SYM>
-__device__ __forceinline__ GroupParams make_params(float a, float b) {
-    // SYM: a = amax.  ASYM: a = wmax, b = wmin.
-    GroupParams p;
-    if (SYM) {
-        p.s = fmaxf(__fdiv_rn(a, 8.0f), 1e-9f);
-        p.zp = 8.0f;
-    } else {
-        p.s = __fdiv_rn(fmaxf(__fsub_rn(a, b), 1e-9f), 15.0f);
-        p.zp = fminf(fmaxf(rintf(__fdiv_rn(-b, p.s)), 0.0f), 15.0f);
-    }
-    p.r = __frcp_rn(p.s);
-    return p;
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
 }
 
 template <bool SYM, int G, bool SNR>
-__global__ void __launch_bounds__(kThreads) gptq_quant_kernel(
+__global__ void __launch_bounds__(QTile<G>::THREADS, 3) gptq_quant_kernel(
     const uint16_t* __restrict__ w, int64_t n, int64_t k, int32_t* __restrict__ qweight,
     int32_t* __restrict__ qzeros, uint16_t* __restrict__ scales, int32_t* __restrict__ g_idx,
-    double* __restrict__ slots) {
-    constexpr int LPG = G / 8;                    // lanes per group
-    constexpr int RPL = LPG >= 8 ? 1 : 8 / LPG;   // rows whose parameters each lane computes
-    constexpr int GPT = kKT / G;                  // groups per tile along k
-    __shared__ uint32_t s_qw[kKT / 8][kNT + 1];
-    __shared__ uint16_t s_sc[GPT][kNT];
-    __shared__ uint8_t s_zp[GPT][kNT];
-
+    double* __restrict__ slots, unsigned* __restrict__ counter, double* __restrict__ snr_db) {
+    using T = QTile<G>;
+    extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t tiles_n = (n + kNT - 1) / kNT, tiles_k = (k + kKT - 1) / kKT;
+    unsigned char* wsm = smem + warp * (T::NS * T::STAGE);
+    const int64_t tn = (n + 31) / 32, tk = (k + T::KT - 1) / T::KT, ntiles = tn * tk;
+    const int64_t gwarp = (int64_t)blockIdx.x * T::WARPS + warp;
+    const int64_t nwarps = (int64_t)gridDim.x * T::WARPS;
+
+    auto issue = [&](int64_t t, int stage) {
+        if (t < ntiles) {
+            const int64_t n0 = (t % tn) * 32, k0 = (t / tn) * T::KT;
+            unsigned char* dst = wsm + stage * T::STAGE;
+#pragma unroll
+            for (int i = 0; i < T::CH; ++i) {
+                const int idx = i * 32 + lane, row = idx / T::CH, ch = idx % T::CH;
+                const int64_t gr = n0 + row, gk = k0 + 8 * ch;
+                if (gr < n && gk < k) wq::cp_async16(dst + row * T::ROWB + 16 * ch, w + gr * k + gk);
+            }
+        }
+        wq::cp_async_commit();
+    };
+
     double dw = 0.0, de = 0.0;
-
-    for (int64_t t = blockIdx.x; t < tiles_n * tiles_k; t += gridDim.x) {
-        const int64_t n0 = (t % tiles_n) * kNT, k0 = (t / tiles_n) * kKT;
-        const int64_t kk = k0 + 8 * lane;
-        const bool kval = kk < k;  // k % G == 0: a group is all-valid or all-invalid
-
-        uint4 v[8];
+    int64_t t = gwarp;
+    issue(t, 0);
+    for (int j = 0; t < ntiles; ++j, t += nwarps) {
+        issue(t + nwarps, (j + 1) & 1);
+        wq::cp_async_wait<1>();
+        __syncwarp();
+        const int64_t n0 = (t % tn) * 32, k0 = (t / tn) * T::KT;
+        const int64_t col = n0 + lane;
+        const bool rowv = col < n;
+        const unsigned char* rsm = wsm + (j & 1) * T::STAGE + lane * T::ROWB;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int64_t row = n0 + warp + 8 * i;
-            v[i] = (kval && row < n) ? wq::ld_stream(w + row * k + kk) : make_uint4(0, 0, 0, 0);
-        }
-
-        // per-row group statistics, reduced over the LPG lanes of the group
-        float ra[8], rb[8];
+        for (int g = 0; g < T::KT / G; ++g) {
+            if (k0 + g * G >= k) break;  // k % G == 0: warp-uniform
+            uint4 v[G / 8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float x[8] = {wq::bf_lo(v[i].x), wq::bf_hi(v[i].x), wq::bf_lo(v[i].y), wq::bf_hi(v[i].y),
-                          wq::bf_lo(v[i].z), wq::bf_hi(v[i].z), wq::bf_lo(v[i].w), wq::bf_hi(v[i].w)};
-            float a, b = 0.0f;
+            for (int c = 0; c < G / 8; ++c) v[c] = *reinterpret_cast<const uint4*>(rsm + 16 * (g * (G / 8) + c));
+            float s, zp;
             if (SYM) {
-                a = fabsf(x[0]);
+                const uint32_t M = 0x7fff7fffu;
+                uint32_t m = __vmaxu2(v[0].x & M, v[0].y & M);
 #pragma unroll
-                for (int j = 1; j < 8; ++j) a = fmaxf(a, fabsf(x[j]));
-#pragma unroll
-                for (int m = 1; m < LPG; m <<= 1) a = fmaxf(a, wq::shfl_xor(a, m));
+                for (int c = 0; c < G / 8; ++c)
+                    m = __vmaxu2(m, __vmaxu2(__vmaxu2(v[c].x & M, v[c].y & M), __vmaxu2(v[c].z & M, v[c].w & M)));
+                const float amax = wq::bf_to_f(max(m & 0xffffu, m >> 16));
+                s = fmaxf(__fdiv_rn(amax, 8.0f), 1e-9f);
+                zp = 8.0f;
             } else {
-                a = x[0];
-                b = x[0];
+                uint32_t mx = v[0].x, mn = v[0].x;
 #pragma unroll
-                for (int j = 1; j < 8; ++j) { a = fmaxf(a, x[j]); b = fminf(b, x[j]); }
-#pragma unroll
-                for (int m = 1; m < LPG; m <<= 1) {
-                    a = fmaxf(a, wq::shfl_xor(a, m));
-                    b = fminf(b, wq::shfl_xor(b, m));
+                for (int c = 0; c < G / 8; ++c) {
+                    mx = bmax2(mx, bmax2(bmax2(v[c].x, v[c].y), bmax2(v[c].z, v[c].w)));
+                    mn = bmin2(mn, bmin2(bmin2(v[c].x, v[c].y), bmin2(v[c].z, v[c].w)));
                 }
+                const float wmax = fmaxf(wq::bf_lo(mx), wq::bf_hi(mx));
+                const float wmin = fminf(wq::bf_lo(mn), wq::bf_hi(mn));
+                s = __fdiv_rn(fmaxf(__fsub_rn(wmax, wmin), 1e-9f), 15.0f);
+                zp = fminf(fmaxf(rintf(__fdiv_rn(-wmin, s)), 0.0f), 15.0f);
             }
-            ra[i] = a;
-            rb[i] = b;
-        }
-
-        // each lane derives the parameters of the rows i with i % LPG == lane % LPG
-        // (once per group instead of once per lane), then they are broadcast
-        GroupParams own[RPL];
+            const float r = __frcp_rn(s);
+            const float lo = -zp, hi = 15.0f - zp;
+            const uint32_t cg = (uint32_t)((int)zp - 0x4B400000) * 0x11111111u;
+            const wq::f2_t R2 = wq::f2(r, r), NS2 = wq::f2(-s, -s), M2 = wq::f2(kMagic, kMagic);
+            const wq::f2_t NM2 = wq::f2(-kMagic, -kMagic);
+            const bool exact = s <= 0x1p100f;  // r stays normal: the correction step is exact
+            wq::f2_t sw2 = wq::f2(0.0f, 0.0f), se2 = sw2;
+            const int64_t r0 = (k0 + g * G) / 8;
 #pragma unroll
-        for (int p = 0; p < RPL; ++p) {
-            const int sel = LPG >= 8 ? ((lane % LPG) & 7) : (lane % LPG) + p * LPG;
-            float a = ra[0], b = rb[0];
+            for (int c = 0; c < G / 8; ++c) {
+                const uint32_t u[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+                uint32_t word = cg;
 #pragma unroll
-            for (int i = 1; i < 8; ++i)
-                if (sel == i) { a = ra[i]; b = rb[i]; }
-            own[p] = make_params<SYM>(a, b);
-        }
-
-        float sw = 0.0f, se = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int src = (lane & ~(LPG - 1)) | (i % LPG);
-            const GroupParams& o = own[LPG >= 8 ? 0 : i / LPG];
-            GroupParams P;
-            P.s = __shfl_sync(0xffffffffu, o.s, src);
-            P.r = __shfl_sync(0xffffffffu, o.r, src);
-            P.zp = __shfl_sync(0xffffffffu, o.zp, src);
-            const float lo = -P.zp, hi = 15.0f - P.zp;
-            const uint32_t zpi = (uint32_t)P.zp;
-            float x[8] = {wq::bf_lo(v[i].x), wq::bf_hi(v[i].x), wq::bf_lo(v[i].y), wq::bf_hi(v[i].y),
-                          wq::bf_lo(v[i].z), wq::bf_hi(v[i].z), wq::bf_lo(v[i].w), wq::bf_hi(v[i].w)};
-            const bool exact_path = P.s <= 0x1p100f;  // r stays normal
-            uint32_t word = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float q = exact_path ? wq::div_by_recip(x[j], P.s, P.r) : __fdiv_rn(x[j], P.s);
-                q = fminf(fmaxf(q, lo), hi);
-                const float tq = __fadd_rn(q, kMagic);  // rint(q) + 1.5*2^23, exact
-                const uint32_t code = (uint32_t)(__float_as_int(tq) - 0x4B400000) + zpi;
-                word |= code << (4 * j);
-                if (SNR) {
-                    const float deq = __fmul_rn(__fsub_rn(tq, kMagic), P.s);  // (code - zp) * s
-                    const float e = __fsub_rn(x[j], deq);
-                    sw = __fadd_rn(sw, __fmul_rn(x[j], x[j]));
-                    se = __fadd_rn(se, __fmul_rn(e, e));
-                }
-            }
-            const int col = warp + 8 * i;
-            s_qw[lane][col] = word;
-            if ((lane % LPG) == 0) {
-                s_sc[lane / LPG][col] = __half_as_ushort(__float2half_rn(P.s));
-                s_zp[lane / LPG][col] = (uint8_t)zpi;
-            }
-        }
-        if (SNR) {
-            dw += (double)sw;
-            de += (double)se;
-        }
-        __syncthreads();
-
-        // qweight rows r = k0/8 + rl, columns n0 .. n0+63, 16 bytes per thread
-        const int64_t rows_q = k / 8;
-        for (int idx = threadIdx.x; idx < (kKT / 8) * (kNT / 4); idx += kThreads) {
-            const int rl = idx / (kNT / 4), c4 = (idx % (kNT / 4)) * 4;
-            const int64_t r = k0 / 8 + rl, c = n0 + c4;
-            if (r < rows_q && c < n) {
-                uint4 o = make_uint4(s_qw[rl][c4], s_qw[rl][c4 + 1], s_qw[rl][c4 + 2], s_qw[rl][c4 + 3]);
-                *reinterpret_cast<uint4*>(qweight + r * n + c) = o;
-            }
-        }
-        const int64_t gk = k / G;
-        for (int idx = threadIdx.x; idx < GPT * kNT; idx += kThreads) {
-            const int gl = idx / kNT, c = idx % kNT;
-            const int64_t g = k0 / G + gl;
-            if (g < gk && n0 + c < n) scales[g * n + n0 + c] = s_sc[gl][c];
-        }
-        if (qzeros) {
-            for (int idx = threadIdx.x; idx < GPT * (kNT / 8); idx += kThreads) {
-                const int gl = idx / (kNT / 8), c8 = idx % (kNT / 8);
-                const int64_t g = k0 / G + gl;
-                if (g < gk && n0 + 8 * c8 < n) {
-                    uint32_t word = 0x77777777u;
-                    if (!SYM) {
-                        word = 0;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) word |= (uint32_t)s_zp[gl][8 * c8 + j] << (4 * j);
+                for (int p = 0; p < 4; ++p) {
+                    const wq::f2_t x = wq::bf2_to_f2(u[p]);
+                    float q0, q1;
+                    if (exact) {
+                        const wq::f2_t qa = wq::mul2(x, R2);
+                        const wq::f2_t rem = wq::fma2(qa, NS2, x);
+                        wq::f2u(wq::fma2(rem, R2, qa), q0, q1);
+                    } else {
+                        float x0, x1;
+                        wq::f2u(x, x0, x1);
+                        q0 = __fdiv_rn(x0, s);
+                        q1 = __fdiv_rn(x1, s);
                     }
-                    qzeros[g * (n / 8) + n0 / 8 + c8] = (int32_t)word;
+                    q0 = fminf(fmaxf(q0, lo), hi);
+                    q1 = fminf(fmaxf(q1, lo), hi);
+                    const wq::f2_t tq = wq::add2(wq::f2(q0, q1), M2);  // rint(q) + 1.5*2^23
+                    float t0, t1;
+                    wq::f2u(tq, t0, t1);
+                    word += (uint32_t)__float_as_int(t0) << (8 * p);
+                    word += (uint32_t)__float_as_int(t1) << (8 * p + 4);
+                    if (SNR) {
+                        const wq::f2_t e = wq::fma2(wq::add2(tq, NM2), NS2, x);  // x - (code-zp)*s
+                        se2 = wq::fma2(e, e, se2);
+                        sw2 = wq::fma2(x, x, sw2);
+                    }
                 }
+                if (rowv) qweight[(r0 + c) * n + col] = (int32_t)word;
+            }
+            if (SNR) {
+                float a0, a1, b0, b1;
+                wq::f2u(sw2, a0, a1);
+                wq::f2u(se2, b0, b1);
+                if (rowv) {
+                    dw += (double)a0 + (double)a1;
+                    de += (double)b0 + (double)b1;
+                }
+            }
+            const int64_t gi = (k0 + g * G) / G;
+            if (rowv) scales[gi * n + col] = __half_as_ushort(__float2half_rn(s));
+            if (qzeros) {
+                uint32_t zw = SYM ? 0x77777777u : ((uint32_t)zp << (4 * (lane & 7)));
+                if (!SYM) {
+                    zw |= __shfl_xor_sync(0xffffffffu, zw, 1);
+                    zw |= __shfl_xor_sync(0xffffffffu, zw, 2);
+                    zw |= __shfl_xor_sync(0xffffffffu, zw, 4);
+                }
+                if (rowv && (lane & 7) == 0) qzeros[gi * (n / 8) + col / 8] = (int32_t)zw;
             }
         }
         if (g_idx && n0 == 0) {
-            for (int idx = threadIdx.x; idx < kKT; idx += kThreads)
-                if (k0 + idx < k) g_idx[k0 + idx] = (int32_t)((k0 + idx) / G);
-        }
-        __syncthreads();
-    }
-
-    if (SNR) {
-        __shared__ double sa[kThreads / 32], sb[kThreads / 32];
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) {
-            dw += __shfl_xor_sync(0xffffffffu, dw, m);
-            de += __shfl_xor_sync(0xffffffffu, de, m);
+            for (int i = lane; i < T::KT; i += 32)
+                if (k0 + i < k) g_idx[k0 + i] = (int32_t)((k0 + i) / G);
         }
-        if (lane == 0) { sa[warp] = dw; sb[warp] = de; }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            double ta = 0.0, tb = 0.0;
-            for (int i = 0; i < kThreads / 32; ++i) { ta += sa[i]; tb += sb[i]; }
-            slots[2 * blockIdx.x] = ta;
-            slots[2 * blockIdx.x + 1] = tb;
-        }
+        __syncwarp();
     }
+    wq::cp_async_wait<0>();
+    if (SNR) wq::finish_snr(dw, de, slots, counter, snr_db, nullptr);
 }
 
 template <bool SYM, int G, bool SNR>
 wq_status launch_quant(const uint16_t* w, int64_t n, int64_t k, int32_t* qweight, int32_t* qzeros,
-                       uint16_t* scales, int32_t* g_idx, double* slots, int* grid_out,
-                       cudaStream_t st) {
-    const int64_t tiles = ((n + kNT - 1) / kNT) * ((k + kKT - 1) / kKT);
+                       uint16_t* scales, int32_t* g_idx, double* slots, unsigned* counter,
+                       double* snr_db, cudaStream_t st) {
+    using T = QTile<G>;
     const void* fn = (const void*)gptq_quant_kernel<SYM, G, SNR>;
-    const int grid = wqh::grid_for(fn, kThreads, 0, tiles, wqh::kMaxPartials);
-    gptq_quant_kernel<SYM, G, SNR><<<grid, kThreads, 0, st>>>(w, n, k, qweight, qzeros, scales, g_idx, slots);
-    *grid_out = grid;
+    static bool attr_set = false;  // per-process; the attribute is per function
+    if (!attr_set) {
+        wq_status s = wqh::cuda_status(
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM));
+        if (s != WQ_OK) return s;
+        attr_set = true;
+    }
+    const int64_t warp_tiles = ((n + 31) / 32) * ((k + T::KT - 1) / T::KT);
+    const int grid = wqh::grid_for(fn, T::THREADS, T::SMEM, (warp_tiles + T::WARPS - 1) / T::WARPS,
+                                   wqh::kMaxPartials);
+    gptq_quant_kernel<SYM, G, SNR><<<grid, T::THREADS, T::SMEM, st>>>(
+        w, n, k, qweight, qzeros, scales, g_idx, slots, counter, snr_db);
     return wqh::check_launch();
 }
 
@@ -237,19 +223,21 @@ wq_status quantize(const uint16_t* w, int64_t n, int64_t k, int group, int32_t* 
         return WQ_ERR_WORKSPACE_TOO_SMALL;
     if (!wqh::aligned16(w) || !wqh::aligned16(qweight) || !wqh::aligned_to(scales, 2) ||
         (qzeros && !wqh::aligned_to(qzeros, 4)) || (g_idx && !wqh::aligned_to(g_idx, 4)) ||
-        (snr_db && !wqh::aligned_to(ws, 8)))
+        (snr_db && !wqh::aligned_to(ws, 256)))
         return WQ_ERR_MISALIGNED;
     cudaStream_t st = (cudaStream_t)stream;
-    double* slots = (double*)ws;
-    int grid = 0;
-    wq_status s;
+    unsigned* counter = snr_db ? (unsigned*)ws : nullptr;
+    double* slots = snr_db ? (double*)((char*)ws + wqh::kCtrlBytes) : nullptr;
+    if (snr_db) {
+        wq_status s0 = wqh::cuda_status(cudaMemsetAsync(counter, 0, sizeof(unsigned), st));
+        if (s0 != WQ_OK) return s0;
+    }
 #define WQ_GPTQ_CASE(GG)                                                                          \
     case GG:                                                                                      \
-        s = snr_db ? launch_quant<SYM, GG, true>(w, n, k, qweight, qzeros, scales, g_idx, slots,  \
-                                                 &grid, st)                                       \
-                   : launch_quant<SYM, GG, false>(w, n, k, qweight, qzeros, scales, g_idx, slots, \
-                                                  &grid, st);                                     \
-        break;
+        return snr_db ? launch_quant<SYM, GG, true>(w, n, k, qweight, qzeros, scales, g_idx,      \
+                                                    slots, counter, snr_db, st)                   \
+                      : launch_quant<SYM, GG, false>(w, n, k, qweight, qzeros, scales, g_idx,     \
+                                                     slots, counter, snr_db, st);
     switch (group) {
         WQ_GPTQ_CASE(32)
         WQ_GPTQ_CASE(64)
@@ -258,8 +246,6 @@ wq_status quantize(const uint16_t* w, int64_t n, int64_t k, int group, int32_t* 
         default: return WQ_ERR_UNSUPPORTED;
     }
 #undef WQ_GPTQ_CASE
-    if (s != WQ_OK || !snr_db) return s;
-    return wqh::launch_snr_finalize(slots, grid, snr_db, nullptr, st);
 }
 
 // ------------------------------------------------------------------ dequant

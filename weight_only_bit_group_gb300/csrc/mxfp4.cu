@@ -4,7 +4,8 @@
 // Layout: k % 32 == 0, so the 32-value blocks of a row-major [n, k] matrix are
 // consecutive in memory and the whole matrix is a flat stream of blocks.  One
 // thread takes one 16-byte chunk (8 bf16 values), four lanes make one block:
-//   load   uint4 (8 bf16)                -> 16 B per lane, 512 B per warp
+//   load   uint4 (8 bf16) by cp.async into a two-stage per-thread shared-memory
+//          pipeline (the next chunks stream in while these are coded)
 //   amax   16-bit SIMD max of |bf16| bit patterns, 2 shuffles over 4 lanes
 //   code   v = w * 2^-exp (exact), hardware cvt to e2m1x2 (round half even,
 //          saturate at 6) -- the e2m1 encoding IS the page's magnitude index
@@ -60,39 +61,57 @@ __global__ void __launch_bounds__(kThreads) mxfp4_quant_kernel(const uint4* __re
                                                                int64_t nchunks,
                                                                uint32_t* __restrict__ packed,
                                                                uint8_t* __restrict__ e8m0) {
+    // two pipeline stages of kUnroll 16-byte chunks, private to each thread
+    __shared__ __align__(16) uint4 stage_buf[2][kUnroll][kThreads];
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+    const int64_t step = nwarps * 32 * kUnroll;
+
+    auto issue = [&](int64_t wb, int st) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t c = wb + (int64_t)u * nwarps * 32 + lane;
+            if (c < nchunks) wq::cp_async16(&stage_buf[st][u][threadIdx.x], w + c);
+        }
+        wq::cp_async_commit();
+    };
+
     // Every lane of a warp runs the same trip count (shuffles below); lanes past
     // the end compute on zeros and store nothing.  nchunks % 4 == 0 and chunk
     // indices are 4-aligned per lane quad, so a quad is all-valid or all-invalid.
-    for (int64_t wb = warp * 32; wb < nchunks; wb += nwarps * 32 * kUnroll) {
+    issue(warp * 32, 0);
+    int j = 0;
+    for (int64_t wb = warp * 32; wb < nchunks; wb += step, ++j) {
+        issue(wb + step, (j + 1) & 1);
+        wq::cp_async_wait<1>();
         uint4 v[kUnroll];
         int64_t ch[kUnroll];
 #pragma unroll
-        for (int j = 0; j < kUnroll; ++j) {
-            ch[j] = wb + (int64_t)j * nwarps * 32 + lane;
-            v[j] = ch[j] < nchunks ? wq::ld_stream(w + ch[j]) : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < kUnroll; ++u) {
+            ch[u] = wb + (int64_t)u * nwarps * 32 + lane;
+            v[u] = ch[u] < nchunks ? stage_buf[j & 1][u][threadIdx.x] : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int j = 0; j < kUnroll; ++j) {
+        for (int u = 0; u < kUnroll; ++u) {
             const uint32_t M = 0x7fff7fffu;
-            uint32_t m2 = __vmaxu2(__vmaxu2(v[j].x & M, v[j].y & M), __vmaxu2(v[j].z & M, v[j].w & M));
+            uint32_t m2 = __vmaxu2(__vmaxu2(v[u].x & M, v[u].y & M), __vmaxu2(v[u].z & M, v[u].w & M));
             uint32_t a = max(m2 & 0xffffu, m2 >> 16);
             a = max(a, wq::shfl_xor(a, 1));
             a = max(a, wq::shfl_xor(a, 2));
             const int ex = exp_from_bf16_mag(a);
             const float inv = __uint_as_float((uint32_t)(127 - ex) << 23);  // 2^-exp, normal
-            uint32_t word = code_pair<TIE>(wq::bf_lo(v[j].x), wq::bf_hi(v[j].x), inv);
-            word |= code_pair<TIE>(wq::bf_lo(v[j].y), wq::bf_hi(v[j].y), inv) << 8;
-            word |= code_pair<TIE>(wq::bf_lo(v[j].z), wq::bf_hi(v[j].z), inv) << 16;
-            word |= code_pair<TIE>(wq::bf_lo(v[j].w), wq::bf_hi(v[j].w), inv) << 24;
-            if (ch[j] < nchunks) {
-                packed[ch[j]] = word;
-                if ((lane & 3) == 0) e8m0[ch[j] >> 2] = (uint8_t)(ex + 127);
+            uint32_t word = code_pair<TIE>(wq::bf_lo(v[u].x), wq::bf_hi(v[u].x), inv);
+            word |= code_pair<TIE>(wq::bf_lo(v[u].y), wq::bf_hi(v[u].y), inv) << 8;
+            word |= code_pair<TIE>(wq::bf_lo(v[u].z), wq::bf_hi(v[u].z), inv) << 16;
+            word |= code_pair<TIE>(wq::bf_lo(v[u].w), wq::bf_hi(v[u].w), inv) << 24;
+            if (ch[u] < nchunks) {
+                packed[ch[u]] = word;
+                if ((lane & 3) == 0) e8m0[ch[u] >> 2] = (uint8_t)(ex + 127);
             }
         }
     }
+    wq::cp_async_wait<0>();
 }
 
 // Two e2m1 nibbles of one byte -> two binary32 magnitudes with sign (exact).

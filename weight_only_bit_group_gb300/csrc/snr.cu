@@ -2,9 +2,9 @@
 // quantize_sym / quantize_asym: snr = 20*log10(||w|| / max(||w - deq||, 1e-12));
 // quantize_dflash_mxfp4.py main(): rel = ||deq - w|| / ||w||).
 //
-// Two passes, no atomics, deterministic for a given grid: every CTA writes its
-// (sum w^2, sum e^2) to its own workspace slot; one CTA adds the slots in index
-// order and evaluates the formulas.  Terms are binary32 (as the page computes
+// One pass, deterministic for a given grid: every CTA writes its (sum w^2,
+// sum e^2) to its own workspace slot; the last CTA to finish adds the slots in
+// index order and evaluates the formulas (nothing waits).  Terms are binary32 (as the page computes
 // them); sums are binary32 over at most 32 terms per thread and binary64 above.
 #include "wq_common.cuh"
 
@@ -12,25 +12,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
-
-// Sum two doubles over the CTA in a fixed order; thread 0 writes the slot.
-__device__ __forceinline__ void cta_store_pair(double a, double b, double* slot) {
-    __shared__ double sa[kThreads / 32], sb[kThreads / 32];
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) {
-        a += __shfl_xor_sync(0xffffffffu, a, m);
-        b += __shfl_xor_sync(0xffffffffu, b, m);
-    }
-    const int warp = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) { sa[warp] = a; sb[warp] = b; }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double ta = 0.0, tb = 0.0;
-        for (int i = 0; i < kThreads / 32; ++i) { ta += sa[i]; tb += sb[i]; }
-        slot[0] = ta;
-        slot[1] = tb;
-    }
-}
 
 template <int DEQ_BF16>
 __device__ __forceinline__ void load_deq8(const void* deq, int64_t c, float d[8]) {
@@ -52,7 +33,10 @@ __device__ __forceinline__ void load_deq8(const void* deq, int64_t c, float d[8]
 template <int DEQ_BF16>
 __global__ void __launch_bounds__(kThreads) snr_partial_nk(const uint4* __restrict__ w,
                                                            const void* __restrict__ deq,
-                                                           int64_t nchunks, double* __restrict__ slots) {
+                                                           int64_t nchunks, double* __restrict__ slots,
+                                                           unsigned* __restrict__ counter,
+                                                           double* __restrict__ snr_db,
+                                                           double* __restrict__ rel_err) {
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     double dw = 0.0, de = 0.0;
     for (int64_t base = (int64_t)blockIdx.x * kThreads + threadIdx.x; base < nchunks;
@@ -78,7 +62,7 @@ __global__ void __launch_bounds__(kThreads) snr_partial_nk(const uint4* __restri
         dw += (double)sw;
         de += (double)se;
     }
-    cta_store_pair(dw, de, slots + 2 * blockIdx.x);
+    wq::finish_snr(dw, de, slots, counter, snr_db, rel_err);
 }
 
 // deq laid out [k, n] (the GPTQ page's layout): 64 x 64 tiles, the deq tile is
@@ -88,7 +72,10 @@ constexpr int kT = 64;
 template <int DEQ_BF16>
 __global__ void __launch_bounds__(kThreads) snr_partial_kn(const uint16_t* __restrict__ w,
                                                            const void* __restrict__ deq, int64_t n,
-                                                           int64_t k, double* __restrict__ slots) {
+                                                           int64_t k, double* __restrict__ slots,
+                                                           unsigned* __restrict__ counter,
+                                                           double* __restrict__ snr_db,
+                                                           double* __restrict__ rel_err) {
     __shared__ float sd[kT][kT + 1];  // [k][n]
     const int64_t tiles_n = (n + kT - 1) / kT, tiles_k = (k + kT - 1) / kT;
     double dw = 0.0, de = 0.0;
@@ -135,44 +122,10 @@ __global__ void __launch_bounds__(kThreads) snr_partial_kn(const uint16_t* __res
         dw += (double)sw;
         de += (double)se;
     }
-    cta_store_pair(dw, de, slots + 2 * blockIdx.x);
-}
-
-__global__ void __launch_bounds__(kThreads) snr_finalize(const double* __restrict__ slots, int nslots,
-                                                         double* __restrict__ snr_db,
-                                                         double* __restrict__ rel_err) {
-    __shared__ double sa[kThreads], sb[kThreads];
-    double a = 0.0, b = 0.0;
-    for (int i = threadIdx.x; i < nslots; i += kThreads) {
-        a += slots[2 * i];
-        b += slots[2 * i + 1];
-    }
-    sa[threadIdx.x] = a;
-    sb[threadIdx.x] = b;
-    __syncthreads();
-    for (int s = kThreads / 2; s >= 1; s >>= 1) {
-        if (threadIdx.x < s) {
-            sa[threadIdx.x] += sa[threadIdx.x + s];
-            sb[threadIdx.x] += sb[threadIdx.x + s];
-        }
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-        const double nw = sqrt(sa[0]), ne = sqrt(sb[0]);
-        if (snr_db) *snr_db = 20.0 * log10(nw / fmax(ne, 1e-12));
-        if (rel_err) *rel_err = ne / nw;
-    }
+    wq::finish_snr(dw, de, slots, counter, snr_db, rel_err);
 }
 
 }  // namespace
-
-namespace wqh {
-wq_status launch_snr_finalize(const double* slots, int nslots, double* snr_db, double* rel_err,
-                              cudaStream_t st) {
-    snr_finalize<<<1, kThreads, 0, st>>>(slots, nslots, snr_db, rel_err);
-    return check_launch();
-}
-}  // namespace wqh
 
 extern "C" wq_status quant_snr(const uint16_t* w, const void* deq, int deq_dtype, int deq_layout,
                                int64_t n, int64_t k, double* snr_db, double* rel_err,
@@ -186,35 +139,45 @@ extern "C" wq_status quant_snr(const uint16_t* w, const void* deq, int deq_dtype
     if (!wqh::aligned16(w) || !wqh::aligned16(deq) || !wqh::aligned_to(workspace, 8))
         return WQ_ERR_MISALIGNED;
     if (deq_layout == WQ_LAYOUT_NK && (n * k) % 8 != 0) return WQ_ERR_BAD_SHAPE;
-    cudaStream_t st = (cudaStream_t)stream;
-    double* slots = (double*)workspace;
-    int grid = 1;
-    if (n * k > 0) {
-        if (deq_layout == WQ_LAYOUT_NK) {
-            const int64_t nchunks = n * k / 8;
-            const void* fn = deq_dtype == WQ_DTYPE_BF16 ? (const void*)snr_partial_nk<1>
-                                                        : (const void*)snr_partial_nk<0>;
-            grid = wqh::grid_for(fn, kThreads, 0, (nchunks + kThreads - 1) / kThreads, wqh::kMaxPartials);
-            if (deq_dtype == WQ_DTYPE_BF16)
-                snr_partial_nk<1><<<grid, kThreads, 0, st>>>((const uint4*)w, deq, nchunks, slots);
-            else
-                snr_partial_nk<0><<<grid, kThreads, 0, st>>>((const uint4*)w, deq, nchunks, slots);
-        } else {
-            const int64_t tiles = ((n + kT - 1) / kT) * ((k + kT - 1) / kT);
-            const void* fn = deq_dtype == WQ_DTYPE_BF16 ? (const void*)snr_partial_kn<1>
-                                                        : (const void*)snr_partial_kn<0>;
-            grid = wqh::grid_for(fn, kThreads, 0, tiles, wqh::kMaxPartials);
-            if (deq_dtype == WQ_DTYPE_BF16)
-                snr_partial_kn<1><<<grid, kThreads, 0, st>>>(w, deq, n, k, slots);
-            else
-                snr_partial_kn<0><<<grid, kThreads, 0, st>>>(w, deq, n, k, slots);
+    if (n == 0 || k == 0) {
+        // empty tensor: 20*log10(0 / 1e-12) = -inf, 0/0 = NaN, as torch gives
+        const double v[2] = {-INFINITY, NAN};
+        if (snr_db) {
+            wq_status s0 = wqh::cuda_status(cudaMemcpyAsync(snr_db, &v[0], sizeof(double),
+                                                            cudaMemcpyHostToDevice, (cudaStream_t)stream));
+            if (s0 != WQ_OK) return s0;
         }
-        wq_status s = wqh::check_launch();
-        if (s != WQ_OK) return s;
-    } else {
-        // empty tensor: one zero slot, so the finalize gives 20*log10(0/1e-12) = -inf
-        wq_status s = wqh::cuda_status(cudaMemsetAsync(slots, 0, 2 * sizeof(double), st));
-        if (s != WQ_OK) return s;
+        if (rel_err)
+            return wqh::cuda_status(cudaMemcpyAsync(rel_err, &v[1], sizeof(double),
+                                                    cudaMemcpyHostToDevice, (cudaStream_t)stream));
+        return WQ_OK;
     }
-    return wqh::launch_snr_finalize(slots, grid, snr_db, rel_err, st);
+    cudaStream_t st = (cudaStream_t)stream;
+    unsigned* counter = (unsigned*)workspace;
+    double* slots = (double*)((char*)workspace + wqh::kCtrlBytes);
+    wq_status s = wqh::cuda_status(cudaMemsetAsync(counter, 0, sizeof(unsigned), st));
+    if (s != WQ_OK) return s;
+    if (deq_layout == WQ_LAYOUT_NK) {
+        const int64_t nchunks = n * k / 8;
+        const void* fn = deq_dtype == WQ_DTYPE_BF16 ? (const void*)snr_partial_nk<1>
+                                                    : (const void*)snr_partial_nk<0>;
+        const int grid = wqh::grid_for(fn, kThreads, 0, (nchunks + kThreads - 1) / kThreads,
+                                       wqh::kMaxPartials);
+        if (deq_dtype == WQ_DTYPE_BF16)
+            snr_partial_nk<1><<<grid, kThreads, 0, st>>>((const uint4*)w, deq, nchunks, slots, counter,
+                                                          snr_db, rel_err);
+        else
+            snr_partial_nk<0><<<grid, kThreads, 0, st>>>((const uint4*)w, deq, nchunks, slots, counter,
+                                                          snr_db, rel_err);
+    } else {
+        const int64_t tiles = ((n + kT - 1) / kT) * ((k + kT - 1) / kT);
+        const void* fn = deq_dtype == WQ_DTYPE_BF16 ? (const void*)snr_partial_kn<1>
+                                                    : (const void*)snr_partial_kn<0>;
+        const int grid = wqh::grid_for(fn, kThreads, 0, tiles, wqh::kMaxPartials);
+        if (deq_dtype == WQ_DTYPE_BF16)
+            snr_partial_kn<1><<<grid, kThreads, 0, st>>>(w, deq, n, k, slots, counter, snr_db, rel_err);
+        else
+            snr_partial_kn<0><<<grid, kThreads, 0, st>>>(w, deq, n, k, slots, counter, snr_db, rel_err);
+    }
+    return wqh::check_launch();
 }

@@ -116,24 +116,39 @@ __device__ __forceinline__ void store_shards(const uint32_t (&blo)[8], const uin
 }
 
 template <int NBITS>
-__global__ void __launch_bounds__(kThreads) uintx_quant_fused(const uint16_t* __restrict__ w,
-                                                              int64_t numel, uint8_t* __restrict__ packed,
-                                                              uint16_t* __restrict__ scale,
-                                                              uint8_t* __restrict__ zp) {
+__global__ void __launch_bounds__(kThreads, 2) uintx_quant_fused(const uint16_t* __restrict__ w,
+                                                                 int64_t numel, uint8_t* __restrict__ packed,
+                                                                 uint16_t* __restrict__ scale,
+                                                                 uint8_t* __restrict__ zp) {
     constexpr int QMAX = (1 << NBITS) - 1;
+    // two pipeline stages x 8 segments x 16 bytes, private to each thread
+    extern __shared__ __align__(16) uint4 dyn_smem[];
+    uint4 (*stage_buf)[8][kThreads] = reinterpret_cast<uint4 (*)[8][kThreads]>(dyn_smem);
     const int64_t L1 = numel / 8;  // multiple of 64
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
     const int64_t items = (L1 + 255) / 256;
 
-    for (int64_t it = warp; it < items; it += nwarps) {
+    auto issue = [&](int64_t it, int st) {
+        const int64_t d = it * 256 + 8 * lane;
+        if (it < items && d < L1) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) wq::cp_async16(&stage_buf[st][m][threadIdx.x], w + m * L1 + d);
+        }
+        wq::cp_async_commit();
+    };
+
+    issue(warp, 0);
+    int j = 0;
+    for (int64_t it = warp; it < items; it += nwarps, ++j) {
+        issue(it + nwarps, (j + 1) & 1);
+        wq::cp_async_wait<1>();
         const int64_t d0 = it * 256, d = d0 + 8 * lane;
         const bool valid = d < L1;  // uniform over an octet (64 positions)
         uint4 v[8];
 #pragma unroll
-        for (int m = 0; m < 8; ++m)
-            v[m] = valid ? wq::ld_stream(w + m * L1 + d) : make_uint4(0, 0, 0, 0);
+        for (int m = 0; m < 8; ++m) v[m] = valid ? stage_buf[j & 1][m][threadIdx.x] : make_uint4(0, 0, 0, 0);
 
         float mn[8], mx[8];
 #pragma unroll
@@ -202,6 +217,7 @@ __global__ void __launch_bounds__(kThreads) uintx_quant_fused(const uint16_t* __
         }
         if (valid) store_shards<NBITS>(blo, bhi, packed, numel, L1, d);
     }
+    wq::cp_async_wait<0>();
 }
 
 // ----------------------------------------------------------- general path
@@ -416,8 +432,16 @@ wq_status quant_nbits(const uint16_t* w, int64_t numel, int group, uint8_t* pack
     if (group == 64 && numel % 512 == 0) {
         const int64_t items = (numel / 8 + 255) / 256;  // one per warp
         const void* fn = (const void*)uintx_quant_fused<NBITS>;
-        const int grid = wqh::grid_for(fn, kThreads, 0, (items + 7) / 8, 1 << 30);
-        uintx_quant_fused<NBITS><<<grid, kThreads, 0, st>>>(w, numel, packed, scale, zp);
+        constexpr int smem = 2 * 8 * kThreads * 16;
+        static bool attr_set = false;
+        if (!attr_set) {
+            wq_status s = wqh::cuda_status(
+                cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+            if (s != WQ_OK) return s;
+            attr_set = true;
+        }
+        const int grid = wqh::grid_for(fn, kThreads, smem, (items + 7) / 8, 1 << 30);
+        uintx_quant_fused<NBITS><<<grid, kThreads, smem, st>>>(w, numel, packed, scale, zp);
         return wqh::check_launch();
     }
     const int64_t ngroups = numel / group;

@@ -75,12 +75,109 @@ __device__ __forceinline__ float div_by_recip(float x, float s, float r) {
     return __fmaf_rn(rem, r, q0);
 }
 
+// ------------------------------------------------------------------ cp.async
+// 16-byte global -> shared copy that bypasses L1 (LDGSTS); completion is tracked
+// per thread by commit groups and awaited in hardware (no spin loop).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ------------------------------------------------------------------ f32x2
+// Packed binary32 pairs (Blackwell FFMA2/FMUL2/FADD2): each lane of the pair is
+// one IEEE binary32 operation, round to nearest even, subnormals kept.
+typedef unsigned long long f2_t;
+__device__ __forceinline__ f2_t f2(float lo, float hi) {
+    f2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2u(f2_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t mul2(f2_t a, f2_t b) {
+    f2_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t add2(f2_t a, f2_t b) {
+    f2_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c) {
+    f2_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+// The two bf16 of a packed word as a binary32 pair (exact).
+__device__ __forceinline__ f2_t bf2_to_f2(uint32_t u) {
+    return f2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
 // ------------------------------------------------------------------ warp
 __device__ __forceinline__ float shfl_xor(float v, int m) {
     return __shfl_xor_sync(0xffffffffu, v, m);
 }
 __device__ __forceinline__ uint32_t shfl_xor(uint32_t v, int m) {
     return __shfl_xor_sync(0xffffffffu, v, m);
+}
+
+// ------------------------------------------------------------------ reductions
+// CTA-wide fixed-order sum of a pair of doubles (kThreads = blockDim.x = 256).
+// The result is valid in thread 0 only.
+__device__ __forceinline__ void cta_sum_pair(double& a, double& b, double* sa, double* sb) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, m);
+        b += __shfl_xor_sync(0xffffffffu, b, m);
+    }
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) { sa[warp] = a; sb[warp] = b; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        a = 0.0;
+        b = 0.0;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) { a += sa[i]; b += sb[i]; }
+    }
+    __syncthreads();
+}
+
+// End of a two-level (sum w^2, sum e^2) reduction, with no waiting: each CTA
+// stores its pair in its own slot, publishes it (fence) and counts itself in;
+// the CTA that arrives last adds all slots in index order (deterministic for a
+// given grid) and writes snr_db = 20*log10(sqrt(Sw)/max(sqrt(Se),1e-12)) and
+// rel_err = sqrt(Se)/sqrt(Sw).  *counter must be 0 when the kernel starts.
+__device__ __forceinline__ void finish_snr(double a, double b, double* slots, unsigned* counter,
+                                           double* snr_db, double* rel_err) {
+    __shared__ double sa[32], sb[32];
+    __shared__ bool last;
+    cta_sum_pair(a, b, sa, sb);
+    if (threadIdx.x == 0) {
+        slots[2 * blockIdx.x] = a;
+        slots[2 * blockIdx.x + 1] = b;
+        __threadfence();
+        last = atomicAdd(counter, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    double ta = 0.0, tb = 0.0;
+    for (unsigned i = threadIdx.x; i < gridDim.x; i += blockDim.x) {
+        ta += __ldcg(slots + 2 * i);
+        tb += __ldcg(slots + 2 * i + 1);
+    }
+    cta_sum_pair(ta, tb, sa, sb);
+    if (threadIdx.x == 0) {
+        const double nw = sqrt(ta), ne = sqrt(tb);
+        if (snr_db) *snr_db = 20.0 * log10(nw / fmax(ne, 1e-12));
+        if (rel_err) *rel_err = ne / nw;
+    }
 }
 
 }  // namespace wq
@@ -100,14 +197,11 @@ wq_status check_launch();
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 inline bool aligned_to(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
-// Partial-sum slots: a CTA writes its binary64 partials to its own slot, a
-// one-CTA finalize kernel adds the slots in index order (deterministic for a
-// given grid).  Grids of reduction kernels never exceed this many CTAs.
+// Partial-sum slots: a CTA writes its binary64 partials to its own slot and the
+// last CTA to finish adds the slots in index order (deterministic for a given
+// grid).  Grids of reduction kernels never exceed this many CTAs.
 constexpr int kMaxPartials = 4096;
-
-// One-CTA reduction of `nslots` (sum w^2, sum e^2) slots into snr_db / rel_err
-// (either may be NULL).  Defined in snr.cu.
-wq_status launch_snr_finalize(const double* slots, int nslots, double* snr_db, double* rel_err,
-                              cudaStream_t st);
+// Workspace control block (arrival counter) ahead of the slots.
+constexpr size_t kCtrlBytes = 256;
 
 }  // namespace wqh
