@@ -174,6 +174,25 @@ wq_status awq_search(const uint16_t* w, int64_t n, int64_t k, const float* a,
                      float* best_s, int32_t* best_idx, float* best_alpha, double* errs,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* awq_search_static_scratch -- awq_search without a caller workspace.
+ * The paper has no counterpart: this is a convenience of this library for
+ * callers that cannot allocate device memory when they run the search (code
+ * inside another component's memory pool, framework plug-ins that must not
+ * allocate on their threads, paths that must not risk the device-wide
+ * synchronisation an allocation can cause).
+ * Same arguments and results as awq_search, minus workspace/workspace_bytes.
+ * Scratch: a fixed 2,687,232-byte array inside the library (held by every GPU
+ * that loads the library until the process exits), enough for k <= 16384 and
+ * n_alpha <= 16; larger k returns WQ_ERR_BAD_SHAPE before any launch.  The
+ * first call on a device (with that device current) looks the array's device
+ * address up once; make that first call before any stream capture.  Every call
+ * shares the array: calls that overlap on the GPU race and must be serialised by
+ * the caller.  Calls no allocation routine. */
+wq_status awq_search_static_scratch(const uint16_t* w, int64_t n, int64_t k, const float* a,
+                                    const float* alphas_host, int n_alpha, int max_rows,
+                                    int tie_mode, float* best_s, int32_t* best_idx,
+                                    float* best_alpha, double* errs, void* stream);
+
 /* ---------------------------------------------------------------- uintx
  * uintx_packed_bytes: size of the packed buffer for numel codes of nbits bits:
  * the sum over the power-of-two shards k in {4, 2, 1} present in nbits of
