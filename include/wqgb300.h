@@ -181,7 +181,7 @@ wq_status awq_search(const uint16_t* w, int64_t n, int64_t k, const float* a,
  * allocate on their threads, paths that must not risk the device-wide
  * synchronisation an allocation can cause).
  * Same arguments and results as awq_search, minus workspace/workspace_bytes.
- * Scratch: a fixed 2,687,232-byte array inside the library (held by every GPU
+ * Scratch: a fixed 2,883,840-byte array inside the library (held by every GPU
  * that loads the library until the process exits), enough for k <= 16384 and
  * n_alpha <= 16; larger k returns WQ_ERR_BAD_SHAPE before any launch.  The
  * first call on a device (with that device current) looks the array's device

@@ -6,21 +6,21 @@
 //                   err = sum over the row subsample of ((deq(quant(W*s)) / s - W) * a_c)^2
 //   best = first alpha with the strictly smallest err
 //
-// Four kernels on the caller's stream:
-//   awq_tables    grid (k/256, n_alpha): t = clamp(an^alpha, 1e-2, 1e2) and log t
-//                 per column and alpha (pow/log in binary64 rounded once to
-//                 binary32; mean(a_c) as a binary64 sum in a fixed order, the
-//                 same in every CTA), a_c [k].
-//   awq_norm      one CTA per alpha: exp(mean(log t)) (fixed-order binary64
-//                 sum), s = t / gm and RN(1/s).
+// Four kernels on the caller's stream (plus one memset of the arrival counter):
+//   awq_logs      a_c [k] and ln(an) per column (binary64; mean(a_c) as a
+//                 binary64 sum in a fixed order, the same in every CTA).
+//   awq_tables    grid (k/256, n_alpha): t = clamp(an^alpha, 1e-2, 1e2) per
+//                 column and alpha (binary64, rounded once to binary32) and
+//                 gm = exp(mean ln t) per alpha from the last CTA.
+//   awq_scale     s = t / gm and a_c / s for every column and alpha.
 //   awq_err       every subsampled weight is read once; all alphas are evaluated
-//                 in registers (4 rows x 8 columns per lane, s/1-s loaded once per
-//                 alpha for those 4 rows).  Per element and alpha: W*s, the
-//                 32-block amax by 2 quad shuffles, the exact block exponent,
-//                 hardware e2m1 rounding, exact dequant, the quotient by s (exact
-//                 reciprocal + one FMA correction), the weighted square.  Per-CTA
-//                 binary64 partials go to the workspace.
-//   awq_finalize  one CTA: partials added in index order, argmin, best_s copy.
+//                 in registers (4 rows x 8 columns per lane, s and a_c/s loaded
+//                 once per alpha for those 4 rows).  Per element and alpha: W*s,
+//                 the 32-block amax by 2 quad shuffles, the exact block exponent,
+//                 hardware e2m1 rounding, the exact quantization error, the
+//                 weighted square.  Per-CTA binary64 partials go to the
+//                 workspace; the last CTA adds them in index order, takes the
+//                 argmin and copies best_s.
 #include "wq_common.cuh"
 
 namespace {
@@ -49,48 +49,96 @@ __device__ double block_sum_256(double v, double* red) {
     return red[kThreads / 32];
 }
 
-// Grid (ceil(k/256), n_alpha).  Every CTA forms mean(a_c) in the same fixed
-// order (so all agree bit for bit), then for its 256 columns and its alpha:
-// t = clamp(an^alpha, 1e-2, 1e2) -> t_tab, log(t) rounded to binary32 -> l_tab.
-__global__ void __launch_bounds__(kThreads) awq_tables(const float* __restrict__ a, int64_t k,
-                                                       AlphaList al, float* __restrict__ t_tab,
-                                                       float* __restrict__ l_tab,
-                                                       float* __restrict__ a_c) {
+// Grid ceil(k/256).  Every CTA forms mean(a_c) in the same fixed order (so all
+// agree bit for bit), then for its columns a_c and L = ln(an) in binary64.
+__global__ void __launch_bounds__(kThreads) awq_logs(const float* __restrict__ a, int64_t k,
+                                                     float* __restrict__ a_c,
+                                                     double* __restrict__ lan) {
     __shared__ double red[kThreads / 32 + 1];
-    double part = 0.0;
-    for (int64_t c = threadIdx.x; c < k; c += kThreads) part += (double)fmaxf(__ldg(a + c), 1e-8f);
-    const float mean = (float)(block_sum_256(part, red) / (double)k);
+    double ps = 0.0;
+    for (int64_t c = threadIdx.x; c < k; c += kThreads) ps += (double)fmaxf(__ldg(a + c), 1e-8f);
+    const float mean = (float)(block_sum_256(ps, red) / (double)k);
     const int64_t c = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const int i = blockIdx.y;
     if (c < k) {
         const float ac = fmaxf(__ldg(a + c), 1e-8f);
-        if (i == 0) a_c[c] = ac;
+        a_c[c] = ac;
         const float an = __fdiv_rn(ac, mean);
-        float t = (float)pow((double)an, (double)al.v[i]);
-        t = fminf(fmaxf(t, 1e-2f), 1e2f);
-        t_tab[(int64_t)i * k + c] = t;
-        l_tab[(int64_t)i * k + c] = (float)log((double)t);
+        lan[c] = log((double)an);
+        reinterpret_cast<float*>(lan + k)[c] = an;  // an itself, for alpha = 1
     }
 }
 
-// One CTA per alpha: gm = exp(mean(log t)) from the binary32 logs (binary64 sum
-// in a fixed order), then s = t / gm and r = RN(1/s).  r_tab holds the logs on
-// entry (all read before any is overwritten).
-__global__ void __launch_bounds__(kThreads) awq_norm(int64_t k, float* __restrict__ s_tab,
-                                                     float* __restrict__ r_tab) {
+// Grid (ceil(k/256), n_alpha): t = an^alpha = exp(alpha * L) in binary64 (alpha
+// = 0 and 1 give exactly 1 and an), rounded once to binary32 and clamped to
+// [1e-2, 1e2]; then ln t of the binary32 t, rounded to binary32.  ln t comes from
+// the binary64 exp already at hand: ln(t32) = alpha*L + ln(t32/t64) and
+// t32/t64 - 1 is below 2^-24, so the first-order term carries it to far below
+// binary32 resolution.  Each CTA adds its columns' logs (fixed order) into its
+// own slot; the last CTA to finish adds, per alpha, the slots in index order and
+// stores gm[alpha] = exp(mean ln t) rounded to binary32.
+__global__ void __launch_bounds__(kThreads) awq_tables(int64_t k, AlphaList al, int n_alpha,
+                                                       const double* __restrict__ lan,
+                                                       float* __restrict__ t_tab,
+                                                       double* __restrict__ part,
+                                                       float* __restrict__ gm,
+                                                       unsigned* __restrict__ counter) {
     __shared__ double red[kThreads / 32 + 1];
-    const int i = blockIdx.x;
-    float* s = s_tab + (int64_t)i * k;
-    float* r = r_tab + (int64_t)i * k;
-    double part = 0.0;
-    for (int64_t c = threadIdx.x; c < k; c += kThreads) part += (double)r[c];
-    const float lmean = (float)(block_sum_256(part, red) / (double)k);
-    const float gm = (float)exp((double)lmean);
-    for (int64_t c = threadIdx.x; c < k; c += kThreads) {
-        const float sv = __fdiv_rn(s[c], gm);
-        s[c] = sv;
-        r[c] = __frcp_rn(sv);
+    __shared__ bool last;
+    const int64_t c = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int i = blockIdx.y;
+    const bool valid = c < k;
+    const float alpha = al.v[i];
+    double td = 1.0, lt = 0.0;
+    if (valid) {
+        const double L = lan[c];
+        if (alpha == 1.0f) {
+            td = (double)reinterpret_cast<const float*>(lan + k)[c];
+            lt = L;
+        } else if (alpha != 0.0f) {
+            lt = (double)alpha * L;
+            td = exp(lt);
+        }
     }
+    float t = (float)td;
+    if (t < 1e-2f) {
+        t = 1e-2f;
+        lt = log((double)1e-2f);
+    } else if (t > 1e2f) {
+        t = 1e2f;
+        lt = log((double)1e2f);
+    } else {
+        lt += ((double)t - td) / td;
+    }
+    if (valid) t_tab[(int64_t)i * k + c] = t;
+    const double cta = block_sum_256(valid ? (double)(float)lt : 0.0, red);
+    if (threadIdx.x == 0) {
+        part[(int64_t)i * gridDim.x + blockIdx.x] = cta;
+        __threadfence();
+        last = atomicAdd(counter, 1u) == gridDim.x * gridDim.y - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    if (threadIdx.x < n_alpha) {
+        double v = 0.0;
+        for (unsigned b = 0; b < gridDim.x; ++b) v += __ldcg(part + (int64_t)threadIdx.x * gridDim.x + b);
+        const float lmean = (float)(v / (double)k);
+        gm[threadIdx.x] = (float)exp((double)lmean);
+    }
+    if (threadIdx.x == 0) *counter = 0u;  // every other CTA has counted itself in: ready for awq_err
+}
+
+// Grid (ceil(k/256), n_alpha): s = t / gm (IEEE) and q = a_c / s.
+__global__ void __launch_bounds__(kThreads) awq_scale(int64_t k, const float* __restrict__ gm,
+                                                      const float* __restrict__ a_c,
+                                                      float* __restrict__ s_tab,
+                                                      float* __restrict__ q_tab) {
+    const int64_t c = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int i = blockIdx.y;
+    if (c >= k) return;
+    const float sv = __fdiv_rn(s_tab[(int64_t)i * k + c], __ldcg(gm + i));
+    s_tab[(int64_t)i * k + c] = sv;
+    q_tab[(int64_t)i * k + c] = __fdiv_rn(a_c[c], sv);
 }
 
 // exp = clamp(floor(log2(amax)) - 2, -127, 127) for a binary32 amax >= 0 (0 -> 0).
@@ -123,26 +171,37 @@ __device__ __forceinline__ uint32_t page_tie(uint32_t nib, float v) {
     return (m == 0.75f || m == 1.75f || m == 3.5f) ? nib - 2u : nib;
 }
 
+// Per element and alpha the page's error term is e = (deq/s - w) * a_c.  Here it
+// is evaluated as (deq - ws) * (a_c/s) with ws = w*s the value that was
+// quantized: algebraically the same product, without a division per element.
+// deq - ws is exact: with v = ws * 2^-exp (exact), deq - ws = (e2m1(v) - v) *
+// 2^exp and e2m1(v) - v is an exact difference (the two lie within a factor two
+// of each other, or e2m1(v) = 0).  The terms therefore differ from the page's
+// only by the rounding of ws and of the final products (relative 1e-7), far
+// inside the 1e-4 agreement required of the errors.
 template <int TIE>
 __global__ void __launch_bounds__(kThreads) awq_err(const uint16_t* __restrict__ w, int64_t k,
                                                     int64_t rows, int64_t row_stride, int n_alpha,
-                                                    const float* __restrict__ s_tab,
-                                                    const float* __restrict__ r_tab,
-                                                    const float* __restrict__ a_c,
-                                                    double* __restrict__ slots) {
+                                                    AlphaList al, const float* __restrict__ s_tab,
+                                                    const float* __restrict__ q_tab,
+                                                    double* __restrict__ slots,
+                                                    unsigned* __restrict__ counter,
+                                                    float* __restrict__ best_s,
+                                                    int32_t* __restrict__ best_idx,
+                                                    float* __restrict__ best_alpha,
+                                                    double* __restrict__ errs) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t gwarp = (int64_t)blockIdx.x * (kThreads / 32) + warp;
     const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
     const int64_t col_chunks = (k + 255) / 256;
     const int64_t row_batches = (rows + kRowsPerLane - 1) / kRowsPerLane;
 
-    double acc[kMaxAlpha];
-#pragma unroll
-    for (int i = 0; i < kMaxAlpha; ++i) acc[i] = 0.0;
+    wq::KSum acc[kMaxAlpha];  // compensated binary32 sums (the binary64 pipe is narrow)
 
     for (int64_t it = gwarp; it < col_chunks * row_batches; it += nwarps) {
-        const int64_t col = (it % col_chunks) * 256 + 8 * lane;
-        const int64_t r0 = (it / col_chunks) * kRowsPerLane;
+        const int64_t rb = it / col_chunks;  // once per 32 x 4 values, all alphas
+        const int64_t col = (it - rb * col_chunks) * 256 + 8 * lane;
+        const int64_t r0 = rb * kRowsPerLane;
         const bool cval = col < k;  // k % 32 == 0: a lane quad is valid or not as a whole
         uint4 wv[kRowsPerLane];
 #pragma unroll
@@ -151,41 +210,32 @@ __global__ void __launch_bounds__(kThreads) awq_err(const uint16_t* __restrict__
             wv[q] = (cval && r < rows) ? wq::ld_stream(w + (r * row_stride) * k + col)
                                        : make_uint4(0, 0, 0, 0);
         }
-        float ac[8];
-        {
-            const float4 a0 = cval ? __ldg(reinterpret_cast<const float4*>(a_c + col)) : make_float4(0, 0, 0, 0);
-            const float4 a1 = cval ? __ldg(reinterpret_cast<const float4*>(a_c + col) + 1) : make_float4(0, 0, 0, 0);
-            ac[0] = a0.x; ac[1] = a0.y; ac[2] = a0.z; ac[3] = a0.w;
-            ac[4] = a1.x; ac[5] = a1.y; ac[6] = a1.z; ac[7] = a1.w;
-        }
 #pragma unroll
         for (int i = 0; i < kMaxAlpha; ++i) {
             if (i >= n_alpha) break;
-            float s[8], rr[8];
+            float s[8], qa[8];
             {
-                const float4* sp = reinterpret_cast<const float4*>(s_tab + (int64_t)i * k + (cval ? col : 0));
-                const float4* rp = reinterpret_cast<const float4*>(r_tab + (int64_t)i * k + (cval ? col : 0));
-                const float4 s0 = __ldg(sp), s1 = __ldg(sp + 1), q0 = __ldg(rp), q1 = __ldg(rp + 1);
+                const int64_t off = (int64_t)i * k + (cval ? col : 0);
+                const float4 s0 = __ldg(reinterpret_cast<const float4*>(s_tab + off));
+                const float4 s1 = __ldg(reinterpret_cast<const float4*>(s_tab + off) + 1);
+                const float4 q0 = cval ? __ldg(reinterpret_cast<const float4*>(q_tab + off)) : make_float4(0, 0, 0, 0);
+                const float4 q1 = cval ? __ldg(reinterpret_cast<const float4*>(q_tab + off) + 1) : make_float4(0, 0, 0, 0);
                 s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
                 s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
-                rr[0] = q0.x; rr[1] = q0.y; rr[2] = q0.z; rr[3] = q0.w;
-                rr[4] = q1.x; rr[5] = q1.y; rr[6] = q1.z; rr[7] = q1.w;
+                qa[0] = q0.x; qa[1] = q0.y; qa[2] = q0.z; qa[3] = q0.w;
+                qa[4] = q1.x; qa[5] = q1.y; qa[6] = q1.z; qa[7] = q1.w;
             }
             float part = 0.0f;
 #pragma unroll
             for (int q = 0; q < kRowsPerLane; ++q) {
                 const uint32_t u[4] = {wv[q].x, wv[q].y, wv[q].z, wv[q].w};
-                float x[8], ws[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    x[2 * j] = wq::bf_lo(u[j]);
-                    x[2 * j + 1] = wq::bf_hi(u[j]);
-                }
+                float ws[8];
                 float amax = 0.0f;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    ws[j] = __fmul_rn(x[j], s[j]);
-                    amax = fmaxf(amax, fabsf(ws[j]));
+                for (int j = 0; j < 4; ++j) {
+                    ws[2 * j] = __fmul_rn(wq::bf_lo(u[j]), s[2 * j]);
+                    ws[2 * j + 1] = __fmul_rn(wq::bf_hi(u[j]), s[2 * j + 1]);
+                    amax = fmaxf(amax, fmaxf(fabsf(ws[2 * j]), fabsf(ws[2 * j + 1])));
                 }
                 amax = fmaxf(amax, wq::shfl_xor(amax, 1));
                 amax = fmaxf(amax, wq::shfl_xor(amax, 2));
@@ -199,24 +249,24 @@ __global__ void __launch_bounds__(kThreads) awq_err(const uint16_t* __restrict__
                     if (TIE == WQ_TIE_PAGE_LITERAL) b = page_tie(b & 15u, v0) | (page_tie(b >> 4, v1) << 4);
                     float m0, m1;
                     e2m1x2_to_f(b, m0, m1);
-                    const float d0 = __fmul_rn(m0, sc), d1 = __fmul_rn(m1, sc);
-                    const float q0 = wq::div_by_recip(d0, s[2 * j], rr[2 * j]);
-                    const float q1 = wq::div_by_recip(d1, s[2 * j + 1], rr[2 * j + 1]);
-                    const float e0 = __fmul_rn(__fsub_rn(q0, x[2 * j]), ac[2 * j]);
-                    const float e1 = __fmul_rn(__fsub_rn(q1, x[2 * j + 1]), ac[2 * j + 1]);
-                    part = __fadd_rn(part, __fmul_rn(e0, e0));
-                    part = __fadd_rn(part, __fmul_rn(e1, e1));
+                    const float e0 = __fmul_rn(__fmul_rn(__fsub_rn(m0, v0), sc), qa[2 * j]);
+                    const float e1 = __fmul_rn(__fmul_rn(__fsub_rn(m1, v1), sc), qa[2 * j + 1]);
+                    part = __fmaf_rn(e0, e0, part);
+                    part = __fmaf_rn(e1, e1, part);
                 }
             }
-            acc[i] += (double)part;
+            acc[i].add(part);
         }
     }
 
-    // CTA partial per alpha, fixed order
+    // CTA partial per alpha, fixed order; the last CTA to finish reduces them all
     __shared__ double red[kThreads / 32][kMaxAlpha];
+    __shared__ double e[kMaxAlpha];
+    __shared__ bool last;
+    __shared__ int best;
 #pragma unroll
     for (int i = 0; i < kMaxAlpha; ++i) {
-        double v = acc[i];
+        double v = acc[i].value();
 #pragma unroll
         for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
         if (lane == 0) red[warp][i] = v;
@@ -226,23 +276,17 @@ __global__ void __launch_bounds__(kThreads) awq_err(const uint16_t* __restrict__
         double t = 0.0;
         for (int wgi = 0; wgi < kThreads / 32; ++wgi) t += red[wgi][threadIdx.x];
         slots[(int64_t)blockIdx.x * n_alpha + threadIdx.x] = t;
+        __threadfence();
     }
-}
-
-__global__ void __launch_bounds__(kThreads) awq_finalize(const double* __restrict__ slots, int nslots,
-                                                         int n_alpha, AlphaList al, int64_t k,
-                                                         const float* __restrict__ s_tab,
-                                                         float* __restrict__ best_s,
-                                                         int32_t* __restrict__ best_idx,
-                                                         float* __restrict__ best_alpha,
-                                                         double* __restrict__ errs) {
-    __shared__ double e[kMaxAlpha];
-    __shared__ int best;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(counter, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
     // warp w sums alphas w, w + 8: lane-strided slots, then a fixed shuffle tree
     for (int i = warp; i < n_alpha; i += kThreads / 32) {
         double t = 0.0;
-        for (int b = lane; b < nslots; b += 32) t += slots[(int64_t)b * n_alpha + i];
+        for (unsigned b = lane; b < gridDim.x; b += 32) t += __ldcg(slots + (int64_t)b * n_alpha + i);
 #pragma unroll
         for (int m = 16; m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
         if (lane == 0) e[i] = t;
@@ -259,7 +303,7 @@ __global__ void __launch_bounds__(kThreads) awq_finalize(const double* __restric
     __syncthreads();
     if (errs && threadIdx.x < n_alpha) errs[threadIdx.x] = e[threadIdx.x];
     if (best_s)
-        for (int64_t c = threadIdx.x; c < k; c += kThreads) best_s[c] = s_tab[(int64_t)best * k + c];
+        for (int64_t c = threadIdx.x; c < k; c += kThreads) best_s[c] = __ldcg(s_tab + (int64_t)best * k + c);
 }
 
 }  // namespace
@@ -291,31 +335,37 @@ extern "C" wq_status awq_search(const uint16_t* w, int64_t n, int64_t k, const f
     auto up = [](size_t b) { return (b + 255) & ~(size_t)255; };
     char* ws = (char*)workspace + wqh::kCtrlBytes;
     float* s_tab = (float*)ws;
-    float* r_tab = (float*)(ws + up((size_t)n_alpha * k * sizeof(float)));
+    float* r_tab = (float*)(ws + up((size_t)n_alpha * k * sizeof(float)));  // a_c / s
     float* a_c = (float*)(ws + 2 * up((size_t)n_alpha * k * sizeof(float)));
-    double* slots = (double*)(ws + 2 * up((size_t)n_alpha * k * sizeof(float)) + up((size_t)k * sizeof(float)));
+    double* lan = (double*)(ws + 2 * up((size_t)n_alpha * k * sizeof(float)) + up((size_t)k * sizeof(float)));
+    double* slots = (double*)((char*)lan + up((size_t)k * (sizeof(double) + sizeof(float))));
 
     cudaStream_t st = (cudaStream_t)stream;
-    awq_tables<<<dim3((unsigned)((k + kThreads - 1) / kThreads), (unsigned)n_alpha), kThreads, 0, st>>>(
-        a, k, al, s_tab, r_tab, a_c);
-    wq_status s = wqh::check_launch();
+    unsigned* counter = (unsigned*)workspace;
+    float* gm = (float*)((char*)workspace + 64);  // n_alpha <= 16 floats in the control block
+    wq_status s = wqh::cuda_status(cudaMemsetAsync(counter, 0, sizeof(unsigned), st));
     if (s != WQ_OK) return s;
-    awq_norm<<<n_alpha, kThreads, 0, st>>>(k, s_tab, r_tab);
+    const unsigned col_ctas = (unsigned)((k + kThreads - 1) / kThreads);
+    awq_logs<<<col_ctas, kThreads, 0, st>>>(a, k, a_c, lan);
     s = wqh::check_launch();
     if (s != WQ_OK) return s;
-
+    awq_tables<<<dim3(col_ctas, (unsigned)n_alpha), kThreads, 0, st>>>(k, al, n_alpha, lan, s_tab, slots, gm,
+                                                                        counter);
+    s = wqh::check_launch();
+    if (s != WQ_OK) return s;
+    awq_scale<<<dim3(col_ctas, (unsigned)n_alpha), kThreads, 0, st>>>(k, gm, a_c, s_tab, r_tab);
+    s = wqh::check_launch();
+    if (s != WQ_OK) return s;
     const int64_t items = ((k + 255) / 256) * ((rows + kRowsPerLane - 1) / kRowsPerLane);
     const int64_t ctas = (items + (kThreads / 32) - 1) / (kThreads / 32);
-    int grid;
     if (tie_mode == WQ_TIE_HALF_EVEN) {
-        grid = wqh::grid_for((const void*)awq_err<WQ_TIE_HALF_EVEN>, kThreads, 0, ctas, wqh::kMaxPartials);
-        awq_err<WQ_TIE_HALF_EVEN><<<grid, kThreads, 0, st>>>(w, k, rows, stride, n_alpha, s_tab, r_tab, a_c, slots);
+        const int grid = wqh::grid_for((const void*)awq_err<WQ_TIE_HALF_EVEN>, kThreads, 0, ctas, wqh::kMaxPartials);
+        awq_err<WQ_TIE_HALF_EVEN><<<grid, kThreads, 0, st>>>(w, k, rows, stride, n_alpha, al, s_tab, r_tab,
+                                                             slots, counter, best_s, best_idx, best_alpha, errs);
     } else {
-        grid = wqh::grid_for((const void*)awq_err<WQ_TIE_PAGE_LITERAL>, kThreads, 0, ctas, wqh::kMaxPartials);
-        awq_err<WQ_TIE_PAGE_LITERAL><<<grid, kThreads, 0, st>>>(w, k, rows, stride, n_alpha, s_tab, r_tab, a_c, slots);
+        const int grid = wqh::grid_for((const void*)awq_err<WQ_TIE_PAGE_LITERAL>, kThreads, 0, ctas, wqh::kMaxPartials);
+        awq_err<WQ_TIE_PAGE_LITERAL><<<grid, kThreads, 0, st>>>(w, k, rows, stride, n_alpha, al, s_tab, r_tab,
+                                                                slots, counter, best_s, best_idx, best_alpha, errs);
     }
-    s = wqh::check_launch();
-    if (s != WQ_OK) return s;
-    awq_finalize<<<1, kThreads, 0, st>>>(slots, grid, n_alpha, al, k, s_tab, best_s, best_idx, best_alpha, errs);
     return wqh::check_launch();
 }

@@ -29,10 +29,10 @@ constexpr int kStaticMaxAlpha = 16;
 
 // Workspace layout of awq_search for k = 16384, n_alpha = 16 (see
 // wq_workspace_bytes): control block, two [16][16384] binary32 tables,
-// a_c [16384], 4096 x 16 binary64 partials.
+// a_c [16384], ln(an) and an [16384], 4096 x 16 binary64 partials.
 constexpr size_t kStaticScratchBytes =
     256 + 2 * (size_t)kStaticMaxAlpha * kStaticMaxK * 4 + (size_t)kStaticMaxK * 4 +
-    (size_t)4096 * kStaticMaxAlpha * 8;
+    (size_t)kStaticMaxK * 12 + (size_t)4096 * kStaticMaxAlpha * 8;
 
 static __device__ __align__(256) unsigned char g_awq_scratch[kStaticScratchBytes];
 

@@ -111,9 +111,9 @@ extern "C" int64_t uintx_packed_bytes(int64_t numel, int nbits) {
 // Workspace layouts (all offsets 256-byte aligned):
 //   GPTQ quantize with SNR, quant_snr: control block (arrival counter) |
 //               kMaxPartials x 2 doubles of per-CTA sums.
-//   awq_search: control block | s table [n_alpha][k] f32 | 1/s table
-//               [n_alpha][k] f32 | a_c [k] f32 | per-CTA partials
-//               kMaxPartials x n_alpha doubles.
+//   awq_search: control block | s table [n_alpha][k] f32 | a_c/s table
+//               [n_alpha][k] f32 | a_c [k] f32 | ln(an) [k] f64 + an [k] f32 |
+//               per-CTA partials kMaxPartials x n_alpha doubles.
 extern "C" size_t wq_workspace_bytes(int op, int64_t n, int64_t k, int arg) {
     (void)n;
     auto up = [](size_t b) { return (b + 255) & ~(size_t)255; };
@@ -125,6 +125,7 @@ extern "C" size_t wq_workspace_bytes(int op, int64_t n, int64_t k, int arg) {
             if (arg < 1 || k < 0) return 0;
             size_t tab = up((size_t)arg * (size_t)k * sizeof(float));
             return wqh::kCtrlBytes + 2 * tab + up((size_t)k * sizeof(float)) +
+                   up((size_t)k * (sizeof(double) + sizeof(float))) +
                    up((size_t)wqh::kMaxPartials * (size_t)arg * sizeof(double));
         }
         default:

@@ -2,40 +2,46 @@
 // (export_gptq_cpu.py: pack_int32, quantize_sym, quantize_asym; module docstring
 // for the uint4b8 dequant rule).
 //
-// Quantize: a warp owns a tile of 32 output channels (rows of w) x KT input
-// channels (KT = 128, or the group when it is larger) and lane l owns row
-// n0 + l.  The tile arrives in shared memory through a two-stage per-warp
-// cp.async pipeline (each copy instruction moves two whole 256-byte row
-// segments, fully coalesced; rows are padded to 272 bytes so the per-lane
-// reads are bank-conflict free) while the previous tile is computed.  A lane
-// holds whole groups of its row, so the group max/min is an in-thread bf16x2
-// reduction and the scale / zero point are computed once per group with true
-// IEEE divisions.  Per element: the quotient by the scale from a correctly
-// rounded reciprocal plus one FMA correction (bit-identical to IEEE division),
-// the clamp to [-zp, 15-zp] (exact before rounding, the bounds are integers),
-// round-half-even by the binary32 adder (x + 1.5*2^23), and the nibble pack as
-// one IMAD per element.  The eight codes along k of one row are one qweight
-// word, so the 32 lanes store 32 consecutive qweight columns (128 bytes) per
-// word row -- the [K/8, N] transpose costs nothing.  Packed-pair (f32x2) math
-// halves the issue slots of the arithmetic.  The optional reconstruction SNR
-// is accumulated from the same registers and reduced by the last CTA.
+// Quantize.  A warp owns a tile of 16 output channels (rows of w) x 128 input
+// channels (256 for group 256); lanes 2r and 2r+1 own row n0 + r, each half of
+// the tile's input channels.  Tiles are numbered K-fastest, so the warps that
+// run at the same time sweep long contiguous stretches of the same rows.  A tile
+// arrives in shared memory through a two-stage per-warp cp.async pipeline (each
+// copy instruction moves two whole 256-byte row segments into 256-byte aligned,
+// XOR-swizzled rows, so the per-lane reads are bank-conflict free) while the
+// previous tile is coded.  The group max/min is a bf16x2 reduction inside the lane (plus
+// one shuffle when a group spans the lane pair); scale and zero point use true
+// IEEE divisions once per group.  Per element pair, with packed binary32 pairs
+// (f32x2): the clamp to the code range is applied to w itself, in bf16x2, with
+// bounds bf16(lo*s) and bf16(hi*s) (exact, see bound2); the quotient by the
+// scale is a correctly rounded reciprocal plus one FMA correction step
+// (bit-identical to IEEE division); round-half-even comes from the binary32
+// adder (q + 1.5*2^23); the nibble pack is one IMAD per code.  The eight codes
+// along k of one row are one qweight word, so the [K/8, N] transpose costs
+// nothing.  The optional reconstruction SNR is accumulated from the same
+// registers and reduced by the last CTA to finish.
 #include "wq_common.cuh"
 
 namespace {
 
 constexpr int kThreads = 256;  // dequant kernels
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr float kRcp15 = 1.0f / 15.0f;  // RN(1/15), correctly rounded by the compiler
 
 template <int G>
 struct QTile {
-    static constexpr int KT = G < 128 ? 128 : G;     // input channels per warp tile
-    static constexpr int CH = KT / 8;                 // 16-byte chunks per row
-    static constexpr int ROWB = KT * 2 + 16;          // padded shared-memory row
-    static constexpr int STAGE = 32 * ROWB;           // one stage of one warp
-    static constexpr int NS = 2;                      // pipeline stages
-    static constexpr int WARPS = KT > 128 ? 2 : 4;    // warps per CTA
+    static constexpr int KT = G > 128 ? G : 128;      // input channels per warp tile
+    static constexpr int R = 16;                       // output channels per warp tile
+    static constexpr int HALF = KT / 2;                // input channels per lane (2 lanes per row)
+    static constexpr int GL = G < HALF ? G : HALF;     // group elements one lane holds
+    static constexpr int LPG = G / GL;                 // lanes per group (1 or 2)
+    static constexpr int CH = KT / 8;                  // 16-byte chunks per row
+    static constexpr int ROWB = KT * 2;                // shared-memory row (swizzled, unpadded)
+    static constexpr int STAGE = R * ROWB;             // one stage of one warp
+    static constexpr int NS = 2;                       // pipeline stages
+    static constexpr int WARPS = 4;                    // warps per CTA
     static constexpr int THREADS = 32 * WARPS;
-    static constexpr int SMEM = NS * WARPS * STAGE;
+    static constexpr int SMEM = NS * WARPS * STAGE + 1024;  // + room to align the base to 1 KB
 };
 
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
@@ -48,144 +54,234 @@ __device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
     asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
+// |a| max |b| per bf16 half (sign bits are garbage: callers mask them).
+__device__ __forceinline__ uint32_t babsmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
 
+// Per-group constants of the code computation.
+struct GroupConst {
+    float s;        // binary32 scale
+    float zp;       // zero point (8 for sym)
+    uint32_t lo2;   // bf16x2 lower clamp bound on w: bf16(-zp * s), both halves
+    uint32_t hi2;   // bf16x2 upper clamp bound on w: bf16((15 - zp) * s)
+};
+
+// Clamping w to [bf16(lo*s), bf16(hi*s)] before dividing gives exactly the
+// page's clamp(round(w/s), lo, hi): a bf16 bound is off lo*s (hi*s) by at most
+// 2^-8 relative, i.e. by less than 15 * 2^-8 < 0.5 code steps, so every w that
+// moves rounds to the same end code either way.
+__device__ __forceinline__ uint32_t bound2(float v) {
+    const uint32_t b = wq::f_to_bf(v);
+    return b | (b << 16);
+}
+
+// Codes of one 8-value chunk (one qweight word) and the SNR terms, on packed
+// binary32 pairs.  Per value: clamp (bf16x2, on w), q = RN(w/s) by reciprocal +
+// correction, t = rint(q) + 1.5*2^23 from the binary32 adder; the low bits of
+// t hold rint(q), and the word is sum over i of bits(t_i) << 4i plus the
+// per-group constant cg = (zp - bits(1.5*2^23)) * 0x11111111 (mod 2^32).
+template <bool SYM, bool SNR>
+__device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst& gc, const wq::f2_t R2,
+                                                const wq::f2_t NS2, uint32_t cg, wq::f2_t& sw2,
+                                                wq::f2_t& se2) {
+    const wq::f2_t M2 = wq::f2(kMagic, kMagic), NM2 = wq::f2(-kMagic, -kMagic);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    uint32_t word = cg;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        uint32_t uc = bmin2(u[p], gc.hi2);
+        if (!SYM) uc = bmax2(uc, gc.lo2);  // sym: w/s >= -8 always
+        const wq::f2_t x = wq::bf2_to_f2(uc);
+        const wq::f2_t qa = wq::mul2(x, R2);
+        const wq::f2_t rem = wq::fma2(qa, NS2, x);                          // x - qa*s, exact
+        const wq::f2_t tq = wq::add2(wq::fma2(rem, R2, qa), M2);            // rint(RN(x/s)) + 1.5*2^23
+        float t0, t1;
+        wq::f2u(tq, t0, t1);
+        word += (uint32_t)__float_as_int(t0) << (8 * p);
+        word += (uint32_t)__float_as_int(t1) << (8 * p + 4);
+        if (SNR) {
+            const wq::f2_t xo = wq::bf2_to_f2(u[p]);
+            const wq::f2_t e = wq::fma2(wq::add2(tq, NM2), NS2, xo);       // w - (code - zp) * s
+            se2 = wq::fma2(e, e, se2);
+            sw2 = wq::fma2(xo, xo, sw2);
+        }
+    }
+    return word;
+}
+
+// Shared-memory position of 16-byte chunk `ch` of tile row `r`: rows stay
+// 256-byte aligned (cp.async destinations line up with the global lines) and
+// the chunks of each half-row are XOR-swizzled by (2*(r%4) + half), so that the
+// eight lanes of a quarter-warp (rows r..r+3, both halves) reading the same
+// logical chunk hit eight different bank groups.
+template <int CH>
+__device__ __forceinline__ int swz(int r, int ch) {
+    const int h = ch / (CH / 2), c = ch % (CH / 2);
+    return h * (CH / 2) + (c ^ ((2 * (r & 3) + h) & 7));
+}
+
+// Warp tile: 16 output channels (rows of w) x KT input channels; lanes 2r and
+// 2r+1 own row n0 + r, each half of the tile's K range (64 values, or 128 for
+// group 256).  Tiles are numbered K-fastest.
 template <bool SYM, int G, bool SNR>
-__global__ void __launch_bounds__(QTile<G>::THREADS, 3) gptq_quant_kernel(
+__global__ void __launch_bounds__(QTile<G>::THREADS, 6) gptq_quant_kernel(
     const uint16_t* __restrict__ w, int64_t n, int64_t k, int32_t* __restrict__ qweight,
     int32_t* __restrict__ qzeros, uint16_t* __restrict__ scales, int32_t* __restrict__ g_idx,
     double* __restrict__ slots, unsigned* __restrict__ counter, double* __restrict__ snr_db) {
     using T = QTile<G>;
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    // static shared memory (the SNR reduction) may precede the dynamic buffer:
+    // re-align so that every staged row starts on a 256-byte boundary
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int row = lane >> 1, half = lane & 1;
     unsigned char* wsm = smem + warp * (T::NS * T::STAGE);
-    const int64_t tn = (n + 31) / 32, tk = (k + T::KT - 1) / T::KT, ntiles = tn * tk;
+    const int64_t tn = (n + T::R - 1) / T::R, tk = (k + T::KT - 1) / T::KT, ntiles = tn * tk;
     const int64_t gwarp = (int64_t)blockIdx.x * T::WARPS + warp;
     const int64_t nwarps = (int64_t)gridDim.x * T::WARPS;
 
     auto issue = [&](int64_t t, int stage) {
         if (t < ntiles) {
-            const int64_t n0 = (t % tn) * 32, k0 = (t / tn) * T::KT;
+            const int64_t n0 = (t / tk) * T::R, k0 = (t % tk) * T::KT;
             unsigned char* dst = wsm + stage * T::STAGE;
 #pragma unroll
-            for (int i = 0; i < T::CH; ++i) {
-                const int idx = i * 32 + lane, row = idx / T::CH, ch = idx % T::CH;
-                const int64_t gr = n0 + row, gk = k0 + 8 * ch;
-                if (gr < n && gk < k) wq::cp_async16(dst + row * T::ROWB + 16 * ch, w + gr * k + gk);
+            for (int i = 0; i < T::R * T::CH / 32; ++i) {
+                const int idx = i * 32 + lane, r = idx / T::CH, ch = idx % T::CH;
+                const int64_t gr = n0 + r, gk = k0 + 8 * ch;
+                if (gr < n && gk < k)
+                    wq::cp_async16(dst + r * T::ROWB + 16 * swz<T::CH>(r, ch), w + gr * k + gk);
             }
         }
         wq::cp_async_commit();
     };
 
-    double dw = 0.0, de = 0.0;
+    wq::KSum ksw, kse;
     int64_t t = gwarp;
     issue(t, 0);
     for (int j = 0; t < ntiles; ++j, t += nwarps) {
         issue(t + nwarps, (j + 1) & 1);
         wq::cp_async_wait<1>();
         __syncwarp();
-        const int64_t n0 = (t % tn) * 32, k0 = (t / tn) * T::KT;
-        const int64_t col = n0 + lane;
+        const int64_t n0 = (t / tk) * T::R, k0 = (t % tk) * T::KT;
+        const int64_t col = n0 + row;
         const bool rowv = col < n;
-        const unsigned char* rsm = wsm + (j & 1) * T::STAGE + lane * T::ROWB;
-#pragma unroll
-        for (int g = 0; g < T::KT / G; ++g) {
-            if (k0 + g * G >= k) break;  // k % G == 0: warp-uniform
-            uint4 v[G / 8];
-#pragma unroll
-            for (int c = 0; c < G / 8; ++c) v[c] = *reinterpret_cast<const uint4*>(rsm + 16 * (g * (G / 8) + c));
+        const int64_t kl = k0 + half * T::HALF;  // first input channel of this lane
+        const uint4* rp = reinterpret_cast<const uint4*>(wsm + (j & 1) * T::STAGE + row * T::ROWB);
+        const int sw_ = (2 * (row & 3) + half) & 7;  // swizzle of this lane's half-row
+        const uint4* lp = rp + half * (T::HALF / 8);
+#pragma unroll 1
+        for (int g = 0; g < T::HALF / T::GL; ++g) {
+            const int64_t kg = kl + g * T::GL;
+            // group validity is uniform over the lanes sharing a group (k % G == 0) but
+            // may differ between the two halves: shuffles below run on every lane
+            const bool gval = kg < k;
+            const int gofs = g * (T::GL / 8);  // first logical chunk of the group in this half
             float s, zp;
             if (SYM) {
-                const uint32_t M = 0x7fff7fffu;
-                uint32_t m = __vmaxu2(v[0].x & M, v[0].y & M);
-#pragma unroll
-                for (int c = 0; c < G / 8; ++c)
-                    m = __vmaxu2(m, __vmaxu2(__vmaxu2(v[c].x & M, v[c].y & M), __vmaxu2(v[c].z & M, v[c].w & M)));
+                uint32_t m = 0;
+#pragma unroll 4
+                for (int c = 0; c < T::GL / 8; ++c) {
+                    const uint4 v = lp[(gofs + c) ^ sw_];
+                    m = babsmax2(m, babsmax2(babsmax2(v.x, v.y), babsmax2(v.z, v.w)));
+                }
+                if (T::LPG == 2) m = babsmax2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                m &= 0x7fff7fffu;
                 const float amax = wq::bf_to_f(max(m & 0xffffu, m >> 16));
-                s = fmaxf(__fdiv_rn(amax, 8.0f), 1e-9f);
+                s = fmaxf(__fmul_rn(amax, 0.125f), 1e-9f);  // amax / 8: exact for any bf16 amax
                 zp = 8.0f;
             } else {
-                uint32_t mx = v[0].x, mn = v[0].x;
-#pragma unroll
-                for (int c = 0; c < G / 8; ++c) {
-                    mx = bmax2(mx, bmax2(bmax2(v[c].x, v[c].y), bmax2(v[c].z, v[c].w)));
-                    mn = bmin2(mn, bmin2(bmin2(v[c].x, v[c].y), bmin2(v[c].z, v[c].w)));
+                uint32_t mx = lp[gofs ^ sw_].x, mn = mx;
+#pragma unroll 4
+                for (int c = 0; c < T::GL / 8; ++c) {
+                    const uint4 v = lp[(gofs + c) ^ sw_];
+                    mx = bmax2(mx, bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w)));
+                    mn = bmin2(mn, bmin2(bmin2(v.x, v.y), bmin2(v.z, v.w)));
+                }
+                if (T::LPG == 2) {
+                    mx = bmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mn = bmin2(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
                 }
                 const float wmax = fmaxf(wq::bf_lo(mx), wq::bf_hi(mx));
                 const float wmin = fminf(wq::bf_lo(mn), wq::bf_hi(mn));
-                s = __fdiv_rn(fmaxf(__fsub_rn(wmax, wmin), 1e-9f), 15.0f);
-                zp = fminf(fmaxf(rintf(__fdiv_rn(-wmin, s)), 0.0f), 15.0f);
+                const float range = fmaxf(__fsub_rn(wmax, wmin), 1e-9f);
+                // range / 15 and -wmin / s as IEEE quotients: reciprocal + one FMA
+                // correction (exact while the operands stay in the normal range)
+                s = range <= 0x1p120f ? wq::div_by_recip(range, 15.0f, kRcp15) : __fdiv_rn(range, 15.0f);
+                const float q = s <= 0x1p100f ? wq::div_by_recip(-wmin, s, __frcp_rn(s)) : __fdiv_rn(-wmin, s);
+                zp = fminf(fmaxf(rintf(q), 0.0f), 15.0f);
             }
-            const float r = __frcp_rn(s);
-            const float lo = -zp, hi = 15.0f - zp;
-            const uint32_t cg = (uint32_t)((int)zp - 0x4B400000) * 0x11111111u;
-            const wq::f2_t R2 = wq::f2(r, r), NS2 = wq::f2(-s, -s), M2 = wq::f2(kMagic, kMagic);
-            const wq::f2_t NM2 = wq::f2(-kMagic, -kMagic);
-            const bool exact = s <= 0x1p100f;  // r stays normal: the correction step is exact
-            wq::f2_t sw2 = wq::f2(0.0f, 0.0f), se2 = sw2;
-            const int64_t r0 = (k0 + g * G) / 8;
-#pragma unroll
-            for (int c = 0; c < G / 8; ++c) {
-                const uint32_t u[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-                uint32_t word = cg;
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    const wq::f2_t x = wq::bf2_to_f2(u[p]);
-                    float q0, q1;
-                    if (exact) {
-                        const wq::f2_t qa = wq::mul2(x, R2);
-                        const wq::f2_t rem = wq::fma2(qa, NS2, x);
-                        wq::f2u(wq::fma2(rem, R2, qa), q0, q1);
-                    } else {
-                        float x0, x1;
-                        wq::f2u(x, x0, x1);
-                        q0 = __fdiv_rn(x0, s);
-                        q1 = __fdiv_rn(x1, s);
+            if (gval) {
+                GroupConst gc;
+                gc.s = s;
+                gc.zp = zp;
+                gc.lo2 = bound2(__fmul_rn(-zp, s));
+                gc.hi2 = bound2(__fmul_rn(15.0f - zp, s));
+                const int64_t r0 = kg / 8;
+                wq::f2_t sw2 = wq::f2(0.0f, 0.0f), se2 = sw2;
+                if (s <= 0x1p100f) {  // 1/s normal: the reciprocal + correction step is exact
+                    const float r = __frcp_rn(s);
+                    const wq::f2_t R2 = wq::f2(r, r), NS2 = wq::f2(-s, -s);
+                    const uint32_t cg = (uint32_t)((int)zp - 0x4B400000) * 0x11111111u;
+#pragma unroll 2
+                    for (int c = 0; c < T::GL / 8; ++c) {
+                        const uint32_t word = quant_chunk<SYM, SNR>(lp[(gofs + c) ^ sw_], gc, R2, NS2, cg, sw2, se2);
+                        if (rowv) qweight[(r0 + c) * n + col] = (int32_t)word;
                     }
-                    q0 = fminf(fmaxf(q0, lo), hi);
-                    q1 = fminf(fmaxf(q1, lo), hi);
-                    const wq::f2_t tq = wq::add2(wq::f2(q0, q1), M2);  // rint(q) + 1.5*2^23
-                    float t0, t1;
-                    wq::f2u(tq, t0, t1);
-                    word += (uint32_t)__float_as_int(t0) << (8 * p);
-                    word += (uint32_t)__float_as_int(t1) << (8 * p + 4);
-                    if (SNR) {
-                        const wq::f2_t e = wq::fma2(wq::add2(tq, NM2), NS2, x);  // x - (code-zp)*s
-                        se2 = wq::fma2(e, e, se2);
-                        sw2 = wq::fma2(x, x, sw2);
+                } else {  // astronomically large scales: plain IEEE division
+                    const float lo = -zp, hi = 15.0f - zp;
+                    float sw = 0.f, se = 0.f;
+#pragma unroll 1
+                    for (int c = 0; c < T::GL / 8; ++c) {
+                        const uint4 v = lp[(gofs + c) ^ sw_];
+                        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+                        uint32_t word = 0;
+                        for (int e = 0; e < 8; ++e) {
+                            const float x = (e & 1) ? wq::bf_hi(u[e >> 1]) : wq::bf_lo(u[e >> 1]);
+                            const float rq = rintf(fminf(fmaxf(__fdiv_rn(x, s), lo), hi));
+                            word |= (uint32_t)((int)rq + (int)zp) << (4 * e);
+                            const float dd = __fsub_rn(x, __fmul_rn(rq, s));
+                            sw = __fmaf_rn(x, x, sw);
+                            se = __fmaf_rn(dd, dd, se);
+                        }
+                        if (rowv) qweight[(r0 + c) * n + col] = (int32_t)word;
                     }
+                    sw2 = wq::f2(sw, 0.f);
+                    se2 = wq::f2(se, 0.f);
                 }
-                if (rowv) qweight[(r0 + c) * n + col] = (int32_t)word;
-            }
-            if (SNR) {
-                float a0, a1, b0, b1;
-                wq::f2u(sw2, a0, a1);
-                wq::f2u(se2, b0, b1);
-                if (rowv) {
-                    dw += (double)a0 + (double)a1;
-                    de += (double)b0 + (double)b1;
+                if (SNR && rowv) {
+                    float a0, a1, b0, b1;
+                    wq::f2u(sw2, a0, a1);
+                    wq::f2u(se2, b0, b1);
+                    ksw.add(__fadd_rn(a0, a1));
+                    kse.add(__fadd_rn(b0, b1));
                 }
             }
-            const int64_t gi = (k0 + g * G) / G;
-            if (rowv) scales[gi * n + col] = __half_as_ushort(__float2half_rn(s));
+            const int64_t gi = kg / G;
+            const bool owner = T::LPG == 1 || half == 0;  // one lane writes per group
+            if (gval && rowv && owner) scales[gi * n + col] = __half_as_ushort(__float2half_rn(s));
             if (qzeros) {
-                uint32_t zw = SYM ? 0x77777777u : ((uint32_t)zp << (4 * (lane & 7)));
+                // zero points of 8 consecutive rows (lanes 2r, r = 0..7 or 8..15)
+                uint32_t zw = SYM ? 0x77777777u : ((uint32_t)zp << (4 * (row & 7)));
                 if (!SYM) {
-                    zw |= __shfl_xor_sync(0xffffffffu, zw, 1);
                     zw |= __shfl_xor_sync(0xffffffffu, zw, 2);
                     zw |= __shfl_xor_sync(0xffffffffu, zw, 4);
+                    zw |= __shfl_xor_sync(0xffffffffu, zw, 8);
                 }
-                if (rowv && (lane & 7) == 0) qzeros[gi * (n / 8) + col / 8] = (int32_t)zw;
+                if (gval && rowv && owner && (row & 7) == 0) qzeros[gi * (n / 8) + col / 8] = (int32_t)zw;
             }
         }
         if (g_idx && n0 == 0) {
-#pragma unroll
             for (int i = lane; i < T::KT; i += 32)
                 if (k0 + i < k) g_idx[k0 + i] = (int32_t)((k0 + i) / G);
         }
         __syncwarp();
     }
     wq::cp_async_wait<0>();
-    if (SNR) wq::finish_snr(dw, de, slots, counter, snr_db, nullptr);
+    if (SNR) wq::finish_snr(ksw.value(), kse.value(), slots, counter, snr_db, nullptr);
 }
 
 template <bool SYM, int G, bool SNR>
@@ -201,7 +297,7 @@ wq_status launch_quant(const uint16_t* w, int64_t n, int64_t k, int32_t* qweight
         if (s != WQ_OK) return s;
         attr_set = true;
     }
-    const int64_t warp_tiles = ((n + 31) / 32) * ((k + T::KT - 1) / T::KT);
+    const int64_t warp_tiles = ((n + T::R - 1) / T::R) * ((k + T::KT - 1) / T::KT);
     const int grid = wqh::grid_for(fn, T::THREADS, T::SMEM, (warp_tiles + T::WARPS - 1) / T::WARPS,
                                    wqh::kMaxPartials);
     gptq_quant_kernel<SYM, G, SNR><<<grid, T::THREADS, T::SMEM, st>>>(
@@ -265,14 +361,14 @@ template <bool SYM, bool BF16>
 __global__ void __launch_bounds__(kThreads) gptq_dequant_kn(const int32_t* __restrict__ qweight,
                                                             const int32_t* __restrict__ qzeros,
                                                             const uint16_t* __restrict__ scales,
-                                                            int64_t n, int64_t k, int group,
+                                                            int64_t n, int64_t k, int lg_group,
                                                             void* __restrict__ out) {
     const int64_t pairs = n / 2, items = (k / 8) * pairs;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t it = (int64_t)blockIdx.x * kThreads + threadIdx.x; it < items; it += stride) {
         const int64_t r = it / pairs, c = (it % pairs) * 2;
         const uint2 wd = wq::ld_stream2(qweight + r * n + c);
-        const int64_t g = (8 * r) / group;
+        const int64_t g = (8 * r) >> lg_group;
         const uint32_t sc2 = __ldg(reinterpret_cast<const uint32_t*>(scales + g * n + c));
         const float s0 = __half2float(__ushort_as_half((unsigned short)(sc2 & 0xffffu)));
         const float s1 = __half2float(__ushort_as_half((unsigned short)(sc2 >> 16)));
@@ -290,49 +386,76 @@ __global__ void __launch_bounds__(kThreads) gptq_dequant_kn(const int32_t* __res
     }
 }
 
-// [n, k] output: 32 qweight rows x 64 columns per tile, transposed through
-// shared memory; thread = (column, qweight row) writes 8 consecutive k values.
+// [n, k] output: a warp owns 32 output rows (qweight columns n0 .. n0+31) x 128
+// input channels (16 qweight rows); lane l owns output row n0 + l.  Its 16
+// qweight words are 16 coalesced 128-byte warp loads; the 128 outputs go through
+// a padded per-warp shared tile so that the warp writes whole 256-byte (bf16) or
+// 512-byte (fp32) row segments.  Value = (code - zp) * fp16 scale, exact in
+// binary32: (code | 1.5*2^23 bits) - (1.5*2^23 + zp) is the exact small integer.
 template <bool SYM, bool BF16>
-__global__ void __launch_bounds__(kThreads) gptq_dequant_nk(const int32_t* __restrict__ qweight,
-                                                            const int32_t* __restrict__ qzeros,
-                                                            const uint16_t* __restrict__ scales,
-                                                            int64_t n, int64_t k, int group,
-                                                            void* __restrict__ out) {
-    constexpr int RT = 32, CT = 64;
-    __shared__ uint32_t s_w[RT][CT + 1];
-    const int64_t rows_q = k / 8;
-    const int64_t tiles_c = (n + CT - 1) / CT, tiles_r = (rows_q + RT - 1) / RT;
-    for (int64_t t = blockIdx.x; t < tiles_c * tiles_r; t += gridDim.x) {
-        const int64_t c0 = (t % tiles_c) * CT, r0 = (t / tiles_c) * RT;
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < RT * CT; idx += kThreads) {
-            const int rl = idx / CT, cl = idx % CT;
-            const int64_t r = r0 + rl, c = c0 + cl;
-            s_w[rl][cl] = (r < rows_q && c < n) ? (uint32_t)__ldg(qweight + r * n + c) : 0u;
-        }
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < RT * CT; idx += kThreads) {
-            const int cl = idx / RT, rl = idx % RT;
-            const int64_t r = r0 + rl, c = c0 + cl;
-            if (r >= rows_q || c >= n) continue;
-            const int64_t g = (8 * r) / group;
-            const float s = __half2float(__ushort_as_half(__ldg(scales + g * n + c)));
-            const int z = zp_of(qzeros, g, n, c, SYM);
-            const uint32_t wd = s_w[rl][cl];
+__global__ void __launch_bounds__(128) gptq_dequant_nk(const int32_t* __restrict__ qweight,
+                                                       const int32_t* __restrict__ qzeros,
+                                                       const uint16_t* __restrict__ scales,
+                                                       int64_t n, int64_t k, int lg_group,
+                                                       void* __restrict__ out) {
+    constexpr int KT = 128, OB = BF16 ? 2 : 4;
+    constexpr int ROWB = KT * OB + 16;   // padded row of the output tile
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned char* tile = smem + warp * 32 * ROWB;
+    const int64_t tn = (n + 31) / 32, tk = (k + KT - 1) / KT;
+    const int64_t gwarp = (int64_t)blockIdx.x * 4 + warp, nwarps = (int64_t)gridDim.x * 4;
+    for (int64_t t = gwarp; t < tn * tk; t += nwarps) {
+        const int64_t n0 = (t / tk) * 32, k0 = (t % tk) * KT;
+        const int64_t col = n0 + lane;
+        const bool rowv = col < n;
+        const int nw = (int)min((int64_t)KT, k - k0) / 8;  // qweight rows in this tile
+        uint32_t wd[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+            wd[c] = (rowv && c < nw) ? wq::ld_stream1(qweight + (k0 / 8 + c) * n + col) : 0u;
+        unsigned char* mine = tile + lane * ROWB;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const int64_t kk = k0 + 8 * c;
+            const int64_t g = kk >> lg_group;
+            float s = 0.f;
+            int z = 8;
+            if (rowv && c < nw) {
+                s = __half2float(__ushort_as_half(__ldg(scales + g * n + col)));
+                if (!SYM) z = (int)((__ldg(qzeros + g * (n / 8) + col / 8) >> (4 * (col % 8))) & 15);
+            }
+            const wq::f2_t S2 = wq::f2(s, s);
+            const wq::f2_t Z2 = wq::f2(-(kMagic + (float)z), -(kMagic + (float)z));
             float v[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __fmul_rn((float)((int)((wd >> (4 * i)) & 15u) - z), s);
-            const int64_t o = c * k + 8 * r;
+            for (int p = 0; p < 4; ++p) {
+                const uint32_t c0 = (wd[c] >> (8 * p)) & 15u, c1 = (wd[c] >> (8 * p + 4)) & 15u;
+                const wq::f2_t q = wq::f2(__uint_as_float(0x4B400000u | c0), __uint_as_float(0x4B400000u | c1));
+                wq::f2u(wq::mul2(wq::add2(q, Z2), S2), v[2 * p], v[2 * p + 1]);  // (code - zp) * s
+            }
             if (BF16) {
-                uint4 q = make_uint4(wq::f2_to_bf2(v[0], v[1]), wq::f2_to_bf2(v[2], v[3]),
-                                     wq::f2_to_bf2(v[4], v[5]), wq::f2_to_bf2(v[6], v[7]));
-                *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + o) = q;
+                *reinterpret_cast<uint4*>(mine + 16 * c) =
+                    make_uint4(wq::f2_to_bf2(v[0], v[1]), wq::f2_to_bf2(v[2], v[3]),
+                               wq::f2_to_bf2(v[4], v[5]), wq::f2_to_bf2(v[6], v[7]));
             } else {
-                float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + o);
-                p[0] = make_float4(v[0], v[1], v[2], v[3]);
-                p[1] = make_float4(v[4], v[5], v[6], v[7]);
+                *reinterpret_cast<float4*>(mine + 32 * c) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4*>(mine + 32 * c + 16) = make_float4(v[4], v[5], v[6], v[7]);
             }
         }
+        __syncwarp();
+        // copy out: row segments of KT*OB bytes, 16 bytes per lane per instruction
+        constexpr int CPR = KT * OB / 16;  // 16-byte chunks per row (16 or 32)
+        const int valid_chunks = nw * 8 * OB / 16;
+#pragma unroll 4
+        for (int i = 0; i < 32 * CPR / 32; ++i) {
+            const int idx = i * 32 + lane, row = idx / CPR, ch = idx % CPR;
+            const int64_t gr = n0 + row;
+            if (gr < n && ch < valid_chunks)
+                *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(out) + (gr * k + k0) * OB + 16 * ch) =
+                    *reinterpret_cast<const uint4*>(tile + row * ROWB + 16 * ch);
+        }
+        __syncwarp();
     }
 }
 
@@ -343,12 +466,20 @@ wq_status launch_dequant(const int32_t* qweight, const int32_t* qzeros, const ui
         const void* fn = (const void*)gptq_dequant_kn<SYM, BF16>;
         const int64_t items = (k / 8) * (n / 2);
         const int grid = wqh::grid_for(fn, kThreads, 0, (items + kThreads - 1) / kThreads, 1 << 30);
-        gptq_dequant_kn<SYM, BF16><<<grid, kThreads, 0, st>>>(qweight, qzeros, scales, n, k, group, out);
+        gptq_dequant_kn<SYM, BF16><<<grid, kThreads, 0, st>>>(qweight, qzeros, scales, n, k, __builtin_ctz(group), out);
     } else {
         const void* fn = (const void*)gptq_dequant_nk<SYM, BF16>;
-        const int64_t tiles = ((n + 63) / 64) * ((k / 8 + 31) / 32);
-        const int grid = wqh::grid_for(fn, kThreads, 0, tiles, 1 << 30);
-        gptq_dequant_nk<SYM, BF16><<<grid, kThreads, 0, st>>>(qweight, qzeros, scales, n, k, group, out);
+        constexpr int smem = 4 * 32 * (128 * (BF16 ? 2 : 4) + 16);
+        static bool attr_set = false;
+        if (!attr_set) {
+            wq_status s = wqh::cuda_status(
+                cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+            if (s != WQ_OK) return s;
+            attr_set = true;
+        }
+        const int64_t warp_tiles = ((n + 31) / 32) * ((k + 127) / 128);
+        const int grid = wqh::grid_for(fn, 128, smem, (warp_tiles + 3) / 4, 1 << 30);
+        gptq_dequant_nk<SYM, BF16><<<grid, 128, smem, st>>>(qweight, qzeros, scales, n, k, __builtin_ctz(group), out);
     }
     return wqh::check_launch();
 }
@@ -376,7 +507,7 @@ extern "C" wq_status gptq_dequantize(const int32_t* qweight, const int32_t* qzer
                                      int sym, int out_dtype, int out_layout, void* out,
                                      void* stream) {
     if (n < 0 || k < 0) return WQ_ERR_BAD_SHAPE;
-    if (group <= 0 || group % 8 != 0) return WQ_ERR_UNSUPPORTED;
+    if (group < 8 || (group & (group - 1)) != 0) return WQ_ERR_UNSUPPORTED;  // power of two
     if (k % group != 0 || n % 8 != 0) return WQ_ERR_BAD_SHAPE;
     if (out_dtype != WQ_DTYPE_F32 && out_dtype != WQ_DTYPE_BF16) return WQ_ERR_BAD_DTYPE;
     if (out_layout != WQ_LAYOUT_NK && out_layout != WQ_LAYOUT_KN) return WQ_ERR_UNSUPPORTED;

@@ -133,29 +133,43 @@ template <int OUT_BF16>
 __global__ void __launch_bounds__(kThreads) mxfp4_dequant_kernel(const uint32_t* __restrict__ packed,
                                                                  const uint8_t* __restrict__ e8m0,
                                                                  int64_t nchunks, void* __restrict__ out) {
+    // kUnroll independent 8-value chunks per thread: their loads are all in
+    // flight before the first is decoded
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t c = (int64_t)blockIdx.x * kThreads + threadIdx.x; c < nchunks; c += stride) {
-        const uint32_t word = __ldg(packed + c);
-        const float s = e8m0_scale(__ldg(e8m0 + (c >> 2)));
-        float f[8];
+    for (int64_t base = (int64_t)blockIdx.x * kThreads + threadIdx.x; base < nchunks;
+         base += stride * kUnroll) {
+        uint32_t word[kUnroll], ex[kUnroll];
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            float lo, hi;
-            e2m1x2_to_f((word >> (8 * p)) & 0xffu, lo, hi);
-            f[2 * p] = __fmul_rn(lo, s);
-            f[2 * p + 1] = __fmul_rn(hi, s);
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t c = base + u * stride;
+            word[u] = c < nchunks ? wq::ld_stream1(packed + c) : 0u;
+            ex[u] = c < nchunks ? (uint32_t)__ldg(e8m0 + (c >> 2)) : 0u;
         }
-        if (OUT_BF16) {
-            uint4 o;
-            o.x = wq::f2_to_bf2(f[0], f[1]);
-            o.y = wq::f2_to_bf2(f[2], f[3]);
-            o.z = wq::f2_to_bf2(f[4], f[5]);
-            o.w = wq::f2_to_bf2(f[6], f[7]);
-            reinterpret_cast<uint4*>(out)[c] = o;
-        } else {
-            float4* o = reinterpret_cast<float4*>(out) + 2 * c;
-            o[0] = make_float4(f[0], f[1], f[2], f[3]);
-            o[1] = make_float4(f[4], f[5], f[6], f[7]);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t c = base + u * stride;
+            if (c >= nchunks) break;
+            const float s = e8m0_scale(ex[u]);
+            float f[8];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                float lo, hi;
+                e2m1x2_to_f((word[u] >> (8 * p)) & 0xffu, lo, hi);
+                f[2 * p] = __fmul_rn(lo, s);
+                f[2 * p + 1] = __fmul_rn(hi, s);
+            }
+            if (OUT_BF16) {
+                uint4 o;
+                o.x = wq::f2_to_bf2(f[0], f[1]);
+                o.y = wq::f2_to_bf2(f[2], f[3]);
+                o.z = wq::f2_to_bf2(f[4], f[5]);
+                o.w = wq::f2_to_bf2(f[6], f[7]);
+                reinterpret_cast<uint4*>(out)[c] = o;
+            } else {
+                float4* o = reinterpret_cast<float4*>(out) + 2 * c;
+                o[0] = make_float4(f[0], f[1], f[2], f[3]);
+                o[1] = make_float4(f[4], f[5], f[6], f[7]);
+            }
         }
     }
 }
@@ -196,11 +210,11 @@ extern "C" wq_status mxfp4_dequantize(const uint8_t* packed, const uint8_t* e8m0
     cudaStream_t st = (cudaStream_t)stream;
     if (out_dtype == WQ_DTYPE_BF16) {
         int grid = wqh::grid_for((const void*)mxfp4_dequant_kernel<1>, kThreads, 0,
-                                 (nchunks + kThreads - 1) / kThreads, 1 << 30);
+                                 (nchunks + kThreads * kUnroll - 1) / (kThreads * kUnroll), 1 << 30);
         mxfp4_dequant_kernel<1><<<grid, kThreads, 0, st>>>((const uint32_t*)packed, e8m0, nchunks, out);
     } else {
         int grid = wqh::grid_for((const void*)mxfp4_dequant_kernel<0>, kThreads, 0,
-                                 (nchunks + kThreads - 1) / kThreads, 1 << 30);
+                                 (nchunks + kThreads * kUnroll - 1) / (kThreads * kUnroll), 1 << 30);
         mxfp4_dequant_kernel<0><<<grid, kThreads, 0, st>>>((const uint32_t*)packed, e8m0, nchunks, out);
     }
     return wqh::check_launch();

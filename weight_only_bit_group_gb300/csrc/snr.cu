@@ -4,8 +4,10 @@
 //
 // One pass, deterministic for a given grid: every CTA writes its (sum w^2,
 // sum e^2) to its own workspace slot; the last CTA to finish adds the slots in
-// index order and evaluates the formulas (nothing waits).  Terms are binary32 (as the page computes
-// them); sums are binary32 over at most 32 terms per thread and binary64 above.
+// index order and evaluates the formulas (nothing waits).  Terms are binary32
+// (as the page computes them); each thread sums at most 32 terms in binary32,
+// adds those partials into a compensated binary32 running sum (the binary64
+// pipe is narrow on this GPU), and the CTA and final sums are binary64.
 #include "wq_common.cuh"
 
 namespace {
@@ -38,7 +40,7 @@ __global__ void __launch_bounds__(kThreads) snr_partial_nk(const uint4* __restri
                                                            double* __restrict__ snr_db,
                                                            double* __restrict__ rel_err) {
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    double dw = 0.0, de = 0.0;
+    wq::KSum dw, de;
     for (int64_t base = (int64_t)blockIdx.x * kThreads + threadIdx.x; base < nchunks;
          base += stride * kUnroll) {
         float sw = 0.0f, se = 0.0f;
@@ -54,15 +56,15 @@ __global__ void __launch_bounds__(kThreads) snr_partial_nk(const uint4* __restri
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     float e = __fsub_rn(x[i], d[i]);
-                    sw = __fadd_rn(sw, __fmul_rn(x[i], x[i]));
-                    se = __fadd_rn(se, __fmul_rn(e, e));
+                    sw = __fmaf_rn(x[i], x[i], sw);
+                    se = __fmaf_rn(e, e, se);
                 }
             }
         }
-        dw += (double)sw;
-        de += (double)se;
+        dw.add(sw);
+        de.add(se);
     }
-    wq::finish_snr(dw, de, slots, counter, snr_db, rel_err);
+    wq::finish_snr(dw.value(), de.value(), slots, counter, snr_db, rel_err);
 }
 
 // deq laid out [k, n] (the GPTQ page's layout): 64 x 64 tiles, the deq tile is
@@ -78,7 +80,7 @@ __global__ void __launch_bounds__(kThreads) snr_partial_kn(const uint16_t* __res
                                                            double* __restrict__ rel_err) {
     __shared__ float sd[kT][kT + 1];  // [k][n]
     const int64_t tiles_n = (n + kT - 1) / kT, tiles_k = (k + kT - 1) / kT;
-    double dw = 0.0, de = 0.0;
+    wq::KSum dw, de;
     for (int64_t t = blockIdx.x; t < tiles_n * tiles_k; t += gridDim.x) {
         const int64_t n0 = (t % tiles_n) * kT, k0 = (t / tiles_n) * kT;
         __syncthreads();
@@ -113,16 +115,16 @@ __global__ void __launch_bounds__(kThreads) snr_partial_kn(const uint16_t* __res
                     if (kk < k) {
                         float x = wq::bf_to_f(w[nn * k + kk]);
                         float e = __fsub_rn(x, sd[kc + q][nr]);
-                        sw = __fadd_rn(sw, __fmul_rn(x, x));
-                        se = __fadd_rn(se, __fmul_rn(e, e));
+                        sw = __fmaf_rn(x, x, sw);
+                        se = __fmaf_rn(e, e, se);
                     }
                 }
             }
         }
-        dw += (double)sw;
-        de += (double)se;
+        dw.add(sw);
+        de.add(se);
     }
-    wq::finish_snr(dw, de, slots, counter, snr_db, rel_err);
+    wq::finish_snr(dw.value(), de.value(), slots, counter, snr_db, rel_err);
 }
 
 }  // namespace

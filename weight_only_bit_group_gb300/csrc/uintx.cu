@@ -342,12 +342,13 @@ __device__ __forceinline__ float deq1(uint32_t q, float zf, float sc) {
     return __fmul_rn(__fsub_rn((float)q, zf), sc);
 }
 
-// numel % 64 == 0: 8 positions per thread, 16-byte output stores.
+// numel % 64 == 0 and a power-of-two group: 8 positions per thread, 16-byte
+// output stores.
 template <int NBITS, bool BF16>
 __global__ void __launch_bounds__(kThreads) uintx_dequant_vec(const uint8_t* __restrict__ packed,
                                                               const uint16_t* __restrict__ scale,
                                                               const uint8_t* __restrict__ zp,
-                                                              int64_t numel, int group,
+                                                              int64_t numel, int lg_group,
                                                               void* __restrict__ out) {
     const int64_t L1 = numel / 8, items = L1 / 8;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(kThreads) uintx_dequant_vec(const uint8_t* __r
         load_codes<NBITS>(packed, numel, L1, d, blo, bhi);
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
-            const int64_t e = m * L1 + d, g = e / group;  // 8 | group: one group
+            const int64_t e = m * L1 + d, g = e >> lg_group;  // 8 | group: one group
             const float sc = wq::bf_to_f(__ldg(scale + g));
             const float zf = (float)__ldg(zp + g);
             float f[8];
@@ -460,11 +461,12 @@ wq_status quant_nbits(const uint16_t* w, int64_t numel, int group, uint8_t* pack
 template <int NBITS, bool BF16>
 wq_status dequant_nbits(const uint8_t* packed, const uint16_t* scale, const uint8_t* zp,
                         int64_t numel, int group, void* out, cudaStream_t st) {
-    if (numel % 64 == 0) {
+    if (numel % 64 == 0 && (group & (group - 1)) == 0) {
         const int64_t items = numel / 64;
         const int grid = wqh::grid_for((const void*)uintx_dequant_vec<NBITS, BF16>, kThreads, 0,
                                        (items + kThreads - 1) / kThreads, 1 << 30);
-        uintx_dequant_vec<NBITS, BF16><<<grid, kThreads, 0, st>>>(packed, scale, zp, numel, group, out);
+        uintx_dequant_vec<NBITS, BF16><<<grid, kThreads, 0, st>>>(packed, scale, zp, numel,
+                                                                  __builtin_ctz(group), out);
     } else {
         const int64_t L1 = numel / 8;
         const int grid = wqh::grid_for((const void*)uintx_dequant_general<NBITS, BF16>, kThreads, 0,

@@ -89,36 +89,37 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // ------------------------------------------------------------------ f32x2
-// Packed binary32 pairs (Blackwell FFMA2/FMUL2/FADD2): each lane of the pair is
-// one IEEE binary32 operation, round to nearest even, subnormals kept.
-typedef unsigned long long f2_t;
-__device__ __forceinline__ f2_t f2(float lo, float hi) {
-    f2_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
+// Packed binary32 pairs (Blackwell FFMA2/FMUL2/FADD2 through the float2
+// builtins): each half is one IEEE binary32 operation, round to nearest even,
+// subnormals kept.
+typedef float2 f2_t;
+__device__ __forceinline__ f2_t f2(float lo, float hi) { return make_float2(lo, hi); }
 __device__ __forceinline__ void f2u(f2_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    lo = v.x;
+    hi = v.y;
 }
-__device__ __forceinline__ f2_t mul2(f2_t a, f2_t b) {
-    f2_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ f2_t add2(f2_t a, f2_t b) {
-    f2_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c) {
-    f2_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
+__device__ __forceinline__ f2_t mul2(f2_t a, f2_t b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ f2_t add2(f2_t a, f2_t b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c) { return __ffma2_rn(a, b, c); }
 // The two bf16 of a packed word as a binary32 pair (exact).
 __device__ __forceinline__ f2_t bf2_to_f2(uint32_t u) {
-    return f2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
+
+// ------------------------------------------------------------------ sums
+// Compensated (Neumaier) binary32 running sum.  Partial sums of binary32 terms
+// are added here instead of in binary64, whose pipe is narrow on this GPU; the
+// compensation keeps the running sum accurate to a few binary32 ulps however
+// many partials it absorbs.  value() folds the compensation in binary64.
+struct KSum {
+    float s = 0.0f, c = 0.0f;
+    __device__ __forceinline__ void add(float x) {
+        const float t = __fadd_rn(s, x);
+        c = __fadd_rn(c, fabsf(s) >= fabsf(x) ? __fadd_rn(__fsub_rn(s, t), x) : __fadd_rn(__fsub_rn(x, t), s));
+        s = t;
+    }
+    __device__ __forceinline__ double value() const { return (double)s + (double)c; }
+};
 
 // ------------------------------------------------------------------ warp
 __device__ __forceinline__ float shfl_xor(float v, int m) {
