@@ -297,21 +297,49 @@ def run_ours(args, rank, world, dist):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(record):
-        evs = []
-        for name, fn, *_ in phases:
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            evs.append((name, a, b))
-        return evs
+    def timing_event():
+        # inside a graph capture an event must be recorded as an external event
+        # node to be usable for timing after replay
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:  # older torch: no external event records
+            return torch.cuda.Event(enable_timing=True)
 
+    def step_body(evs):
+        for name, fn, *_ in phases:
+            a = timing_event()
+            b = timing_event()
+            a.record()
+            fn()
+            b.record()
+            evs.append((name, a, b))
+
+    # eager warm-up: builds, caches occupancy queries and kernel attributes
     for _ in range(args.warmup):
         flush.zero_()
-        step(False)
+        step_body([])
     torch.cuda.synchronize(dev)
+
+    graph = None
+    graph_events = []
+    if not args.no_graph:
+        # the whole step (every ABI call of every phase, with per-phase timing
+        # events) is captured once and replayed: no host launch cost per step
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step_body(graph_events)
+        for _ in range(args.warmup):
+            flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize(dev)
+
+    def step(record):
+        if graph is not None:
+            graph.replay()
+            return graph_events
+        evs = []
+        step_body(evs)
+        return evs
 
     per_phase = {name: [] for name, *_ in phases}
     step_ms = []
@@ -320,22 +348,21 @@ def run_ours(args, rank, world, dist):
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index) as clk:
         wall0 = time.perf_counter()
-        recs = []
         for _ in range(args.steps):
             flush.zero_()
             evs = step(True)
-            recs.append(evs)
+            # graph events are re-recorded by every replay: read them per step
+            torch.cuda.current_stream(dev).synchronize()
+            tot = 0.0
+            for name, a, b in evs:
+                t = a.elapsed_time(b)
+                per_phase[name].append(t)
+                tot += t
+            step_ms.append(tot)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - wall0
     if dist is not None:
         dist.barrier()
-    for evs in recs:
-        tot = 0.0
-        for name, a, b in evs:
-            t = a.elapsed_time(b)
-            per_phase[name].append(t)
-            tot += t
-        step_ms.append(tot)
     ms = statistics.mean(step_ms)
     if dist is not None:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
@@ -379,6 +406,7 @@ def run_ours(args, rank, world, dist):
                    "gptq_group": GROUP_GPTQ, "uintx_nbits": NBITS_UINTX, "uintx_group": GROUP_UINTX,
                    "mxfp4_ties": "half_even", "awq": "gate||up [28672,4096] -> 2048 rows, 11 alphas",
                    "l2": "flushed (256 MB write) before every step; inputs 436 MB > L2",
+                   "launch": "eager" if args.no_graph else "one CUDA graph per step (captured ABI calls)",
                    "parallelism": f"replicas x{world} (one layer per GPU, no collective)"},
         "roofline": roofline,
         "kernels": kernels,
@@ -418,6 +446,15 @@ def run_e2e(args, wl, dev, dist, world):
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
+    if not args.no_graph:
+        # the copies and every ABI call of the step, captured once
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        step = g.replay
+        for _ in range(max(1, args.warmup)):
+            step()
+        torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
     a = torch.cuda.Event(enable_timing=True)
@@ -613,6 +650,7 @@ def main():
     ap.add_argument("--shape", default="16384x8192")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="issue every call eagerly instead of a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()

@@ -42,6 +42,7 @@ struct QTile {
     static constexpr int WARPS = 4;                    // warps per CTA
     static constexpr int THREADS = 32 * WARPS;
     static constexpr int SMEM = NS * WARPS * STAGE + 1024;  // + room to align the base to 1 KB
+    static constexpr int MINB = KT > 128 ? 3 : 6;          // CTAs per SM (shared memory bound)
 };
 
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
@@ -125,13 +126,16 @@ __device__ __forceinline__ int swz(int r, int ch) {
 
 // Warp tile: 16 output channels (rows of w) x KT input channels; lanes 2r and
 // 2r+1 own row n0 + r, each half of the tile's K range (64 values, or 128 for
-// group 256).  Tiles are numbered K-fastest.
+// group 256).  Tiles are numbered K-fastest and walked with incremental
+// coordinates; every per-tile and per-chunk address is a precomputed per-lane
+// offset plus a constant.
 template <bool SYM, int G, bool SNR>
-__global__ void __launch_bounds__(QTile<G>::THREADS, 6) gptq_quant_kernel(
+__global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::MINB) gptq_quant_kernel(
     const uint16_t* __restrict__ w, int64_t n, int64_t k, int32_t* __restrict__ qweight,
     int32_t* __restrict__ qzeros, uint16_t* __restrict__ scales, int32_t* __restrict__ g_idx,
     double* __restrict__ slots, unsigned* __restrict__ counter, double* __restrict__ snr_db) {
     using T = QTile<G>;
+    constexpr int CPL = T::HALF / 8;  // 16-byte chunks per lane per tile
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // static shared memory (the SNR reduction) may precede the dynamic buffer:
     // re-align so that every staged row starts on a 256-byte boundary
@@ -139,53 +143,80 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, 6) gptq_quant_kernel(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int row = lane >> 1, half = lane & 1;
-    unsigned char* wsm = smem + warp * (T::NS * T::STAGE);
-    const int64_t tn = (n + T::R - 1) / T::R, tk = (k + T::KT - 1) / T::KT, ntiles = tn * tk;
+    const uint32_t wsm = (uint32_t)__cvta_generic_to_shared(smem + warp * (T::NS * T::STAGE));
+    const int64_t tn = (n + T::R - 1) / T::R, tk = (k + T::KT - 1) / T::KT;
     const int64_t gwarp = (int64_t)blockIdx.x * T::WARPS + warp;
     const int64_t nwarps = (int64_t)gridDim.x * T::WARPS;
+    const int64_t dn = nwarps / tk, dk = nwarps % tk;  // tile step, once
 
-    auto issue = [&](int64_t t, int stage) {
-        if (t < ntiles) {
-            const int64_t n0 = (t / tk) * T::R, k0 = (t % tk) * T::KT;
-            unsigned char* dst = wsm + stage * T::STAGE;
+    // copy plan: instruction i moves chunk (lane % CH) of tile row i*(32/CH) + lane/CH
+    constexpr int RPI = 32 / T::CH;  // rows per copy instruction (2, or 1 for KT = 256)
+    // the swizzle repeats every 4 rows, i.e. every NP instructions
+    constexpr int NP = 4 / RPI;
+    const int cr = lane / T::CH, cch = lane % T::CH;
+    uint32_t cdst[NP];  // destination offset for instruction index i % NP
 #pragma unroll
-            for (int i = 0; i < T::R * T::CH / 32; ++i) {
-                const int idx = i * 32 + lane, r = idx / T::CH, ch = idx % T::CH;
-                const int64_t gr = n0 + r, gk = k0 + 8 * ch;
-                if (gr < n && gk < k)
-                    wq::cp_async16(dst + r * T::ROWB + 16 * swz<T::CH>(r, ch), w + gr * k + gk);
+    for (int pi = 0; pi < NP; ++pi) {
+        const int r = pi * RPI + cr;
+        cdst[pi] = (uint32_t)(r * T::ROWB + 16 * swz<T::CH>(r, cch));
+    }
+    // this lane's reads: chunk c of its half-row sits at roff8[c % 8] + 16 (c - c % 8)
+    // (the swizzle permutes chunks within each aligned group of eight)
+    const int sw_ = (2 * (row & 3) + half) & 7;
+    const uint32_t rbase = (uint32_t)(row * T::ROWB + 16 * half * (T::CH / 2));
+    uint32_t roff8[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) roff8[c] = rbase + 16 * (c ^ sw_);
+#define WQ_CHUNK(c) (*reinterpret_cast<const uint4*>(stage + roff8[(c) & 7] + 16 * ((c) & ~7)))
+
+    auto issue = [&](int64_t nb, int64_t kb, int stage) {
+        if (nb < tn) {
+            const int64_t n0 = nb * T::R, k0 = kb * T::KT;
+            const bool kv = k0 + 8 * cch < k;
+            const uint16_t* src = w + (n0 + cr) * k + k0 + 8 * cch;
+            const int64_t rows_left = n - n0 - cr;  // copy row r exists iff i*RPI < rows_left
+            const uint32_t dst = wsm + stage * T::STAGE;
+#pragma unroll
+            for (int i = 0; i < T::R / RPI; ++i) {
+                if (kv && i * RPI < rows_left) {
+                    const uint32_t d = dst + (uint32_t)((i / NP) * 4 * T::ROWB) + cdst[i % NP];
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d),
+                                 "l"(src + (int64_t)i * RPI * k) : "memory");
+                }
             }
         }
         wq::cp_async_commit();
     };
 
     wq::KSum ksw, kse;
-    int64_t t = gwarp;
-    issue(t, 0);
-    for (int j = 0; t < ntiles; ++j, t += nwarps) {
-        issue(t + nwarps, (j + 1) & 1);
+    int64_t nb = gwarp / tk, kb = gwarp % tk;
+    issue(nb, kb, 0);
+    for (int j = 0; nb < tn; ++j) {
+        int64_t nb2 = nb + dn, kb2 = kb + dk;
+        if (kb2 >= tk) { kb2 -= tk; ++nb2; }
+        issue(nb2, kb2, (j + 1) & 1);
         wq::cp_async_wait<1>();
         __syncwarp();
-        const int64_t n0 = (t / tk) * T::R, k0 = (t % tk) * T::KT;
+        const int64_t n0 = nb * T::R, k0 = kb * T::KT;
         const int64_t col = n0 + row;
         const bool rowv = col < n;
         const int64_t kl = k0 + half * T::HALF;  // first input channel of this lane
-        const uint4* rp = reinterpret_cast<const uint4*>(wsm + (j & 1) * T::STAGE + row * T::ROWB);
-        const int sw_ = (2 * (row & 3) + half) & 7;  // swizzle of this lane's half-row
-        const uint4* lp = rp + half * (T::HALF / 8);
-#pragma unroll 1
+        const unsigned char* stage = smem + (j & 1) * T::STAGE + warp * (T::NS * T::STAGE);
+        int32_t* qp = qweight + (kl / 8) * n + col;  // qweight word of the lane's first chunk
+#pragma unroll
         for (int g = 0; g < T::HALF / T::GL; ++g) {
             const int64_t kg = kl + g * T::GL;
             // group validity is uniform over the lanes sharing a group (k % G == 0) but
             // may differ between the two halves: shuffles below run on every lane
             const bool gval = kg < k;
-            const int gofs = g * (T::GL / 8);  // first logical chunk of the group in this half
+            constexpr int GC = T::GL / 8;  // chunks per group part
+            const int c0 = g * GC;
             float s, zp;
             if (SYM) {
                 uint32_t m = 0;
-#pragma unroll 4
-                for (int c = 0; c < T::GL / 8; ++c) {
-                    const uint4 v = lp[(gofs + c) ^ sw_];
+#pragma unroll
+                for (int c = 0; c < GC; ++c) {
+                    const uint4 v = WQ_CHUNK(c0 + c);
                     m = babsmax2(m, babsmax2(babsmax2(v.x, v.y), babsmax2(v.z, v.w)));
                 }
                 if (T::LPG == 2) m = babsmax2(m, __shfl_xor_sync(0xffffffffu, m, 1));
@@ -194,10 +225,11 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, 6) gptq_quant_kernel(
                 s = fmaxf(__fmul_rn(amax, 0.125f), 1e-9f);  // amax / 8: exact for any bf16 amax
                 zp = 8.0f;
             } else {
-                uint32_t mx = lp[gofs ^ sw_].x, mn = mx;
-#pragma unroll 4
-                for (int c = 0; c < T::GL / 8; ++c) {
-                    const uint4 v = lp[(gofs + c) ^ sw_];
+                const uint4 v0 = WQ_CHUNK(c0);
+                uint32_t mx = v0.x, mn = v0.x;
+#pragma unroll
+                for (int c = 0; c < GC; ++c) {
+                    const uint4 v = WQ_CHUNK(c0 + c);
                     mx = bmax2(mx, bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w)));
                     mn = bmin2(mn, bmin2(bmin2(v.x, v.y), bmin2(v.z, v.w)));
                 }
@@ -220,25 +252,28 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, 6) gptq_quant_kernel(
                 gc.zp = zp;
                 gc.lo2 = bound2(__fmul_rn(-zp, s));
                 gc.hi2 = bound2(__fmul_rn(15.0f - zp, s));
-                const int64_t r0 = kg / 8;
                 wq::f2_t sw2 = wq::f2(0.0f, 0.0f), se2 = sw2;
                 if (s <= 0x1p100f) {  // 1/s normal: the reciprocal + correction step is exact
                     const float r = __frcp_rn(s);
                     const wq::f2_t R2 = wq::f2(r, r), NS2 = wq::f2(-s, -s);
                     const uint32_t cg = (uint32_t)((int)zp - 0x4B400000) * 0x11111111u;
-#pragma unroll 2
-                    for (int c = 0; c < T::GL / 8; ++c) {
-                        const uint32_t word = quant_chunk<SYM, SNR>(lp[(gofs + c) ^ sw_], gc, R2, NS2, cg, sw2, se2);
-                        if (rowv) qweight[(r0 + c) * n + col] = (int32_t)word;
+#pragma unroll
+                    for (int c = 0; c < GC; ++c) {
+                        const uint4 v = WQ_CHUNK(c0 + c);
+                        const uint32_t word = quant_chunk<SYM, SNR>(v, gc, R2, NS2, cg, sw2, se2);
+                        if (rowv) qp[(int64_t)(c0 + c) * n] = (int32_t)word;
                     }
                 } else {  // astronomically large scales: plain IEEE division
                     const float lo = -zp, hi = 15.0f - zp;
                     float sw = 0.f, se = 0.f;
 #pragma unroll 1
-                    for (int c = 0; c < T::GL / 8; ++c) {
-                        const uint4 v = lp[(gofs + c) ^ sw_];
+                    for (int c = 0; c < GC; ++c) {
+                        const int cc = c0 + c;
+                        const uint4 v = *reinterpret_cast<const uint4*>(
+                            stage + rbase + 16 * ((cc & ~7) | ((cc & 7) ^ sw_)));
                         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
                         uint32_t word = 0;
+#pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const float x = (e & 1) ? wq::bf_hi(u[e >> 1]) : wq::bf_lo(u[e >> 1]);
                             const float rq = rintf(fminf(fmaxf(__fdiv_rn(x, s), lo), hi));
@@ -247,7 +282,7 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, 6) gptq_quant_kernel(
                             sw = __fmaf_rn(x, x, sw);
                             se = __fmaf_rn(dd, dd, se);
                         }
-                        if (rowv) qweight[(r0 + c) * n + col] = (int32_t)word;
+                        if (rowv) qp[(int64_t)(c0 + c) * n] = (int32_t)word;
                     }
                     sw2 = wq::f2(sw, 0.f);
                     se2 = wq::f2(se, 0.f);
@@ -279,10 +314,13 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, 6) gptq_quant_kernel(
                 if (k0 + i < k) g_idx[k0 + i] = (int32_t)((k0 + i) / G);
         }
         __syncwarp();
+        nb = nb2;
+        kb = kb2;
     }
     wq::cp_async_wait<0>();
     if (SNR) wq::finish_snr(ksw.value(), kse.value(), slots, counter, snr_db, nullptr);
 }
+#undef WQ_CHUNK
 
 template <bool SYM, int G, bool SNR>
 wq_status launch_quant(const uint16_t* w, int64_t n, int64_t k, int32_t* qweight, int32_t* qzeros,
