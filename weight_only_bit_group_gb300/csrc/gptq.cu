@@ -393,34 +393,72 @@ __device__ __forceinline__ int zp_of(const int32_t* __restrict__ qzeros, int64_t
     return (int)((zw >> (4 * (col % 8))) & 15u);
 }
 
-// [k, n] output: thread = (qweight row r, two adjacent columns); the 8 output
-// rows 8r..8r+7 are written at those two columns (coalesced along n).
+// Codes of one qweight word as binary32 values 1.5*2^23 + code, two at a time:
+// byte j of lo = nibble 2j, byte j of hi = nibble 2j + 1, and one byte permute
+// places a byte under the exponent bits 0x4B40.
+__device__ __forceinline__ uint32_t code_f(uint32_t bytes, int j) {
+    return __byte_perm(bytes, 0x4B400000u, 0x7640u + (unsigned)j);
+}
+
+// [k, n] output.  A CTA tile is one qweight row r (output rows 8r .. 8r+7) x
+// 1024 columns, 4 per thread (one 16-byte load; per output row one 8-byte bf16
+// or 16-byte fp32 store, coalesced along n).  CTA tiles are walked with
+// incremental, block-uniform coordinates.  Value = (code - zp) * fp16 scale,
+// exact in binary32, computed on column pairs with f32x2 arithmetic.
 template <bool SYM, bool BF16>
 __global__ void __launch_bounds__(kThreads) gptq_dequant_kn(const int32_t* __restrict__ qweight,
                                                             const int32_t* __restrict__ qzeros,
                                                             const uint16_t* __restrict__ scales,
                                                             int64_t n, int64_t k, int lg_group,
                                                             void* __restrict__ out) {
-    const int64_t pairs = n / 2, items = (k / 8) * pairs;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t it = (int64_t)blockIdx.x * kThreads + threadIdx.x; it < items; it += stride) {
-        const int64_t r = it / pairs, c = (it % pairs) * 2;
-        const uint2 wd = wq::ld_stream2(qweight + r * n + c);
-        const int64_t g = (8 * r) >> lg_group;
-        const uint32_t sc2 = __ldg(reinterpret_cast<const uint32_t*>(scales + g * n + c));
-        const float s0 = __half2float(__ushort_as_half((unsigned short)(sc2 & 0xffffu)));
-        const float s1 = __half2float(__ushort_as_half((unsigned short)(sc2 >> 16)));
-        const int z0 = zp_of(qzeros, g, n, c, SYM), z1 = zp_of(qzeros, g, n, c + 1, SYM);
+    constexpr int CB = kThreads * 4;  // columns per CTA tile
+    const int64_t rows = k / 8, ncb = (n + CB - 1) / CB;
+    const int64_t dr = gridDim.x / ncb, dcb = gridDim.x % ncb;
+    int64_t r = blockIdx.x / ncb, cb = blockIdx.x % ncb;
+    for (; r < rows;) {
+        const int64_t c = cb * CB + 4 * threadIdx.x;
+        if (c < n) {  // n % 8 == 0: four columns are all valid or all not
+            const uint4 wd = wq::ld_stream(qweight + r * n + c);
+            const int64_t g = (8 * r) >> lg_group;
+            const uint32_t s01 = __ldg(reinterpret_cast<const uint32_t*>(scales + g * n + c));
+            const uint32_t s23 = __ldg(reinterpret_cast<const uint32_t*>(scales + g * n + c + 2));
+            float z[4] = {8.f, 8.f, 8.f, 8.f};
+            if (!SYM) {
+                const uint32_t zw = (uint32_t)__ldg(qzeros + g * (n / 8) + c / 8) >> (4 * (c & 4));
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float v0 = __fmul_rn((float)((int)((wd.x >> (4 * i)) & 15u) - z0), s0);
-            const float v1 = __fmul_rn((float)((int)((wd.y >> (4 * i)) & 15u) - z1), s1);
-            const int64_t o = (8 * r + i) * n + c;
-            if (BF16)
-                *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(out) + o) = wq::f2_to_bf2(v0, v1);
-            else
-                *reinterpret_cast<float2*>(reinterpret_cast<float*>(out) + o) = make_float2(v0, v1);
+                for (int j = 0; j < 4; ++j) z[j] = (float)((zw >> (4 * j)) & 15u);
+            }
+            const wq::f2_t S01 = wq::f2(__half2float(__ushort_as_half((unsigned short)(s01 & 0xffffu))),
+                                        __half2float(__ushort_as_half((unsigned short)(s01 >> 16))));
+            const wq::f2_t S23 = wq::f2(__half2float(__ushort_as_half((unsigned short)(s23 & 0xffffu))),
+                                        __half2float(__ushort_as_half((unsigned short)(s23 >> 16))));
+            const wq::f2_t Z01 = wq::f2(-(kMagic + z[0]), -(kMagic + z[1]));
+            const wq::f2_t Z23 = wq::f2(-(kMagic + z[2]), -(kMagic + z[3]));
+            const uint32_t lo[4] = {wd.x & 0x0F0F0F0Fu, wd.y & 0x0F0F0F0Fu, wd.z & 0x0F0F0F0Fu, wd.w & 0x0F0F0F0Fu};
+            const uint32_t hi[4] = {(wd.x >> 4) & 0x0F0F0F0Fu, (wd.y >> 4) & 0x0F0F0F0Fu,
+                                    (wd.z >> 4) & 0x0F0F0F0Fu, (wd.w >> 4) & 0x0F0F0F0Fu};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t* src = (i & 1) ? hi : lo;
+                const int j = i >> 1;
+                const wq::f2_t q01 = wq::f2(__uint_as_float(code_f(src[0], j)), __uint_as_float(code_f(src[1], j)));
+                const wq::f2_t q23 = wq::f2(__uint_as_float(code_f(src[2], j)), __uint_as_float(code_f(src[3], j)));
+                const wq::f2_t v01 = wq::mul2(wq::add2(q01, Z01), S01);
+                const wq::f2_t v23 = wq::mul2(wq::add2(q23, Z23), S23);
+                float a0, a1, a2, a3;
+                wq::f2u(v01, a0, a1);
+                wq::f2u(v23, a2, a3);
+                const int64_t o = (8 * r + i) * n + c;
+                if (BF16)
+                    *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + o) =
+                        make_uint2(wq::f2_to_bf2(a0, a1), wq::f2_to_bf2(a2, a3));
+                else
+                    *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + o) = make_float4(a0, a1, a2, a3);
+            }
         }
+        r += dr;
+        cb += dcb;
+        if (cb >= ncb) { cb -= ncb; ++r; }
     }
 }
 
@@ -428,8 +466,9 @@ __global__ void __launch_bounds__(kThreads) gptq_dequant_kn(const int32_t* __res
 // input channels (16 qweight rows); lane l owns output row n0 + l.  Its 16
 // qweight words are 16 coalesced 128-byte warp loads; the 128 outputs go through
 // a padded per-warp shared tile so that the warp writes whole 256-byte (bf16) or
-// 512-byte (fp32) row segments.  Value = (code - zp) * fp16 scale, exact in
-// binary32: (code | 1.5*2^23 bits) - (1.5*2^23 + zp) is the exact small integer.
+// 512-byte (fp32) row segments.  Tiles are walked with incremental coordinates.
+// A group spans 2^lg_group / 8 words: with groups of 128 or more every tile is
+// inside one group and needs one scale (and zero point) per lane.
 template <bool SYM, bool BF16>
 __global__ void __launch_bounds__(128) gptq_dequant_nk(const int32_t* __restrict__ qweight,
                                                        const int32_t* __restrict__ qzeros,
@@ -438,39 +477,44 @@ __global__ void __launch_bounds__(128) gptq_dequant_nk(const int32_t* __restrict
                                                        void* __restrict__ out) {
     constexpr int KT = 128, OB = BF16 ? 2 : 4;
     constexpr int ROWB = KT * OB + 16;   // padded row of the output tile
+    constexpr int CPR = KT * OB / 16;    // 16-byte chunks per output row (16 or 32)
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     unsigned char* tile = smem + warp * 32 * ROWB;
+    unsigned char* mine = tile + lane * ROWB;
     const int64_t tn = (n + 31) / 32, tk = (k + KT - 1) / KT;
     const int64_t gwarp = (int64_t)blockIdx.x * 4 + warp, nwarps = (int64_t)gridDim.x * 4;
-    for (int64_t t = gwarp; t < tn * tk; t += nwarps) {
-        const int64_t n0 = (t / tk) * 32, k0 = (t % tk) * KT;
+    const int64_t dn = nwarps / tk, dk = nwarps % tk;
+    const int cpg_mask = lg_group >= 7 ? 15 : (1 << (lg_group - 3)) - 1;  // words per group - 1, capped
+    int64_t nb = gwarp / tk, kb = gwarp % tk;
+    for (; nb < tn;) {
+        const int64_t n0 = nb * 32, k0 = kb * KT;
         const int64_t col = n0 + lane;
         const bool rowv = col < n;
         const int nw = (int)min((int64_t)KT, k - k0) / 8;  // qweight rows in this tile
+        const int32_t* qp = qweight + (k0 / 8) * n + col;
         uint32_t wd[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-            wd[c] = (rowv && c < nw) ? wq::ld_stream1(qweight + (k0 / 8 + c) * n + col) : 0u;
-        unsigned char* mine = tile + lane * ROWB;
+        for (int c = 0; c < 16; ++c) wd[c] = (rowv && c < nw) ? wq::ld_stream1(qp + (int64_t)c * n) : 0u;
+        wq::f2_t S2 = wq::f2(0.f, 0.f), Z2 = wq::f2(-kMagic - 8.f, -kMagic - 8.f);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-            const int64_t kk = k0 + 8 * c;
-            const int64_t g = kk >> lg_group;
-            float s = 0.f;
-            int z = 8;
-            if (rowv && c < nw) {
-                s = __half2float(__ushort_as_half(__ldg(scales + g * n + col)));
-                if (!SYM) z = (int)((__ldg(qzeros + g * (n / 8) + col / 8) >> (4 * (col % 8))) & 15);
+            if ((c & cpg_mask) == 0) {  // first word of a group (uniform)
+                const int64_t g = (k0 + 8 * c) >> lg_group;
+                float sv = 0.f, z = 8.f;
+                if (rowv && c < nw) {
+                    sv = __half2float(__ushort_as_half(__ldg(scales + g * n + col)));
+                    if (!SYM) z = (float)((__ldg(qzeros + g * (n / 8) + col / 8) >> (4 * (col & 7))) & 15);
+                }
+                S2 = wq::f2(sv, sv);
+                Z2 = wq::f2(-(kMagic + z), -(kMagic + z));
             }
-            const wq::f2_t S2 = wq::f2(s, s);
-            const wq::f2_t Z2 = wq::f2(-(kMagic + (float)z), -(kMagic + (float)z));
+            const uint32_t lo = wd[c] & 0x0F0F0F0Fu, hi = (wd[c] >> 4) & 0x0F0F0F0Fu;
             float v[8];
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const uint32_t c0 = (wd[c] >> (8 * p)) & 15u, c1 = (wd[c] >> (8 * p + 4)) & 15u;
-                const wq::f2_t q = wq::f2(__uint_as_float(0x4B400000u | c0), __uint_as_float(0x4B400000u | c1));
-                wq::f2u(wq::mul2(wq::add2(q, Z2), S2), v[2 * p], v[2 * p + 1]);  // (code - zp) * s
+            for (int j = 0; j < 4; ++j) {
+                const wq::f2_t q = wq::f2(__uint_as_float(code_f(lo, j)), __uint_as_float(code_f(hi, j)));
+                wq::f2u(wq::mul2(wq::add2(q, Z2), S2), v[2 * j], v[2 * j + 1]);  // (code - zp) * s
             }
             if (BF16) {
                 *reinterpret_cast<uint4*>(mine + 16 * c) =
@@ -483,17 +527,19 @@ __global__ void __launch_bounds__(128) gptq_dequant_nk(const int32_t* __restrict
         }
         __syncwarp();
         // copy out: row segments of KT*OB bytes, 16 bytes per lane per instruction
-        constexpr int CPR = KT * OB / 16;  // 16-byte chunks per row (16 or 32)
         const int valid_chunks = nw * 8 * OB / 16;
+        unsigned char* obase = reinterpret_cast<unsigned char*>(out) + (n0 * k + k0) * OB;
 #pragma unroll 4
-        for (int i = 0; i < 32 * CPR / 32; ++i) {
-            const int idx = i * 32 + lane, row = idx / CPR, ch = idx % CPR;
-            const int64_t gr = n0 + row;
-            if (gr < n && ch < valid_chunks)
-                *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(out) + (gr * k + k0) * OB + 16 * ch) =
-                    *reinterpret_cast<const uint4*>(tile + row * ROWB + 16 * ch);
+        for (int i = 0; i < CPR; ++i) {
+            const int idx = i * 32 + lane, orow = idx / CPR, ch = idx % CPR;
+            if (n0 + orow < n && ch < valid_chunks)
+                *reinterpret_cast<uint4*>(obase + (int64_t)orow * k * OB + 16 * ch) =
+                    *reinterpret_cast<const uint4*>(tile + orow * ROWB + 16 * ch);
         }
         __syncwarp();
+        nb += dn;
+        kb += dk;
+        if (kb >= tk) { kb -= tk; ++nb; }
     }
 }
 
@@ -502,8 +548,8 @@ wq_status launch_dequant(const int32_t* qweight, const int32_t* qzeros, const ui
                          int64_t n, int64_t k, int group, int layout, void* out, cudaStream_t st) {
     if (layout == WQ_LAYOUT_KN) {
         const void* fn = (const void*)gptq_dequant_kn<SYM, BF16>;
-        const int64_t items = (k / 8) * (n / 2);
-        const int grid = wqh::grid_for(fn, kThreads, 0, (items + kThreads - 1) / kThreads, 1 << 30);
+        const int64_t tiles = (k / 8) * ((n + 4 * kThreads - 1) / (4 * kThreads));
+        const int grid = wqh::grid_for(fn, kThreads, 0, tiles, 1 << 30);
         gptq_dequant_kn<SYM, BF16><<<grid, kThreads, 0, st>>>(qweight, qzeros, scales, n, k, __builtin_ctz(group), out);
     } else {
         const void* fn = (const void*)gptq_dequant_nk<SYM, BF16>;
