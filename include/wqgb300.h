@@ -55,7 +55,7 @@ typedef int wq_status;
 #define WQ_ERR_UNSUPPORTED 5
 #define WQ_ERR_WORKSPACE_TOO_SMALL 6
 #define WQ_ERR_CUDA 7
-#define WQ_ERR_DEVICE_TIMEOUT 8 /* reserved: no kernel in this version waits */
+#define WQ_ERR_DEVICE_TIMEOUT 8 /* a bounded device-side wait ran out (see wq_device_status) */
 
 /* Output element types. */
 #define WQ_DTYPE_F32 0
@@ -90,6 +90,17 @@ const char* wq_last_cuda_error(void);
 /* Library version string. */
 const char* wq_version(void);
 
+/* Device-side status of the kernels that wait on hardware events (the GPTQ
+ * quantize kernels wait on the mbarriers of their TMA loads).  Every such wait
+ * is bounded: one that runs out (a load that never lands) makes the kernel skip
+ * the rest of its work and record WQ_ERR_DEVICE_TIMEOUT in a per-device status
+ * word; the outputs of that call are then incomplete.  This call reads the word
+ * of the current device and clears it: WQ_OK when no wait ran out since the last
+ * call, WQ_ERR_DEVICE_TIMEOUT otherwise, or WQ_ERR_CUDA if the read failed.  It
+ * is synchronous (a device-to-host copy on the legacy default stream): call it
+ * after the streams that ran the kernels have been synchronised. */
+wq_status wq_device_status(void);
+
 /* Bytes of workspace `op` needs for an [n, k] weight (0 if none).  Pure host
  * arithmetic: needs no GPU. */
 size_t wq_workspace_bytes(int op, int64_t n, int64_t k, int arg);
@@ -117,7 +128,9 @@ size_t wq_workspace_bytes(int op, int64_t n, int64_t k, int arg);
  *   asym: scale = max(wmax - wmin, 1e-9) / 15, zp = clamp(round(-wmin/scale), 0, 15),
  *         code = clamp(round(x / scale) + zp, 0, 15)
  * Bit-exact with a true IEEE division (the kernel uses a correctly rounded
- * reciprocal plus one FMA correction step). */
+ * reciprocal plus one FMA correction step).  n and k must be below 2^31 (the
+ * kernel loads w through a TMA tensor map with 32-bit coordinates).  Device
+ * status: see wq_device_status. */
 wq_status gptq_quantize_sym(const uint16_t* w, int64_t n, int64_t k, int group, int32_t* qweight,
                             int32_t* qzeros, uint16_t* scales, int32_t* g_idx, double* snr_db,
                             void* workspace, size_t workspace_bytes, void* stream);

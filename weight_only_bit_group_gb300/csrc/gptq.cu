@@ -3,23 +3,29 @@
 // for the uint4b8 dequant rule).
 //
 // Quantize.  A warp owns a tile of 16 output channels (rows of w) x 128 input
-// channels (256 for group 256); lanes 2r and 2r+1 own row n0 + r, each half of
-// the tile's input channels.  Tiles are numbered K-fastest, so the warps that
-// run at the same time sweep long contiguous stretches of the same rows.  A tile
-// arrives in shared memory through a two-stage per-warp cp.async pipeline (each
-// copy instruction moves two whole 256-byte row segments into 256-byte aligned,
-// XOR-swizzled rows, so the per-lane reads are bank-conflict free) while the
-// previous tile is coded.  The group max/min is a bf16x2 reduction inside the lane (plus
-// one shuffle when a group spans the lane pair); scale and zero point use true
-// IEEE divisions once per group.  Per element pair, with packed binary32 pairs
-// (f32x2): the clamp to the code range is applied to w itself, in bf16x2, with
-// bounds bf16(lo*s) and bf16(hi*s) (exact, see bound2); the quotient by the
-// scale is a correctly rounded reciprocal plus one FMA correction step
-// (bit-identical to IEEE division); round-half-even comes from the binary32
-// adder (q + 1.5*2^23); the nibble pack is one IMAD per code.  The eight codes
-// along k of one row are one qweight word, so the [K/8, N] transpose costs
-// nothing.  The optional reconstruction SNR is accumulated from the same
-// registers and reduced by the last CTA to finish.
+// channels (256 for group 256); lane h*16 + r owns row n0 + r and half h of the
+// tile's input channels.  Tiles are numbered K-fastest, so the warps that run at
+// the same time sweep long contiguous stretches of the same rows.  A tile
+// arrives in shared memory through a two-stage per-warp TMA pipeline: one lane
+// arms the stage's mbarrier and issues 2D tensor-map loads of 16 x 64 bf16
+// boxes with the 128-byte swizzle, which makes the per-lane 16-byte reads bank
+// conflict free; the next tile streams in while the current one is coded.  The
+// group max/min is a bf16x2 reduction inside the lane (plus one shuffle when a
+// group spans both halves); scale and zero point use true IEEE divisions once
+// per group.  Per element pair, with packed binary32 pairs (f32x2): the clamp
+// to the code range is applied to w itself, in bf16x2, with bounds bf16(lo*s)
+// and bf16(hi*s) (exact, see bound2); the quotient by the scale is a correctly
+// rounded reciprocal plus one FMA correction step (bit-identical to IEEE
+// division); round-half-even comes from the binary32 adder (q + 1.5*2^23); the
+// nibble pack is one multiply-add per code.  The eight codes along k of one row
+// are one qweight word, so the [K/8, N] transpose costs nothing.  The optional
+// reconstruction SNR is accumulated from the same registers and reduced by the
+// last CTA to finish.  Every wait on an mbarrier is bounded: a wait that runs
+// out records WQ_ERR_DEVICE_TIMEOUT in a device status word (read by
+// wq_device_status) and the kernel finishes without touching the stage again.
+#include <cudaTypedefs.h>
+#include <mutex>
+
 #include "wq_common.cuh"
 
 namespace {
@@ -32,17 +38,20 @@ template <int G>
 struct QTile {
     static constexpr int KT = G > 128 ? G : 128;      // input channels per warp tile
     static constexpr int R = 16;                       // output channels per warp tile
-    static constexpr int HALF = KT / 2;                // input channels per lane (2 lanes per row)
+    static constexpr int HALF = KT / 2;                // input channels per lane
     static constexpr int GL = G < HALF ? G : HALF;     // group elements one lane holds
     static constexpr int LPG = G / GL;                 // lanes per group (1 or 2)
-    static constexpr int CH = KT / 8;                  // 16-byte chunks per row
-    static constexpr int ROWB = KT * 2;                // shared-memory row (swizzled, unpadded)
-    static constexpr int STAGE = R * ROWB;             // one stage of one warp
+    static constexpr int NB = KT / 64;                 // TMA boxes (16 rows x 64 bf16) per tile
+    static constexpr int BOXB = R * 128;               // bytes per box
+    static constexpr int STAGE = NB * BOXB;            // one stage of one warp
     static constexpr int NS = 2;                       // pipeline stages
     static constexpr int WARPS = 4;                    // warps per CTA
     static constexpr int THREADS = 32 * WARPS;
-    static constexpr int SMEM = NS * WARPS * STAGE + 1024;  // + room to align the base to 1 KB
-    static constexpr int MINB = KT > 128 ? 3 : 6;          // CTAs per SM (shared memory bound)
+    static constexpr int BARS = WARPS * NS * 8;        // mbarriers after the stages
+    static constexpr int SMEM = NS * WARPS * STAGE + BARS + 1024;  // + room to align to 1 KB
+    // CTAs per SM: shared memory allows 6 (3 for 256-wide tiles); with the SNR
+    // sums the code needs more than the 80 registers that 6 CTAs leave
+    static constexpr int minb(bool snr) { return KT > 128 ? 3 : (snr ? 4 : 6); }
 };
 
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
@@ -113,95 +122,91 @@ __device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst&
     return word;
 }
 
-// Shared-memory position of 16-byte chunk `ch` of tile row `r`: rows stay
-// 256-byte aligned (cp.async destinations line up with the global lines) and
-// the chunks of each half-row are XOR-swizzled by (2*(r%4) + half), so that the
-// eight lanes of a quarter-warp (rows r..r+3, both halves) reading the same
-// logical chunk hit eight different bank groups.
-template <int CH>
-__device__ __forceinline__ int swz(int r, int ch) {
-    const int h = ch / (CH / 2), c = ch % (CH / 2);
-    return h * (CH / 2) + (c ^ ((2 * (r & 3) + h) & 7));
+__device__ unsigned g_device_status;  // WQ_ERR_DEVICE_TIMEOUT once a bounded wait ran out
+
+// Wait for phase `parity` of the mbarrier at shared address `bar`, giving up
+// after kMaxPolls polls (each poll may itself suspend for a while).
+constexpr unsigned kMaxPolls = 1u << 22;
+__device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity) {
+    for (unsigned i = 0; i < kMaxPolls; ++i)
+        if (wq::mbar_try_wait(bar, parity)) return true;
+    return false;
 }
 
-// Warp tile: 16 output channels (rows of w) x KT input channels; lanes 2r and
-// 2r+1 own row n0 + r, each half of the tile's K range (64 values, or 128 for
-// group 256).  Tiles are numbered K-fastest and walked with incremental
-// coordinates; every per-tile and per-chunk address is a precomputed per-lane
-// offset plus a constant.
 template <bool SYM, int G, bool SNR>
-__global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::MINB) gptq_quant_kernel(
-    const uint16_t* __restrict__ w, int64_t n, int64_t k, int32_t* __restrict__ qweight,
+__global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_quant_kernel(
+    const __grid_constant__ CUtensorMap wmap, int64_t n, int64_t k, int32_t* __restrict__ qweight,
     int32_t* __restrict__ qzeros, uint16_t* __restrict__ scales, int32_t* __restrict__ g_idx,
     double* __restrict__ slots, unsigned* __restrict__ counter, double* __restrict__ snr_db) {
     using T = QTile<G>;
-    constexpr int CPL = T::HALF / 8;  // 16-byte chunks per lane per tile
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    // static shared memory (the SNR reduction) may precede the dynamic buffer:
-    // re-align so that every staged row starts on a 256-byte boundary
+    // the 128-byte swizzle needs 1 KB aligned boxes
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int row = lane >> 1, half = lane & 1;
-    const uint32_t wsm = (uint32_t)__cvta_generic_to_shared(smem + warp * (T::NS * T::STAGE));
-    const int64_t tn = (n + T::R - 1) / T::R, tk = (k + T::KT - 1) / T::KT;
-    const int64_t gwarp = (int64_t)blockIdx.x * T::WARPS + warp;
-    const int64_t nwarps = (int64_t)gridDim.x * T::WARPS;
-    const int64_t dn = nwarps / tk, dk = nwarps % tk;  // tile step, once
-
-    // copy plan: instruction i moves chunk (lane % CH) of tile row i*(32/CH) + lane/CH
-    constexpr int RPI = 32 / T::CH;  // rows per copy instruction (2, or 1 for KT = 256)
-    // the swizzle repeats every 4 rows, i.e. every NP instructions
-    constexpr int NP = 4 / RPI;
-    const int cr = lane / T::CH, cch = lane % T::CH;
-    uint32_t cdst[NP];  // destination offset for instruction index i % NP
-#pragma unroll
-    for (int pi = 0; pi < NP; ++pi) {
-        const int r = pi * RPI + cr;
-        cdst[pi] = (uint32_t)(r * T::ROWB + 16 * swz<T::CH>(r, cch));
+    const int row = lane & 15, half = lane >> 4;
+    unsigned char* wsm = smem + warp * (T::NS * T::STAGE);
+    const uint32_t wsm_s = (uint32_t)__cvta_generic_to_shared(wsm);
+    const uint32_t bar_s = (uint32_t)__cvta_generic_to_shared(smem + T::WARPS * T::NS * T::STAGE) + warp * T::NS * 8;
+    // tile coordinates fit in 32 bits (n, k < 2^31)
+    const int tn = (int)((n + T::R - 1) / T::R), tk = (int)((k + T::KT - 1) / T::KT);
+    const int gwarp = blockIdx.x * T::WARPS + warp;
+    const int nwarps = gridDim.x * T::WARPS;
+    const int dn = nwarps / tk, dk = nwarps % tk;  // tile step, once
+    if (lane == 0) {
+        for (int i = 0; i < T::NS; ++i) wq::mbar_init(bar_s + 8 * i, 1);
+        wq::mbar_fence_init();
     }
-    // this lane's reads: chunk c of its half-row sits at roff8[c % 8] + 16 (c - c % 8)
-    // (the swizzle permutes chunks within each aligned group of eight)
-    const int sw_ = (2 * (row & 3) + half) & 7;
-    const uint32_t rbase = (uint32_t)(row * T::ROWB + 16 * half * (T::CH / 2));
+    __syncwarp();
+
+    // this lane's reads: chunk c of its half-row sits at roff8[c % 8] + (c / 8) boxes
+    // (the swizzle permutes the 16-byte chunks of each 128-byte box row by row % 8)
     uint32_t roff8[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) roff8[c] = rbase + 16 * (c ^ sw_);
-#define WQ_CHUNK(c) (*reinterpret_cast<const uint4*>(stage + roff8[(c) & 7] + 16 * ((c) & ~7)))
+    for (int c = 0; c < 8; ++c) roff8[c] = (uint32_t)(half * (T::NB / 2) * T::BOXB + row * 128 + 16 * (c ^ (row & 7)));
+#define WQ_CHUNK(c) (*reinterpret_cast<const uint4*>(stage + roff8[(c) & 7] + ((c) >> 3) * T::BOXB))
 
-    auto issue = [&](int64_t nb, int64_t kb, int stage) {
-        if (nb < tn) {
-            const int64_t n0 = nb * T::R, k0 = kb * T::KT;
-            const bool kv = k0 + 8 * cch < k;
-            const uint16_t* src = w + (n0 + cr) * k + k0 + 8 * cch;
-            const int64_t rows_left = n - n0 - cr;  // copy row r exists iff i*RPI < rows_left
-            const uint32_t dst = wsm + stage * T::STAGE;
+    auto issue = [&](int nb, int kb, int st) {
+        if (lane == 0 && nb < tn) {
+            const uint32_t bar = bar_s + 8 * st, dst = wsm_s + st * T::STAGE;
+            wq::mbar_expect_tx(bar, T::STAGE);
 #pragma unroll
-            for (int i = 0; i < T::R / RPI; ++i) {
-                if (kv && i * RPI < rows_left) {
-                    const uint32_t d = dst + (uint32_t)((i / NP) * 4 * T::ROWB) + cdst[i % NP];
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d),
-                                 "l"(src + (int64_t)i * RPI * k) : "memory");
-                }
-            }
+            for (int b = 0; b < T::NB; ++b)
+                wq::tma_load_2d(dst + b * T::BOXB, &wmap, kb * T::KT + 64 * b, nb * T::R, bar);
         }
-        wq::cp_async_commit();
     };
 
     wq::KSum ksw, kse;
-    int64_t nb = gwarp / tk, kb = gwarp % tk;
-    issue(nb, kb, 0);
-    for (int j = 0; nb < tn; ++j) {
-        int64_t nb2 = nb + dn, kb2 = kb + dk;
-        if (kb2 >= tk) { kb2 -= tk; ++nb2; }
-        issue(nb2, kb2, (j + 1) & 1);
-        wq::cp_async_wait<1>();
-        __syncwarp();
-        const int64_t n0 = nb * T::R, k0 = kb * T::KT;
+    bool ok = true;
+    // (nb, kb): tile being coded; (na, ka): tile NS - 1 steps ahead, being loaded
+    int nb = gwarp / tk, kb = gwarp % tk;
+    int na = nb, ka = kb;
+    auto step = [&](int& x, int& y) {
+        x += dn;
+        y += dk;
+        if (y >= tk) { y -= tk; ++x; }
+    };
+#pragma unroll
+    for (int i = 0; i < T::NS - 1; ++i) {
+        issue(na, ka, i);
+        step(na, ka);
+    }
+    int st = 0, ahead = T::NS - 1;  // stage of the current tile / of the tile ahead
+    uint32_t parity = 0;            // phase parity of the current stage's barrier
+    for (; nb < tn;) {
+        issue(na, ka, ahead);
+        step(na, ka);
+        ahead = ahead + 1 == T::NS ? 0 : ahead + 1;
+        if (!wait_stage(bar_s + 8 * st, parity)) {
+            atomicExch(&g_device_status, (unsigned)WQ_ERR_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+        }
+        const int64_t n0 = (int64_t)nb * T::R, k0 = (int64_t)kb * T::KT;
         const int64_t col = n0 + row;
         const bool rowv = col < n;
         const int64_t kl = k0 + half * T::HALF;  // first input channel of this lane
-        const unsigned char* stage = smem + (j & 1) * T::STAGE + warp * (T::NS * T::STAGE);
+        const unsigned char* stage = wsm + st * T::STAGE;
         int32_t* qp = qweight + (kl / 8) * n + col;  // qweight word of the lane's first chunk
 #pragma unroll
         for (int g = 0; g < T::HALF / T::GL; ++g) {
@@ -219,7 +224,7 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::MINB) gptq_quant_
                     const uint4 v = WQ_CHUNK(c0 + c);
                     m = babsmax2(m, babsmax2(babsmax2(v.x, v.y), babsmax2(v.z, v.w)));
                 }
-                if (T::LPG == 2) m = babsmax2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                if (T::LPG == 2) m = babsmax2(m, __shfl_xor_sync(0xffffffffu, m, 16));
                 m &= 0x7fff7fffu;
                 const float amax = wq::bf_to_f(max(m & 0xffffu, m >> 16));
                 s = fmaxf(__fmul_rn(amax, 0.125f), 1e-9f);  // amax / 8: exact for any bf16 amax
@@ -234,8 +239,8 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::MINB) gptq_quant_
                     mn = bmin2(mn, bmin2(bmin2(v.x, v.y), bmin2(v.z, v.w)));
                 }
                 if (T::LPG == 2) {
-                    mx = bmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                    mn = bmin2(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+                    mx = bmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    mn = bmin2(mn, __shfl_xor_sync(0xffffffffu, mn, 16));
                 }
                 const float wmax = fmaxf(wq::bf_lo(mx), wq::bf_hi(mx));
                 const float wmin = fminf(wq::bf_lo(mn), wq::bf_hi(mn));
@@ -257,11 +262,13 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::MINB) gptq_quant_
                     const float r = __frcp_rn(s);
                     const wq::f2_t R2 = wq::f2(r, r), NS2 = wq::f2(-s, -s);
                     const uint32_t cg = (uint32_t)((int)zp - 0x4B400000) * 0x11111111u;
+                    int32_t* qc = qp + (int64_t)c0 * n;
 #pragma unroll
                     for (int c = 0; c < GC; ++c) {
                         const uint4 v = WQ_CHUNK(c0 + c);
                         const uint32_t word = quant_chunk<SYM, SNR>(v, gc, R2, NS2, cg, sw2, se2);
-                        if (rowv) qp[(int64_t)(c0 + c) * n] = (int32_t)word;
+                        if (rowv) *qc = (int32_t)word;
+                        qc += n;
                     }
                 } else {  // astronomically large scales: plain IEEE division
                     const float lo = -zp, hi = 15.0f - zp;
@@ -270,7 +277,8 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::MINB) gptq_quant_
                     for (int c = 0; c < GC; ++c) {
                         const int cc = c0 + c;
                         const uint4 v = *reinterpret_cast<const uint4*>(
-                            stage + rbase + 16 * ((cc & ~7) | ((cc & 7) ^ sw_)));
+                            stage + half * (T::NB / 2) * T::BOXB + (cc >> 3) * T::BOXB + row * 128 +
+                            16 * ((cc & 7) ^ (row & 7)));
                         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
                         uint32_t word = 0;
 #pragma unroll
@@ -299,12 +307,12 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::MINB) gptq_quant_
             const bool owner = T::LPG == 1 || half == 0;  // one lane writes per group
             if (gval && rowv && owner) scales[gi * n + col] = __half_as_ushort(__float2half_rn(s));
             if (qzeros) {
-                // zero points of 8 consecutive rows (lanes 2r, r = 0..7 or 8..15)
+                // zero points of 8 consecutive rows (lanes h*16 + r, r = 0..7 or 8..15)
                 uint32_t zw = SYM ? 0x77777777u : ((uint32_t)zp << (4 * (row & 7)));
                 if (!SYM) {
+                    zw |= __shfl_xor_sync(0xffffffffu, zw, 1);
                     zw |= __shfl_xor_sync(0xffffffffu, zw, 2);
                     zw |= __shfl_xor_sync(0xffffffffu, zw, 4);
-                    zw |= __shfl_xor_sync(0xffffffffu, zw, 8);
                 }
                 if (gval && rowv && owner && (row & 7) == 0) qzeros[gi * (n / 8) + col / 8] = (int32_t)zw;
             }
@@ -314,13 +322,50 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::MINB) gptq_quant_
                 if (k0 + i < k) g_idx[k0 + i] = (int32_t)((k0 + i) / G);
         }
         __syncwarp();
-        nb = nb2;
-        kb = kb2;
+        step(nb, kb);
+        if (++st == T::NS) { st = 0; parity ^= 1u; }
     }
-    wq::cp_async_wait<0>();
+    if (!ok && lane == 0) {
+        // loads may still be in flight into any stage: wait (bounded) for them
+        // before the CTA's shared memory can be handed to another CTA
+        for (int i = 0; i < T::NS; ++i) wait_stage(bar_s + 8 * i, 0), wait_stage(bar_s + 8 * i, 1);
+    }
+    __syncwarp();
     if (SNR) wq::finish_snr(ksw.value(), kse.value(), slots, counter, snr_db, nullptr);
 }
 #undef WQ_CHUNK
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map of w [n, k] bf16 (row-major): boxes of 16 rows x 64 values with the
+// 128-byte swizzle; reads outside the tensor return zeros.
+wq_status weight_map(const uint16_t* w, int64_t n, int64_t k, CUtensorMap* map) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return wqh::cuda_status(cudaErrorNotSupported);
+    const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)n};
+    const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(w), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? WQ_OK : wqh::cuda_status(cudaErrorInvalidValue);
+}
 
 template <bool SYM, int G, bool SNR>
 wq_status launch_quant(const uint16_t* w, int64_t n, int64_t k, int32_t* qweight, int32_t* qzeros,
@@ -335,11 +380,14 @@ wq_status launch_quant(const uint16_t* w, int64_t n, int64_t k, int32_t* qweight
         if (s != WQ_OK) return s;
         attr_set = true;
     }
+    CUtensorMap map;
+    wq_status s = weight_map(w, n, k, &map);
+    if (s != WQ_OK) return s;
     const int64_t warp_tiles = ((n + T::R - 1) / T::R) * ((k + T::KT - 1) / T::KT);
     const int grid = wqh::grid_for(fn, T::THREADS, T::SMEM, (warp_tiles + T::WARPS - 1) / T::WARPS,
                                    wqh::kMaxPartials);
     gptq_quant_kernel<SYM, G, SNR><<<grid, T::THREADS, T::SMEM, st>>>(
-        w, n, k, qweight, qzeros, scales, g_idx, slots, counter, snr_db);
+        map, n, k, qweight, qzeros, scales, g_idx, slots, counter, snr_db);
     return wqh::check_launch();
 }
 
@@ -350,6 +398,7 @@ wq_status quantize(const uint16_t* w, int64_t n, int64_t k, int group, int32_t* 
     if (n < 0 || k < 0) return WQ_ERR_BAD_SHAPE;
     if (group != 32 && group != 64 && group != 128 && group != 256) return WQ_ERR_UNSUPPORTED;
     if (k % group != 0 || n % 8 != 0) return WQ_ERR_BAD_SHAPE;
+    if (n > INT32_MAX || k > INT32_MAX) return WQ_ERR_BAD_SHAPE;  // TMA coordinates are 32-bit
     if (n == 0 || k == 0) return WQ_OK;
     if (!w || !qweight || !scales) return WQ_ERR_NULL_PTR;
     if (snr_db && !ws) return WQ_ERR_NULL_PTR;
@@ -385,13 +434,6 @@ wq_status quantize(const uint16_t* w, int64_t n, int64_t k, int group, int32_t* 
 // ------------------------------------------------------------------ dequant
 // (code - zp) * scale16, exact in binary32 (a 5-bit integer times an 11-bit
 // significand).
-
-__device__ __forceinline__ int zp_of(const int32_t* __restrict__ qzeros, int64_t g, int64_t n,
-                                     int64_t col, bool sym) {
-    if (sym) return 8;
-    const uint32_t zw = (uint32_t)__ldg(qzeros + g * (n / 8) + col / 8);
-    return (int)((zw >> (4 * (col % 8))) & 15u);
-}
 
 // Codes of one qweight word as binary32 values 1.5*2^23 + code, two at a time:
 // byte j of lo = nibble 2j, byte j of hi = nibble 2j + 1, and one byte permute
@@ -607,4 +649,14 @@ extern "C" wq_status gptq_dequantize(const int32_t* qweight, const int32_t* qzer
                   : launch_dequant<true, false>(qweight, qzeros, scales, n, k, group, out_layout, out, st);
     return bf ? launch_dequant<false, true>(qweight, qzeros, scales, n, k, group, out_layout, out, st)
               : launch_dequant<false, false>(qweight, qzeros, scales, n, k, group, out_layout, out, st);
+}
+
+extern "C" wq_status wq_device_status(void) {
+    unsigned v = 0;
+    wq_status s = wqh::cuda_status(cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v)));
+    if (s != WQ_OK) return s;
+    if (v == 0) return WQ_OK;
+    const unsigned zero = 0;
+    s = wqh::cuda_status(cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero)));
+    return s != WQ_OK ? s : (wq_status)v;
 }
