@@ -19,11 +19,16 @@ weights, N(0, 0.02) with 0.5% outlier input columns), all inputs resident in HBM
 metric value = weight GB/s: bf16 bytes of the weights every quantize and every
 dequantize kernel handles (8 passes x 436.2 MB per step) / step time.
 
+The seven calls of a phase are forked onto seven streams and joined back, so
+the small projections (k/v: 4.2M weights) overlap the large ones; the whole
+step is one CUDA graph.
+
 Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
-launching stream; L2 (129 MB) is flushed by a 256 MB write before every step
-(outside the events; the inputs, 436 MB, exceed L2 anyway); a barrier and
-torch.cuda.synchronize() on both sides of the K timed steps; max over ranks.
-Per-phase events give each kernel's average launch duration for the roofline.
+launching stream; L2 (129 MB) is flushed before every step by a 256 MB write
+followed by a 256 MB read (outside the events, leaving no dirty lines; the
+inputs, 436 MB, exceed L2 anyway); a barrier and torch.cuda.synchronize() on
+both sides of the K timed steps; max over ranks.  Per-phase events (on the
+joining stream) give each phase's duration for the roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -128,18 +133,23 @@ class Workload:
 
         self.wq = wq
         self.dev = device
-        self.layer = synth.gptq_layer(seed=2 + seed_offset, device=device)
-        self.numel = sum(w.numel() for _, w in self.layer)
-        gen = torch.Generator(device=device)
-        gen.manual_seed(4 + seed_offset)
-        gate = dict(self.layer)["gate_proj"]
-        up = dict(self.layer)["up_proj"]
-        self.gate_up = torch.cat([gate, up], 0)  # the page concatenates before searching
-        self.act = synth.awq_activation(gate.shape[1], seed=4 + seed_offset, device=device)
+        # the seven projections live in one buffer, in layer order, so gate and up
+        # are adjacent and the page's torch.cat([gate, up]) is a view
+        src = synth.gptq_layer(seed=2 + seed_offset, device=device)
+        self.numel = sum(w.numel() for _, w in src)
+        self.flat = torch.empty(self.numel, dtype=torch.bfloat16, device=device)
+        self.layer = self.views(self.flat, src)
+        for (_, d), (_, w) in zip(self.layer, src):
+            d.copy_(w)
+        del src
+        self.gate_up = self.gate_up_view(self.flat)
+        self.act = synth.awq_activation(self.gate_up.shape[1], seed=4 + seed_offset, device=device)
         self.alphas = synth.ALPHAS
         self.out = []
-        maxnumel = max(w.numel() for _, w in self.layer)
-        self.deq = torch.empty(maxnumel, dtype=torch.bfloat16, device=device)
+        self.deq = [torch.empty(w.shape, dtype=torch.bfloat16, device=device) for _, w in self.layer]
+        # one stream per projection: a phase forks its seven calls onto them and
+        # joins them back (graph branches when captured)
+        self.streams = [torch.cuda.Stream(device) for _ in self.layer]
         for name, w in self.layer:
             n, k = w.shape
             g = k // GROUP_GPTQ
@@ -168,17 +178,49 @@ class Workload:
                             errs=torch.empty(len(self.alphas), dtype=torch.float64, device=device),
                             ws=wq.workspace(wq.WQ_OP_AWQ_SEARCH, n, k, len(self.alphas), device))
 
-    # phases: (name, callable, algorithmic bytes, weight bytes counted in the metric, kernels)
-    def phases(self, inputs=None):
+    @staticmethod
+    def views(flat, like):
+        out, off = [], 0
+        for name, w in like:
+            out.append((name, flat[off: off + w.numel()].view(w.shape)))
+            off += w.numel()
+        return out
+
+    def gate_up_view(self, flat):
+        d = dict(self.views(flat, self.layer))
+        g, u = d["gate_proj"], d["up_proj"]
+        assert u.data_ptr() == g.data_ptr() + g.numel() * g.element_size()
+        return flat[(g.data_ptr() - flat.data_ptr()) // 2:][: g.numel() + u.numel()].view(
+            g.shape[0] + u.shape[0], g.shape[1])
+
+    def parallel(self, fns):
+        """Run fns[i] on stream i, forked from and joined back to the current stream."""
+        main = torch.cuda.current_stream(self.dev)
+        fork = torch.cuda.Event()
+        fork.record(main)
+        joins = []
+        for f, st in zip(fns, self.streams):
+            st.wait_event(fork)
+            with torch.cuda.stream(st):
+                f()
+            e = torch.cuda.Event()
+            e.record(st)
+            joins.append(e)
+        for e in joins:
+            main.wait_event(e)
+
+    # phases: (name, callable, algorithmic bytes, weight bytes counted in the metric,
+    # kernels, per-projection callables)
+    def phases(self, inputs=None, gate_up=None):
         wq = self.wq
         layer = inputs if inputs is not None else self.layer
+        gate_up = gate_up if gate_up is not None else self.gate_up
         P = []
 
         def each(fn):
-            return lambda: [fn(i, w) for i, (_, w) in enumerate(layer)]
+            fns = [lambda i=i, w=w: fn(i, w) for i, (_, w) in enumerate(layer)]
+            return (lambda: self.parallel(fns)), fns
 
-        def deq_view(w):
-            return self.deq[: w.numel()].view(w.shape)
 
         for tag, quant, sym in (("asym", wq.gptq_quantize_asym, False), ("sym", wq.gptq_quantize_sym, True)):
             def q(i, w, quant=quant, tag=tag):
@@ -190,14 +232,14 @@ class Workload:
                 o = self.out[i][tag]
                 n, k = w.shape
                 wq.gptq_dequantize(o["qweight"], o["qzeros"], o["scales"], n, k, GROUP_GPTQ, sym,
-                                   torch.bfloat16, "nk", out=deq_view(w))
+                                   torch.bfloat16, "nk", out=self.deq[i])
 
             qbytes = sum(2 * w.numel() + w.numel() // 2 + (w.numel() // GROUP_GPTQ) * (2 + 0.5)
                          + 4 * w.shape[1] for _, w in layer)
             dbytes = sum(w.numel() // 2 + (w.numel() // GROUP_GPTQ) * (2 + 0.5) + 2 * w.numel()
                          for _, w in layer)
-            P.append((f"gptq_quantize_{tag}", each(q), qbytes, 2 * self.numel, 2 * len(layer)))
-            P.append((f"gptq_dequantize_{tag}", each(d), dbytes, 2 * self.numel, len(layer)))
+            P.append((f"gptq_quantize_{tag}", *each(q)[:1], qbytes, 2 * self.numel, len(layer), each(q)[1]))
+            P.append((f"gptq_dequantize_{tag}", *each(d)[:1], dbytes, 2 * self.numel, len(layer), each(d)[1]))
 
         def mq(i, w):
             o = self.out[i]["mx"]
@@ -205,14 +247,14 @@ class Workload:
 
         def md(i, w):
             o = self.out[i]["mx"]
-            wq.mxfp4_dequantize(o["packed"], o["e8m0"], torch.bfloat16, out=deq_view(w))
+            wq.mxfp4_dequantize(o["packed"], o["e8m0"], torch.bfloat16, out=self.deq[i])
             s = self.out[i]["snr"]
-            wq.quant_snr(w, deq_view(w), "nk", snr_db=s["snr_db"], rel_err=s["rel_err"], ws=s["ws"])
+            wq.quant_snr(w, self.deq[i], "nk", snr_db=s["snr_db"], rel_err=s["rel_err"], ws=s["ws"])
 
         mx_q = sum(2 * w.numel() + w.numel() // 2 + w.numel() // 32 for _, w in layer)
         mx_d = sum(w.numel() // 2 + w.numel() // 32 + 2 * w.numel() + 4 * w.numel() for _, w in layer)
-        P.append(("mxfp4_quantize", each(mq), mx_q, 2 * self.numel, len(layer)))
-        P.append(("mxfp4_dequantize+quant_snr", each(md), mx_d, 2 * self.numel, 3 * len(layer)))
+        P.append(("mxfp4_quantize", *each(mq)[:1], mx_q, 2 * self.numel, len(layer), each(mq)[1]))
+        P.append(("mxfp4_dequantize+quant_snr", *each(md)[:1], mx_d, 2 * self.numel, 2 * len(layer), each(md)[1]))
 
         def uq(i, w):
             o = self.out[i]["ux"]
@@ -222,33 +264,35 @@ class Workload:
             o = self.out[i]["ux"]
             n, k = w.shape
             wq.uintx_dequantize(o["packed"], o["scale"], o["zp"], n, k, NBITS_UINTX, GROUP_UINTX,
-                                torch.bfloat16, out=deq_view(w))
+                                torch.bfloat16, out=self.deq[i])
 
         side = 3 / GROUP_UINTX
         ux_q = sum(w.numel() * (2 + NBITS_UINTX / 8 + side) for _, w in layer)
         ux_d = sum(w.numel() * (NBITS_UINTX / 8 + side + 2) for _, w in layer)
-        P.append(("uintx_quantize", each(uq), ux_q, 2 * self.numel, len(layer)))
-        P.append(("uintx_dequantize", each(ud), ux_d, 2 * self.numel, len(layer)))
+        P.append(("uintx_quantize", *each(uq)[:1], ux_q, 2 * self.numel, len(layer), each(uq)[1]))
+        P.append(("uintx_dequantize", *each(ud)[:1], ux_d, 2 * self.numel, len(layer), each(ud)[1]))
 
         def awq():
             o = self.awq_out
-            wq.awq_search(self.gate_up, self.act, self.alphas, 2048, 0, best_s=o["best_s"],
+            wq.awq_search(gate_up, self.act, self.alphas, 2048, 0, best_s=o["best_s"],
                           best_idx=o["best_idx"], best_alpha=o["best_alpha"], errs=o["errs"], ws=o["ws"])
 
         awq_bytes = 2048 * self.gate_up.shape[1] * 2
-        P.append(("awq_search", awq, awq_bytes, 0, 3))
+        P.append(("awq_search", awq, awq_bytes, 0, 4, None))
         return P
 
     def results(self):
-        """The step's products a caller takes home (quantized tensors + scalars)."""
-        outs = []
+        """The step's products a caller takes home (quantized tensors + scalars):
+        one list per projection, then the AWQ search's."""
+        per = []
         for o in self.out:
+            outs = []
             for tag in ("asym", "sym"):
                 outs += [o[tag]["qweight"], o[tag]["qzeros"], o[tag]["scales"], o[tag]["snr_db"]]
             outs += [o["mx"]["packed"], o["mx"]["e8m0"], o["snr"]["snr_db"], o["snr"]["rel_err"]]
             outs += [o["ux"]["packed"], o["ux"]["scale"], o["ux"]["zp"]]
-        outs += [self.awq_out["best_s"], self.awq_out["best_idx"], self.awq_out["errs"]]
-        return outs
+            per.append(outs)
+        return per, [self.awq_out["best_s"], self.awq_out["best_idx"], self.awq_out["errs"]]
 
 
 def source_sha(kernel_file: str) -> str:
@@ -281,6 +325,22 @@ def ncu_traffic(phase: str, launches: int):
 
 
 # ---------------------------------------------------------------- our arm
+def l2_flusher(dev):
+    """Evict L2 (129 MB) between steps: write a 256 MB buffer, then read another
+    256 MB one, so that the step starts with L2 full of clean lines and none of
+    the flush's write-backs land inside the timed region."""
+    dirty = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    clean = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush():
+        dirty.zero_()
+        torch.sum(clean, 0, out=sink)
+
+    return flush
+
+
+# ---------------------------------------------------------------- our arm
 def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -294,7 +354,7 @@ def run_ours(args, rank, world, dist):
 
     wl = Workload(dev, seed_offset=100 * rank)
     phases = wl.phases()
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_l2 = l2_flusher(dev)
     stream = torch.cuda.current_stream(dev)
 
     def timing_event():
@@ -316,7 +376,7 @@ def run_ours(args, rank, world, dist):
 
     # eager warm-up: builds, caches occupancy queries and kernel attributes
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step_body([])
     torch.cuda.synchronize(dev)
 
@@ -329,7 +389,7 @@ def run_ours(args, rank, world, dist):
         with torch.cuda.graph(graph):
             step_body(graph_events)
         for _ in range(args.warmup):
-            flush.zero_()
+            flush_l2()
             graph.replay()
         torch.cuda.synchronize(dev)
 
@@ -349,7 +409,7 @@ def run_ours(args, rank, world, dist):
     with ClockSampler(dev.index) as clk:
         wall0 = time.perf_counter()
         for _ in range(args.steps):
-            flush.zero_()
+            flush_l2()
             evs = step(True)
             # graph events are re-recorded by every replay: read them per step
             torch.cuda.current_stream(dev).synchronize()
@@ -373,7 +433,7 @@ def run_ours(args, rank, world, dist):
     value = world * weight_bytes / (ms * 1e-3) / 1e9
     peak, peak_kind = peaks()
     kernels = {}
-    for name, fn, alg_bytes, wbytes, nk in phases:
+    for name, fn, alg_bytes, wbytes, nk, *_ in phases:
         t = statistics.mean(per_phase[name])
         gbs = alg_bytes / (t * 1e-3) / 1e9
         kernels[name] = {"ms": round(t, 4), "share": None, "alg_GBps": round(gbs, 1),
@@ -405,8 +465,9 @@ def run_ours(args, rank, world, dist):
                    "weights_per_step": wl.numel, "weight_bytes_per_step": weight_bytes,
                    "gptq_group": GROUP_GPTQ, "uintx_nbits": NBITS_UINTX, "uintx_group": GROUP_UINTX,
                    "mxfp4_ties": "half_even", "awq": "gate||up [28672,4096] -> 2048 rows, 11 alphas",
-                   "l2": "flushed (256 MB write) before every step; inputs 436 MB > L2",
-                   "launch": "eager" if args.no_graph else "one CUDA graph per step (captured ABI calls)",
+                   "l2": "flushed before every step (256 MB write, then 256 MB read so no dirty lines remain); inputs 436 MB > L2",
+                   "launch": ("eager" if args.no_graph else "one CUDA graph per step (captured ABI calls)")
+                             + "; the 7 projections of a phase run on 7 concurrent streams",
                    "parallelism": f"replicas x{world} (one layer per GPU, no collective)"},
         "roofline": roofline,
         "kernels": kernels,
@@ -424,24 +485,54 @@ def run_ours(args, rank, world, dist):
 def run_e2e(args, wl, dev, dist, world):
     """Same step through the public API with host-resident inputs: every step
     copies the layer from pinned host memory to the device and copies the
-    quantized products back, inside the timed region."""
-    host_in = [w.cpu().pin_memory() for _, w in wl.layer]
-    dev_in = [torch.empty_like(w) for _, w in wl.layer]
-    outs = wl.results()
-    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    inputs = [(name, d) for (name, _), d in zip(wl.layer, dev_in)]
-    phases = wl.phases(inputs)
-    h2d = sum(h.numel() * h.element_size() for h in host_in)
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+    quantized products back, inside the timed region.  Each projection is one
+    chain on its own stream (copy in, every row of the path, copy out), so the
+    copies of one projection overlap the kernels of the others; the AWQ search
+    starts once gate and up have landed."""
+    host_flat = wl.flat.cpu().pin_memory()
+    dev_flat = torch.empty_like(wl.flat)
+    host_in = wl.views(host_flat, wl.layer)
+    dev_in = wl.views(dev_flat, wl.layer)
+    phases = wl.phases(dev_in, wl.gate_up_view(dev_flat))
+    per_proj, awq_outs = wl.results()
+    host_per = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs] for outs in per_proj]
+    host_awq = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in awq_outs]
+    chains = [[ph[5][i] for ph in phases if ph[5] is not None] for i in range(len(dev_in))]
+    awq_fn = [ph[1] for ph in phases if ph[5] is None]
+    names = [name for name, _ in wl.layer]
+    h2d = host_flat.numel() * host_flat.element_size()
+    d2h = sum(o.numel() * o.element_size() for outs in per_proj for o in outs) + \
+        sum(o.numel() * o.element_size() for o in awq_outs)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        for h, d in zip(host_in, dev_in):
-            d.copy_(h, non_blocking=True)
-        for _, fn, *_ in phases:
-            fn()
-        for o, h in zip(outs, host_out):
+        # fork from the current stream: inside a capture that is the capturing one
+        main = torch.cuda.current_stream(dev)
+        fork = torch.cuda.Event()
+        fork.record(main)
+        joins, landed = [], {}
+        for i, st in enumerate(wl.streams):
+            st.wait_event(fork)
+            with torch.cuda.stream(st):
+                dev_in[i][1].copy_(host_in[i][1], non_blocking=True)
+                if names[i] in ("gate_proj", "up_proj"):
+                    landed[names[i]] = torch.cuda.Event()
+                    landed[names[i]].record(st)
+                for f in chains[i]:
+                    f()
+                for o, h in zip(per_proj[i], host_per[i]):
+                    h.copy_(o, non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(st)
+            joins.append(e)
+        for e in landed.values():
+            main.wait_event(e)
+        for f in awq_fn:
+            f()
+        for o, h in zip(awq_outs, host_awq):
             h.copy_(o, non_blocking=True)
+        for e in joins:
+            main.wait_event(e)
 
     for _ in range(max(1, args.warmup)):
         step()
@@ -626,7 +717,7 @@ def run_single(args):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     times = []
     for i in range(args.warmup + args.steps):
-        flush.zero_()
+        flush_l2()
         a_ = torch.cuda.Event(enable_timing=True)
         b_ = torch.cuda.Event(enable_timing=True)
         a_.record()

@@ -131,6 +131,9 @@ def test_gptq_layer_full_size_asym():
     refs = pool_map(lambda t: oracle.gptq_quantize(t[1], 128, False), layer)
     for (name, w), ref in zip(layer, refs):
         check_gptq(w, 128, False, ref)
+    torch.cuda.synchronize()
+    # no TMA wait of the quantize kernels ran out of its poll budget
+    assert wq.device_status() == wq.WQ_OK
 
 
 def test_gptq_layer_full_size_sym_sampled():

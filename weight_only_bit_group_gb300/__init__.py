@@ -76,6 +76,7 @@ def lib():
                 "wq_status_string": (ctypes.c_char_p, [I]),
                 "wq_last_cuda_error": (ctypes.c_char_p, []),
                 "wq_version": (ctypes.c_char_p, []),
+                "wq_device_status": (I, []),
                 "wq_workspace_bytes": (SZ, [I, I64, I64, I]),
                 "gptq_quantize_sym": (I, [P, I64, I64, I, P, P, P, P, P, P, SZ, P]),
                 "gptq_quantize_asym": (I, [P, I64, I64, I, P, P, P, P, P, P, SZ, P]),
@@ -117,6 +118,13 @@ def _u16(t: torch.Tensor) -> torch.Tensor:
 
 def _empty(shape, dtype, like):
     return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+def device_status() -> int:
+    """Read and clear the device status word of the current device (wq_device_status):
+    WQ_OK, or WQ_ERR_DEVICE_TIMEOUT if a bounded device-side wait ran out since the
+    last read.  Synchronises with the legacy default stream."""
+    return int(lib().wq_device_status())
 
 
 def workspace_bytes(op: int, n: int, k: int, arg: int = 0) -> int:
