@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads) awq_err(const uint16_t* __restrict__
                                                     int64_t rows, int64_t row_stride, int n_alpha,
                                                     AlphaList al, const float* __restrict__ s_tab,
                                                     const float* __restrict__ q_tab,
-                                                    double* __restrict__ slots,
+                                                    float2* __restrict__ slots,
                                                     unsigned* __restrict__ counter,
                                                     float* __restrict__ best_s,
                                                     int32_t* __restrict__ best_idx,
@@ -259,23 +259,37 @@ __global__ void __launch_bounds__(kThreads) awq_err(const uint16_t* __restrict__
         }
     }
 
-    // CTA partial per alpha, fixed order; the last CTA to finish reduces them all
-    __shared__ double red[kThreads / 32][kMaxAlpha];
+    // CTA partial per alpha, fixed order, in float-float (binary32 hi + lo pairs on
+    // the FP32 pipes); the last CTA to finish reduces them all.  Within a warp a
+    // transposed butterfly halves the number of values per lane at each step, so
+    // that lane l ends with the warp's sum for alpha l / 2.
+    __shared__ float2 red[kThreads / 32][kMaxAlpha];
     __shared__ double e[kMaxAlpha];
     __shared__ bool last;
     __shared__ int best;
+    wq::FF v[kMaxAlpha];
 #pragma unroll
-    for (int i = 0; i < kMaxAlpha; ++i) {
-        double v = acc[i].value();
+    for (int i = 0; i < kMaxAlpha; ++i) v[i] = wq::ff_of(acc[i]);
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
-        if (lane == 0) red[warp][i] = v;
+    for (int h = kMaxAlpha / 2, m = 16; h >= 1; h >>= 1, m >>= 1) {
+        const bool upper = (lane & m) != 0;  // keeps the upper half of its values
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const wq::FF keep = upper ? v[i + h] : v[i];
+            const wq::FF send = upper ? v[i] : v[i + h];
+            v[i] = wq::ff_add(keep, wq::ff_shfl_xor(send, m));
+        }
     }
+    v[0] = wq::ff_add(v[0], wq::ff_shfl_xor(v[0], 1));
+    if ((lane & 1) == 0) red[warp][lane >> 1] = make_float2(v[0].hi, v[0].lo);
     __syncthreads();
     if (threadIdx.x < n_alpha) {
-        double t = 0.0;
-        for (int wgi = 0; wgi < kThreads / 32; ++wgi) t += red[wgi][threadIdx.x];
-        slots[(int64_t)blockIdx.x * n_alpha + threadIdx.x] = t;
+        wq::FF t{0.f, 0.f};
+        for (int wgi = 0; wgi < kThreads / 32; ++wgi) {
+            const float2 r = red[wgi][threadIdx.x];
+            t = wq::ff_add(t, wq::FF{r.x, r.y});
+        }
+        slots[(int64_t)blockIdx.x * n_alpha + threadIdx.x] = make_float2(t.hi, t.lo);
         __threadfence();
     }
     __syncthreads();
@@ -285,11 +299,14 @@ __global__ void __launch_bounds__(kThreads) awq_err(const uint16_t* __restrict__
     __threadfence();
     // warp w sums alphas w, w + 8: lane-strided slots, then a fixed shuffle tree
     for (int i = warp; i < n_alpha; i += kThreads / 32) {
-        double t = 0.0;
-        for (unsigned b = lane; b < gridDim.x; b += 32) t += __ldcg(slots + (int64_t)b * n_alpha + i);
+        wq::FF t{0.f, 0.f};
+        for (unsigned b = lane; b < gridDim.x; b += 32) {
+            const float2 r = __ldcg(slots + (int64_t)b * n_alpha + i);
+            t = wq::ff_add(t, wq::FF{r.x, r.y});
+        }
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
-        if (lane == 0) e[i] = t;
+        for (int m = 16; m >= 1; m >>= 1) t = wq::ff_add(t, wq::ff_shfl_xor(t, m));
+        if (lane == 0) e[i] = wq::ff_value(t);
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -338,7 +355,7 @@ extern "C" wq_status awq_search(const uint16_t* w, int64_t n, int64_t k, const f
     float* r_tab = (float*)(ws + up((size_t)n_alpha * k * sizeof(float)));  // a_c / s
     float* a_c = (float*)(ws + 2 * up((size_t)n_alpha * k * sizeof(float)));
     double* lan = (double*)(ws + 2 * up((size_t)n_alpha * k * sizeof(float)) + up((size_t)k * sizeof(float)));
-    double* slots = (double*)((char*)lan + up((size_t)k * (sizeof(double) + sizeof(float))));
+    float2* slots = (float2*)((char*)lan + up((size_t)k * (sizeof(double) + sizeof(float))));
 
     cudaStream_t st = (cudaStream_t)stream;
     unsigned* counter = (unsigned*)workspace;
@@ -349,7 +366,8 @@ extern "C" wq_status awq_search(const uint16_t* w, int64_t n, int64_t k, const f
     awq_logs<<<col_ctas, kThreads, 0, st>>>(a, k, a_c, lan);
     s = wqh::check_launch();
     if (s != WQ_OK) return s;
-    awq_tables<<<dim3(col_ctas, (unsigned)n_alpha), kThreads, 0, st>>>(k, al, n_alpha, lan, s_tab, slots, gm,
+    awq_tables<<<dim3(col_ctas, (unsigned)n_alpha), kThreads, 0, st>>>(k, al, n_alpha, lan, s_tab,
+                                                                        reinterpret_cast<double*>(slots), gm,
                                                                         counter);
     s = wqh::check_launch();
     if (s != WQ_OK) return s;
@@ -357,7 +375,8 @@ extern "C" wq_status awq_search(const uint16_t* w, int64_t n, int64_t k, const f
     s = wqh::check_launch();
     if (s != WQ_OK) return s;
     const int64_t items = ((k + 255) / 256) * ((rows + kRowsPerLane - 1) / kRowsPerLane);
-    const int64_t ctas = (items + (kThreads / 32) - 1) / (kThreads / 32);
+    // at least two items per warp: the per-CTA reduction is then a small part of the work
+    const int64_t ctas = (items + 2 * (kThreads / 32) - 1) / (2 * (kThreads / 32));
     if (tie_mode == WQ_TIE_HALF_EVEN) {
         const int grid = wqh::grid_for((const void*)awq_err<WQ_TIE_HALF_EVEN>, kThreads, 0, ctas, wqh::kMaxPartials);
         awq_err<WQ_TIE_HALF_EVEN><<<grid, kThreads, 0, st>>>(w, k, rows, stride, n_alpha, al, s_tab, r_tab,

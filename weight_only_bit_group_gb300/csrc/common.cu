@@ -110,7 +110,7 @@ extern "C" int64_t uintx_packed_bytes(int64_t numel, int nbits) {
 
 // Workspace layouts (all offsets 256-byte aligned):
 //   GPTQ quantize with SNR, quant_snr: control block (arrival counter) |
-//               kMaxPartials x 2 doubles of per-CTA sums.
+//               kMaxPartials x 16-byte per-CTA float-float pairs.
 //   awq_search: control block | s table [n_alpha][k] f32 | a_c/s table
 //               [n_alpha][k] f32 | a_c [k] f32 | ln(an) [k] f64 + an [k] f32 |
 //               per-CTA partials kMaxPartials x n_alpha doubles.

@@ -137,7 +137,7 @@ template <bool SYM, int G, bool SNR>
 __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_quant_kernel(
     const __grid_constant__ CUtensorMap wmap, int64_t n, int64_t k, int32_t* __restrict__ qweight,
     int32_t* __restrict__ qzeros, uint16_t* __restrict__ scales, int32_t* __restrict__ g_idx,
-    double* __restrict__ slots, unsigned* __restrict__ counter, double* __restrict__ snr_db) {
+    float4* __restrict__ slots, unsigned* __restrict__ counter, double* __restrict__ snr_db) {
     using T = QTile<G>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // the 128-byte swizzle needs 1 KB aligned boxes
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
         for (int i = 0; i < T::NS; ++i) wait_stage(bar_s + 8 * i, 0), wait_stage(bar_s + 8 * i, 1);
     }
     __syncwarp();
-    if (SNR) wq::finish_snr(ksw.value(), kse.value(), slots, counter, snr_db, nullptr);
+    if (SNR) wq::finish_snr(wq::ff_of(ksw), wq::ff_of(kse), slots, counter, snr_db, nullptr);
 }
 #undef WQ_CHUNK
 
@@ -369,7 +369,7 @@ wq_status weight_map(const uint16_t* w, int64_t n, int64_t k, CUtensorMap* map) 
 
 template <bool SYM, int G, bool SNR>
 wq_status launch_quant(const uint16_t* w, int64_t n, int64_t k, int32_t* qweight, int32_t* qzeros,
-                       uint16_t* scales, int32_t* g_idx, double* slots, unsigned* counter,
+                       uint16_t* scales, int32_t* g_idx, float4* slots, unsigned* counter,
                        double* snr_db, cudaStream_t st) {
     using T = QTile<G>;
     const void* fn = (const void*)gptq_quant_kernel<SYM, G, SNR>;
@@ -410,7 +410,7 @@ wq_status quantize(const uint16_t* w, int64_t n, int64_t k, int group, int32_t* 
         return WQ_ERR_MISALIGNED;
     cudaStream_t st = (cudaStream_t)stream;
     unsigned* counter = snr_db ? (unsigned*)ws : nullptr;
-    double* slots = snr_db ? (double*)((char*)ws + wqh::kCtrlBytes) : nullptr;
+    float4* slots = snr_db ? (float4*)((char*)ws + wqh::kCtrlBytes) : nullptr;
     if (snr_db) {
         wq_status s0 = wqh::cuda_status(cudaMemsetAsync(counter, 0, sizeof(unsigned), st));
         if (s0 != WQ_OK) return s0;

@@ -4,10 +4,12 @@
 //
 // One pass, deterministic for a given grid: every CTA writes its (sum w^2,
 // sum e^2) to its own workspace slot; the last CTA to finish adds the slots in
-// index order and evaluates the formulas (nothing waits).  Terms are binary32
-// (as the page computes them); each thread sums at most 32 terms in binary32,
-// adds those partials into a compensated binary32 running sum (the binary64
-// pipe is narrow on this GPU), and the CTA and final sums are binary64.
+// index order and evaluates the formulas in binary64 (nothing waits).  Terms are
+// binary32 (as the page computes them); each thread sums at most 32 terms in
+// binary32 and adds those partials into a compensated binary32 running sum; the
+// CTA and final sums are float-float (hi + lo binary32 pairs, about 44 bits) on
+// the FP32 pipes, since the binary64 pipe of this GPU is too narrow for a whole
+// wave of CTAs to reduce in binary64.
 #include "wq_common.cuh"
 
 namespace {
@@ -35,7 +37,7 @@ __device__ __forceinline__ void load_deq8(const void* deq, int64_t c, float d[8]
 template <int DEQ_BF16>
 __global__ void __launch_bounds__(kThreads) snr_partial_nk(const uint4* __restrict__ w,
                                                            const void* __restrict__ deq,
-                                                           int64_t nchunks, double* __restrict__ slots,
+                                                           int64_t nchunks, float4* __restrict__ slots,
                                                            unsigned* __restrict__ counter,
                                                            double* __restrict__ snr_db,
                                                            double* __restrict__ rel_err) {
@@ -64,7 +66,7 @@ __global__ void __launch_bounds__(kThreads) snr_partial_nk(const uint4* __restri
         dw.add(sw);
         de.add(se);
     }
-    wq::finish_snr(dw.value(), de.value(), slots, counter, snr_db, rel_err);
+    wq::finish_snr(wq::ff_of(dw), wq::ff_of(de), slots, counter, snr_db, rel_err);
 }
 
 // deq laid out [k, n] (the GPTQ page's layout): 64 x 64 tiles, the deq tile is
@@ -74,7 +76,7 @@ constexpr int kT = 64;
 template <int DEQ_BF16>
 __global__ void __launch_bounds__(kThreads) snr_partial_kn(const uint16_t* __restrict__ w,
                                                            const void* __restrict__ deq, int64_t n,
-                                                           int64_t k, double* __restrict__ slots,
+                                                           int64_t k, float4* __restrict__ slots,
                                                            unsigned* __restrict__ counter,
                                                            double* __restrict__ snr_db,
                                                            double* __restrict__ rel_err) {
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) snr_partial_kn(const uint16_t* __res
         dw.add(sw);
         de.add(se);
     }
-    wq::finish_snr(dw.value(), de.value(), slots, counter, snr_db, rel_err);
+    wq::finish_snr(wq::ff_of(dw), wq::ff_of(de), slots, counter, snr_db, rel_err);
 }
 
 }  // namespace
@@ -156,7 +158,7 @@ extern "C" wq_status quant_snr(const uint16_t* w, const void* deq, int deq_dtype
     }
     cudaStream_t st = (cudaStream_t)stream;
     unsigned* counter = (unsigned*)workspace;
-    double* slots = (double*)((char*)workspace + wqh::kCtrlBytes);
+    float4* slots = (float4*)((char*)workspace + wqh::kCtrlBytes);
     wq_status s = wqh::cuda_status(cudaMemsetAsync(counter, 0, sizeof(unsigned), st));
     if (s != WQ_OK) return s;
     if (deq_layout == WQ_LAYOUT_NK) {

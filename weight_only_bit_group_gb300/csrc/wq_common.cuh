@@ -167,52 +167,93 @@ __device__ __forceinline__ uint32_t shfl_xor(uint32_t v, int m) {
 }
 
 // ------------------------------------------------------------------ reductions
-// CTA-wide fixed-order sum of a pair of doubles (kThreads = blockDim.x = 256).
-// The result is valid in thread 0 only.
-__device__ __forceinline__ void cta_sum_pair(double& a, double& b, double* sa, double* sb) {
+// Float-float numbers hi + lo (|lo| <= ulp(hi)/2): sums carried in two binary32
+// values with about 44 significant bits, on the FP32 pipes (the binary64 pipe of
+// this GPU is far too narrow for a whole wave of CTAs to reduce in binary64).
+struct FF {
+    float hi, lo;
+};
+// Knuth's TwoSum: s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+    float s, e;
+    two_sum(a.hi, b.hi, s, e);
+    e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+    FF r;
+    r.hi = __fadd_rn(s, e);                   // fast renormalisation (|s| >= |e|)
+    r.lo = __fsub_rn(e, __fsub_rn(r.hi, s));
+    return r;
+}
+__device__ __forceinline__ FF ff_of(const KSum& k) {
+    FF r;
+    two_sum(k.s, k.c, r.hi, r.lo);
+    return r;
+}
+__device__ __forceinline__ FF ff_shfl_xor(FF v, int m) {
+    FF r;
+    r.hi = __shfl_xor_sync(0xffffffffu, v.hi, m);
+    r.lo = __shfl_xor_sync(0xffffffffu, v.lo, m);
+    return r;
+}
+__device__ __forceinline__ double ff_value(FF v) { return (double)v.hi + (double)v.lo; }
+
+// CTA-wide fixed-order sum of two float-float values (blockDim.x a multiple of
+// 32, at most 1024).  `scratch` holds 32 float4; the result is valid in thread 0.
+__device__ __forceinline__ void cta_sum_ff2(FF& a, FF& b, float4* scratch) {
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) {
-        a += __shfl_xor_sync(0xffffffffu, a, m);
-        b += __shfl_xor_sync(0xffffffffu, b, m);
+        a = ff_add(a, ff_shfl_xor(a, m));
+        b = ff_add(b, ff_shfl_xor(b, m));
     }
-    const int warp = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) { sa[warp] = a; sb[warp] = b; }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) scratch[warp] = make_float4(a.hi, a.lo, b.hi, b.lo);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        a = 0.0;
-        b = 0.0;
-        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) { a += sa[i]; b += sb[i]; }
+    if (warp == 0) {
+        const int nw = (int)(blockDim.x >> 5);
+        const float4 v = lane < nw ? scratch[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+        a = FF{v.x, v.y};
+        b = FF{v.z, v.w};
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+            a = ff_add(a, ff_shfl_xor(a, m));
+            b = ff_add(b, ff_shfl_xor(b, m));
+        }
     }
     __syncthreads();
 }
 
 // End of a two-level (sum w^2, sum e^2) reduction, with no waiting: each CTA
-// stores its pair in its own slot, publishes it (fence) and counts itself in;
-// the CTA that arrives last adds all slots in index order (deterministic for a
-// given grid) and writes snr_db = 20*log10(sqrt(Sw)/max(sqrt(Se),1e-12)) and
-// rel_err = sqrt(Se)/sqrt(Sw).  *counter must be 0 when the kernel starts.
-__device__ __forceinline__ void finish_snr(double a, double b, double* slots, unsigned* counter,
+// stores its float-float pair in its own 16-byte slot, publishes it (fence) and
+// counts itself in; the CTA that arrives last adds all slots in index order
+// (deterministic for a given grid) and writes, in binary64,
+// snr_db = 20*log10(sqrt(Sw)/max(sqrt(Se),1e-12)) and rel_err = sqrt(Se)/sqrt(Sw).
+// *counter must be 0 when the kernel starts.
+__device__ __forceinline__ void finish_snr(FF a, FF b, float4* slots, unsigned* counter,
                                            double* snr_db, double* rel_err) {
-    __shared__ double sa[32], sb[32];
+    __shared__ float4 scratch[32];
     __shared__ bool last;
-    cta_sum_pair(a, b, sa, sb);
+    cta_sum_ff2(a, b, scratch);
     if (threadIdx.x == 0) {
-        slots[2 * blockIdx.x] = a;
-        slots[2 * blockIdx.x + 1] = b;
+        slots[blockIdx.x] = make_float4(a.hi, a.lo, b.hi, b.lo);
         __threadfence();
         last = atomicAdd(counter, 1u) == gridDim.x - 1;
     }
     __syncthreads();
     if (!last) return;
     __threadfence();
-    double ta = 0.0, tb = 0.0;
+    FF ta{0.f, 0.f}, tb{0.f, 0.f};
     for (unsigned i = threadIdx.x; i < gridDim.x; i += blockDim.x) {
-        ta += __ldcg(slots + 2 * i);
-        tb += __ldcg(slots + 2 * i + 1);
+        const float4 v = __ldcg(slots + i);
+        ta = ff_add(ta, FF{v.x, v.y});
+        tb = ff_add(tb, FF{v.z, v.w});
     }
-    cta_sum_pair(ta, tb, sa, sb);
+    cta_sum_ff2(ta, tb, scratch);
     if (threadIdx.x == 0) {
-        const double nw = sqrt(ta), ne = sqrt(tb);
+        const double nw = sqrt(ff_value(ta)), ne = sqrt(ff_value(tb));
         if (snr_db) *snr_db = 20.0 * log10(nw / fmax(ne, 1e-12));
         if (rel_err) *rel_err = ne / nw;
     }
@@ -235,7 +276,7 @@ wq_status check_launch();
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 inline bool aligned_to(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
-// Partial-sum slots: a CTA writes its binary64 partials to its own slot and the
+// Partial-sum slots: a CTA writes its partial sums to its own 16-byte slot and the
 // last CTA to finish adds the slots in index order (deterministic for a given
 // grid).  Grids of reduction kernels never exceed this many CTAs.
 constexpr int kMaxPartials = 4096;
