@@ -297,19 +297,19 @@ class Workload:
         return per, [self.awq_out["best_s"], self.awq_out["best_idx"], self.awq_out["errs"]]
 
 
-def source_sha(kernel_file: str) -> str:
-    path = os.path.join(ROOT, "weight_only_bit_group_gb300", "csrc", kernel_file)
+def source_sha(kernel_files) -> str:
+    """Fingerprint of the kernel sources a phase runs (plus the shared header)."""
     h = hashlib.sha256()
-    for p in (path, os.path.join(ROOT, "weight_only_bit_group_gb300", "csrc", "wq_common.cuh")):
-        with open(p, "rb") as fh:
+    for f in list(kernel_files) + ["wq_common.cuh"]:
+        with open(os.path.join(ROOT, "weight_only_bit_group_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-PHASE_SOURCE = {"gptq_quantize_asym": "gptq.cu", "gptq_quantize_sym": "gptq.cu",
-                "gptq_dequantize_asym": "gptq.cu", "gptq_dequantize_sym": "gptq.cu",
-                "mxfp4_quantize": "mxfp4.cu", "mxfp4_dequantize+quant_snr": "mxfp4.cu",
-                "uintx_quantize": "uintx.cu", "uintx_dequantize": "uintx.cu", "awq_search": "awq.cu"}
+PHASE_SOURCE = {"gptq_quantize_asym": ["gptq.cu"], "gptq_quantize_sym": ["gptq.cu"],
+                "gptq_dequantize_asym": ["gptq.cu"], "gptq_dequantize_sym": ["gptq.cu"],
+                "mxfp4_quantize": ["mxfp4.cu"], "mxfp4_dequantize+quant_snr": ["mxfp4.cu", "snr.cu"],
+                "uintx_quantize": ["uintx.cu"], "uintx_dequantize": ["uintx.cu"], "awq_search": ["awq.cu"]}
 
 
 def ncu_traffic(phase: str, launches: int):
@@ -736,7 +736,7 @@ def run_single(args):
         alg = min(n, 2048) * k * 2
     else:
         raise SystemExit(f"unknown kernel {name}")
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_l2 = l2_flusher(dev)
     times = []
     for i in range(args.warmup + args.steps):
         flush_l2()
