@@ -196,12 +196,16 @@ class Workload:
             g.shape[0] + u.shape[0], g.shape[1])
 
     def parallel(self, fns):
-        """Run fns[i] on stream i, forked from and joined back to the current stream."""
+        """Run fns[i] on stream i, forked from and joined back to the current stream;
+        the largest projections are issued first so that the small ones fill in
+        behind them."""
         main = torch.cuda.current_stream(self.dev)
         fork = torch.cuda.Event()
         fork.record(main)
         joins = []
-        for f, st in zip(fns, self.streams):
+        order = sorted(range(len(fns)), key=lambda i: -self.layer[i][1].numel())
+        for i in order:
+            f, st = fns[i], self.streams[i]
             st.wait_event(fork)
             with torch.cuda.stream(st):
                 f()
