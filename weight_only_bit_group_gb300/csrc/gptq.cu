@@ -54,23 +54,6 @@ struct QTile {
     static constexpr int minb(bool snr) { return KT > 128 ? 3 : (snr ? 4 : 6); }
 };
 
-__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-// |a| max |b| per bf16 half (sign bits are garbage: callers mask them).
-__device__ __forceinline__ uint32_t babsmax2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
 // Per-group constants of the code computation.
 struct GroupConst {
     float s;        // binary32 scale
@@ -102,8 +85,8 @@ __device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst&
     uint32_t word = cg;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        uint32_t uc = bmin2(u[p], gc.hi2);
-        if (!SYM) uc = bmax2(uc, gc.lo2);  // sym: w/s >= -8 always
+        uint32_t uc = wq::bmin2(u[p], gc.hi2);
+        if (!SYM) uc = wq::bmax2(uc, gc.lo2);  // sym: w/s >= -8 always
         const wq::f2_t x = wq::bf2_to_f2(uc);
         const wq::f2_t qa = wq::mul2(x, R2);
         const wq::f2_t rem = wq::fma2(qa, NS2, x);                          // x - qa*s, exact
@@ -222,9 +205,9 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
 #pragma unroll
                 for (int c = 0; c < GC; ++c) {
                     const uint4 v = WQ_CHUNK(c0 + c);
-                    m = babsmax2(m, babsmax2(babsmax2(v.x, v.y), babsmax2(v.z, v.w)));
+                    m = wq::babsmax2(m, wq::babsmax2(wq::babsmax2(v.x, v.y), wq::babsmax2(v.z, v.w)));
                 }
-                if (T::LPG == 2) m = babsmax2(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                if (T::LPG == 2) m = wq::babsmax2(m, __shfl_xor_sync(0xffffffffu, m, 16));
                 m &= 0x7fff7fffu;
                 const float amax = wq::bf_to_f(max(m & 0xffffu, m >> 16));
                 s = fmaxf(__fmul_rn(amax, 0.125f), 1e-9f);  // amax / 8: exact for any bf16 amax
@@ -235,12 +218,12 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
 #pragma unroll
                 for (int c = 0; c < GC; ++c) {
                     const uint4 v = WQ_CHUNK(c0 + c);
-                    mx = bmax2(mx, bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w)));
-                    mn = bmin2(mn, bmin2(bmin2(v.x, v.y), bmin2(v.z, v.w)));
+                    mx = wq::bmax2(mx, wq::bmax2(wq::bmax2(v.x, v.y), wq::bmax2(v.z, v.w)));
+                    mn = wq::bmin2(mn, wq::bmin2(wq::bmin2(v.x, v.y), wq::bmin2(v.z, v.w)));
                 }
                 if (T::LPG == 2) {
-                    mx = bmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                    mn = bmin2(mn, __shfl_xor_sync(0xffffffffu, mn, 16));
+                    mx = wq::bmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    mn = wq::bmin2(mn, __shfl_xor_sync(0xffffffffu, mn, 16));
                 }
                 const float wmax = fmaxf(wq::bf_lo(mx), wq::bf_hi(mx));
                 const float wmin = fminf(wq::bf_lo(mn), wq::bf_hi(mn));

@@ -28,6 +28,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr uint32_t kB192x2 = 0x43404340u;  // bf16 192 = 1.5 * 2^7, both halves
 
 struct QParams {
     uint32_t scale_bits;  // bf16 bits of the scale
@@ -150,48 +151,29 @@ __global__ void __launch_bounds__(kThreads, 2) uintx_quant_fused(const uint16_t*
 #pragma unroll
         for (int m = 0; m < 8; ++m) v[m] = valid ? stage_buf[j & 1][m][threadIdx.x] : make_uint4(0, 0, 0, 0);
 
-        float mn[8], mx[8];
+        // group min and max as one bf16x2 word (min, -max): every combining step
+        // is a single min.bf16x2
+        uint32_t st[8];
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
-            float x[8] = {wq::bf_lo(v[m].x), wq::bf_hi(v[m].x), wq::bf_lo(v[m].y), wq::bf_hi(v[m].y),
-                          wq::bf_lo(v[m].z), wq::bf_hi(v[m].z), wq::bf_lo(v[m].w), wq::bf_hi(v[m].w)};
-            float a = x[0], b = x[0];
-#pragma unroll
-            for (int j = 1; j < 8; ++j) { a = fminf(a, x[j]); b = fmaxf(b, x[j]); }
-            mn[m] = a;
-            mx[m] = b;
+            uint32_t lo = wq::bmin2(wq::bmin2(v[m].x, v[m].y), wq::bmin2(v[m].z, v[m].w));
+            uint32_t hi = wq::bmax2(wq::bmax2(v[m].x, v[m].y), wq::bmax2(v[m].z, v[m].w));
+            lo = wq::bmin2(lo, wq::bswap2(lo));
+            hi = wq::bmax2(hi, wq::bswap2(hi));
+            st[m] = __byte_perm(lo, hi ^ 0x80008000u, 0x7610);  // (min, -max)
         }
         // reduce-scatter over the octet: lane c ends with segment c's group
-        float k4n[4], k4x[4];
-        {
-            const bool hb = lane & 4;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float sn = hb ? mn[j] : mn[j + 4], sx = hb ? mx[j] : mx[j + 4];
-                const float rn = wq::shfl_xor(sn, 4), rx = wq::shfl_xor(sx, 4);
-                k4n[j] = fminf(hb ? mn[j + 4] : mn[j], rn);
-                k4x[j] = fmaxf(hb ? mx[j + 4] : mx[j], rx);
+        for (int h = 4, msk = 4; h >= 1; h >>= 1, msk >>= 1) {
+            const bool hb = (lane & msk) != 0;  // keeps the upper half of its values
+#pragma unroll
+            for (int j = 0; j < h; ++j) {
+                const uint32_t keep = hb ? st[j + h] : st[j];
+                const uint32_t send = hb ? st[j] : st[j + h];
+                st[j] = wq::bmin2(keep, wq::shfl_xor(send, msk));
             }
         }
-        float k2n[2], k2x[2];
-        {
-            const bool hb = lane & 2;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float sn = hb ? k4n[j] : k4n[j + 2], sx = hb ? k4x[j] : k4x[j + 2];
-                const float rn = wq::shfl_xor(sn, 2), rx = wq::shfl_xor(sx, 2);
-                k2n[j] = fminf(hb ? k4n[j + 2] : k4n[j], rn);
-                k2x[j] = fmaxf(hb ? k4x[j + 2] : k4x[j], rx);
-            }
-        }
-        float gmn, gmx;
-        {
-            const bool hb = lane & 1;
-            const float sn = hb ? k2n[0] : k2n[1], sx = hb ? k2x[0] : k2x[1];
-            const float rn = wq::shfl_xor(sn, 1), rx = wq::shfl_xor(sx, 1);
-            gmn = fminf(hb ? k2n[1] : k2n[0], rn);
-            gmx = fmaxf(hb ? k2x[1] : k2x[0], rx);
-        }
+        const float gmn = wq::bf_lo(st[0]), gmx = -wq::bf_hi(st[0]);
         const int c = lane & 7;
         const QParams qp = qparams<QMAX>(gmn, gmx);
         if (valid) {
@@ -205,15 +187,32 @@ __global__ void __launch_bounds__(kThreads, 2) uintx_quant_fused(const uint16_t*
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             const uint32_t P = __shfl_sync(0xffffffffu, mine, (lane & ~7) | m);
-            const float inv = wq::bf_to_f(P & 0xffffu);
             const uint32_t z = P >> 16;
-            const float lo = -(float)z, hi = (float)(QMAX - (int)z);
-            const uint32_t c01 = code2<QMAX>(v[m].x, inv, lo, hi, z);
-            const uint32_t c23 = code2<QMAX>(v[m].y, inv, lo, hi, z);
-            const uint32_t c45 = code2<QMAX>(v[m].z, inv, lo, hi, z);
-            const uint32_t c67 = code2<QMAX>(v[m].w, inv, lo, hi, z);
-            blo[m] = c01 | (c23 << 16);
-            bhi[m] = c45 | (c67 << 16);
+            if (QMAX <= 63) {
+                // bf16(w * inv) clamped to [-zp, qmax - zp], plus 192: the sum lies in
+                // [129, 255], where bf16 has unit spacing, so the addition rounds half to
+                // even and the low byte of each half is 64 + round(.)
+                const uint32_t inv2 = (P & 0xffffu) * 0x10001u;
+                const uint32_t lo2 = wq::f2_to_bf2(-(float)z, -(float)z);
+                const uint32_t hi2 = wq::f2_to_bf2((float)(QMAX - (int)z), (float)(QMAX - (int)z));
+                const uint32_t zadd = (uint32_t)((int)z - 64) * 0x01010101u;
+                uint32_t q[4];
+                const uint32_t u[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    q[i] = wq::badd2(wq::bmin2(wq::bmax2(wq::bmul2(u[i], inv2), lo2), hi2), kB192x2);
+                blo[m] = __byte_perm(q[0], q[1], 0x6420) + zadd;
+                bhi[m] = __byte_perm(q[2], q[3], 0x6420) + zadd;
+            } else {
+                const float inv = wq::bf_to_f(P & 0xffffu);
+                const float lo = -(float)z, hi = (float)(QMAX - (int)z);
+                const uint32_t c01 = code2<QMAX>(v[m].x, inv, lo, hi, z);
+                const uint32_t c23 = code2<QMAX>(v[m].y, inv, lo, hi, z);
+                const uint32_t c45 = code2<QMAX>(v[m].z, inv, lo, hi, z);
+                const uint32_t c67 = code2<QMAX>(v[m].w, inv, lo, hi, z);
+                blo[m] = c01 | (c23 << 16);
+                bhi[m] = c45 | (c67 << 16);
+            }
         }
         if (valid) store_shards<NBITS>(blo, bhi, packed, numel, L1, d);
     }

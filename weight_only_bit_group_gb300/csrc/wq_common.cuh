@@ -53,6 +53,45 @@ __device__ __forceinline__ uint32_t f2_to_bf2(float lo, float hi) {
 // One bf16 operation: the binary32 op result rounded to bf16, back as binary32.
 __device__ __forceinline__ float bfr(float x) { return bf_to_f(f_to_bf(x)); }
 
+// ------------------------------------------------------------------ bf16x2
+// Packed bf16 pairs.  min/max are exact; mul/add/sub round the exact result once
+// to bf16 (nearest even), i.e. they equal the binary32 operation on the bf16
+// operands followed by one bf16 rounding whenever that binary32 result is exact
+// (always for mul; for add/sub of the small integers used here).
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// |a| max |b| per bf16 half (sign bits are garbage: callers mask them).
+__device__ __forceinline__ uint32_t babsmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t badd2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// The two halves of a bf16x2 word swapped.
+__device__ __forceinline__ uint32_t bswap2(uint32_t a) { return __byte_perm(a, 0, 0x1032); }
+
 // ------------------------------------------------------------------ rounding
 // Round half to even of |x| < 2^22 via the binary32 adder: (x + 1.5*2^23) has
 // unit spacing, so the sum is x rounded to an integer with ties to even (the
