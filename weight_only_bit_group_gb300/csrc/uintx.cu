@@ -54,18 +54,6 @@ __device__ __forceinline__ QParams qparams(float mn, float mx) {
     return p;
 }
 
-// Codes of two bf16 weights (packed in u) for one group: q = clamp(round(bf16(w *
-// inv)) + zp, 0, qmax); the clamp is applied before rounding (integer bounds).
-template <int QMAX>
-__device__ __forceinline__ uint32_t code2(uint32_t u, float inv, float lo, float hi, uint32_t zp) {
-    const uint32_t p2 = wq::f2_to_bf2(__fmul_rn(wq::bf_lo(u), inv), __fmul_rn(wq::bf_hi(u), inv));
-    const float p0 = fminf(fmaxf(wq::bf_lo(p2), lo), hi);
-    const float p1 = fminf(fmaxf(wq::bf_hi(p2), lo), hi);
-    const uint32_t c0 = (uint32_t)(__float_as_int(__fadd_rn(p0, kMagic)) - 0x4B400000) + zp;
-    const uint32_t c1 = (uint32_t)(__float_as_int(__fadd_rn(p1, kMagic)) - 0x4B400000) + zp;
-    return c0 | (c1 << 8);  // two code bytes
-}
-
 template <int NBITS>
 struct Shards {
     static constexpr bool has4 = (NBITS & 4) != 0;
@@ -188,30 +176,37 @@ __global__ void __launch_bounds__(kThreads, 2) uintx_quant_fused(const uint16_t*
         for (int m = 0; m < 8; ++m) {
             const uint32_t P = __shfl_sync(0xffffffffu, mine, (lane & ~7) | m);
             const uint32_t z = P >> 16;
-            if (QMAX <= 63) {
-                // bf16(w * inv) clamped to [-zp, qmax - zp], plus 192: the sum lies in
-                // [129, 255], where bf16 has unit spacing, so the addition rounds half to
-                // even and the low byte of each half is 64 + round(.)
-                const uint32_t inv2 = (P & 0xffffu) * 0x10001u;
-                const uint32_t lo2 = wq::f2_to_bf2(-(float)z, -(float)z);
-                const uint32_t hi2 = wq::f2_to_bf2((float)(QMAX - (int)z), (float)(QMAX - (int)z));
-                const uint32_t zadd = (uint32_t)((int)z - 64) * 0x01010101u;
-                uint32_t q[4];
-                const uint32_t u[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+            // bf16(w * inv) clamped to [-zp, qmax - zp] (bf16x2, exact bounds)
+            const uint32_t inv2 = (P & 0xffffu) * 0x10001u;
+            const uint32_t lo2 = wq::f2_to_bf2(-(float)z, -(float)z);
+            const uint32_t hi2 = wq::f2_to_bf2((float)(QMAX - (int)z), (float)(QMAX - (int)z));
+            const uint32_t u[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+            uint32_t q[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    q[i] = wq::badd2(wq::bmin2(wq::bmax2(wq::bmul2(u[i], inv2), lo2), hi2), kB192x2);
+            for (int i = 0; i < 4; ++i) q[i] = wq::bmin2(wq::bmax2(wq::bmul2(u[i], inv2), lo2), hi2);
+            if (QMAX <= 63) {
+                // + 192 in bf16: the sum lies in [129, 255], where bf16 has unit
+                // spacing, so the addition rounds half to even and the low byte of
+                // each half is 64 + round(.)
+                const uint32_t zadd = (uint32_t)((int)z - 64) * 0x01010101u;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) q[i] = wq::badd2(q[i], kB192x2);
                 blo[m] = __byte_perm(q[0], q[1], 0x6420) + zadd;
                 bhi[m] = __byte_perm(q[2], q[3], 0x6420) + zadd;
             } else {
-                const float inv = wq::bf_to_f(P & 0xffffu);
-                const float lo = -(float)z, hi = (float)(QMAX - (int)z);
-                const uint32_t c01 = code2<QMAX>(v[m].x, inv, lo, hi, z);
-                const uint32_t c23 = code2<QMAX>(v[m].y, inv, lo, hi, z);
-                const uint32_t c45 = code2<QMAX>(v[m].z, inv, lo, hi, z);
-                const uint32_t c67 = code2<QMAX>(v[m].w, inv, lo, hi, z);
-                blo[m] = c01 | (c23 << 16);
-                bhi[m] = c45 | (c67 << 16);
+                // + (1.5 * 2^23 + 128) in binary32: the adder rounds half to even (the
+                // offset is even) and the low byte of the sum is 128 + round(.)
+                const uint32_t zadd = (uint32_t)((int)z - 128) * 0x01010101u;
+                const wq::f2_t M2 = wq::f2(kMagic + 128.0f, kMagic + 128.0f);
+                uint32_t b[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float t0, t1;
+                    wq::f2u(wq::add2(wq::bf2_to_f2(q[i]), M2), t0, t1);
+                    b[i] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x0040);
+                }
+                blo[m] = __byte_perm(b[0], b[1], 0x5410) + zadd;
+                bhi[m] = __byte_perm(b[2], b[3], 0x5410) + zadd;
             }
         }
         if (valid) store_shards<NBITS>(blo, bhi, packed, numel, L1, d);
