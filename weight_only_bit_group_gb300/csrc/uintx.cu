@@ -290,8 +290,8 @@ __global__ void __launch_bounds__(kThreads) uintx_pack_general(const uint16_t* _
 // ----------------------------------------------------------- dequant
 // Codes of positions d .. d+7 of all 8 segments from the shard bytes, then
 // out = bf16(bf16(q - zp) * scale): q - zp is an exact small integer and the
-// product of two bf16 values is exact in binary32, so one cvt.rn gives the page's
-// bf16 result.
+// product of two bf16 values is exact in binary32, so one rounding to bf16 (of
+// the binary32 product, or of mul.rn.bf16x2) gives the page's bf16 result.
 template <int NBITS>
 __device__ __forceinline__ void load_codes(const uint8_t* __restrict__ packed, int64_t numel,
                                            int64_t L1, int64_t d, uint32_t (&blo)[8],
@@ -353,16 +353,17 @@ __global__ void __launch_bounds__(kThreads) uintx_dequant_vec(const uint8_t* __r
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             const int64_t e = m * L1 + d, g = e >> lg_group;  // 8 | group: one group
-            const float sc = wq::bf_to_f(__ldg(scale + g));
-            const float zf = (float)__ldg(zp + g);
-            float f[8];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                f[j] = deq1((blo[m] >> (8 * j)) & 0xffu, zf, sc);
-                f[j + 4] = deq1((bhi[m] >> (8 * j)) & 0xffu, zf, sc);
-            }
-            const uint4 o = make_uint4(wq::f2_to_bf2(f[0], f[1]), wq::f2_to_bf2(f[2], f[3]),
-                                       wq::f2_to_bf2(f[4], f[5]), wq::f2_to_bf2(f[6], f[7]));
+            // bf16x2 arithmetic: the code byte under 0x43 is the bf16 128 + q, so
+            // (128 + q) - (128 + zp) is the exact bf16 q - zp and mul.rn rounds the
+            // exact product with the scale once, as the page's bf16 multiply does
+            const uint32_t s2 = (uint32_t)__ldg(scale + g) * 0x10001u;
+            const float zb = 128.0f + (float)__ldg(zp + g);
+            const uint32_t z2 = wq::f2_to_bf2(zb, zb);
+            const uint4 o = make_uint4(
+                wq::bmul2(wq::bsub2(__byte_perm(blo[m], 0x43434343u, 0x4140), z2), s2),
+                wq::bmul2(wq::bsub2(__byte_perm(blo[m], 0x43434343u, 0x4342), z2), s2),
+                wq::bmul2(wq::bsub2(__byte_perm(bhi[m], 0x43434343u, 0x4140), z2), s2),
+                wq::bmul2(wq::bsub2(__byte_perm(bhi[m], 0x43434343u, 0x4342), z2), s2));
             if (BF16) {
                 reinterpret_cast<uint4*>(out)[e / 8] = o;
             } else {
