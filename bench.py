@@ -511,10 +511,11 @@ def run_ours(args, rank, world, dist):
 def run_e2e(args, wl, dev, dist, world):
     """Same step through the public API with host-resident inputs: every step
     copies the layer from pinned host memory to the device and copies the
-    quantized products back, inside the timed region.  Each projection is one
-    chain on its own stream (copy in, every row of the path, copy out), so the
-    copies of one projection overlap the kernels of the others; the AWQ search
-    starts once gate and up have landed."""
+    quantized products back, inside the timed region.  The copies in run one
+    after another on one stream; each projection is then one chain on its own
+    stream (every row of the path, copy out), so the copies of one projection
+    overlap the kernels and copies of the others; the AWQ search starts once gate
+    and up have landed."""
     host_flat = wl.flat.cpu().pin_memory()
     dev_flat = torch.empty_like(wl.flat)
     host_in = wl.views(host_flat, wl.layer)
@@ -531,19 +532,29 @@ def run_e2e(args, wl, dev, dist, world):
         sum(o.numel() * o.element_size() for o in awq_outs)
     stream = torch.cuda.current_stream(dev)
 
+    copy_in = torch.cuda.Stream(dev)
+    order = sorted(range(len(dev_in)), key=lambda i: -dev_in[i][1].numel())
+
     def step():
         # fork from the current stream: inside a capture that is the capturing one
         main = torch.cuda.current_stream(dev)
         fork = torch.cuda.Event()
         fork.record(main)
-        joins, landed = [], {}
-        for i, st in enumerate(wl.streams):
-            st.wait_event(fork)
-            with torch.cuda.stream(st):
+        # host->device copies one after another (largest first) on one stream, so
+        # each projection's chain starts as soon as its own input has landed and
+        # its device->host copies overlap the copies in of the later projections
+        copy_in.wait_event(fork)
+        landed = {}
+        for i in order:
+            with torch.cuda.stream(copy_in):
                 dev_in[i][1].copy_(host_in[i][1], non_blocking=True)
-                if names[i] in ("gate_proj", "up_proj"):
-                    landed[names[i]] = torch.cuda.Event()
-                    landed[names[i]].record(st)
+            landed[i] = torch.cuda.Event()
+            landed[i].record(copy_in)
+        joins = []
+        for i in order:
+            st = wl.streams[i]
+            st.wait_event(landed[i])
+            with torch.cuda.stream(st):
                 for f in chains[i]:
                     f()
                 for o, h in zip(per_proj[i], host_per[i]):
@@ -551,6 +562,7 @@ def run_e2e(args, wl, dev, dist, world):
             e = torch.cuda.Event()
             e.record(st)
             joins.append(e)
+        landed = {names[i]: e for i, e in landed.items() if names[i] in ("gate_proj", "up_proj")}
         for e in landed.values():
             main.wait_event(e)
         for f in awq_fn:
