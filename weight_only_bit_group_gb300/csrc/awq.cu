@@ -128,7 +128,8 @@ __global__ void __launch_bounds__(kThreads) awq_tables(int64_t k, AlphaList al, 
     if (threadIdx.x == 0) *counter = 0u;  // every other CTA has counted itself in: ready for awq_err
 }
 
-// Grid (ceil(k/256), n_alpha): s = t / gm (IEEE) and q = a_c / s.
+// Grid (ceil(k/256), n_alpha): s = t / gm (IEEE) and q = (a_c / s)^2, the
+// column weight of the squared error term.
 __global__ void __launch_bounds__(kThreads) awq_scale(int64_t k, const float* __restrict__ gm,
                                                       const float* __restrict__ a_c,
                                                       float* __restrict__ s_tab,
@@ -138,7 +139,8 @@ __global__ void __launch_bounds__(kThreads) awq_scale(int64_t k, const float* __
     if (c >= k) return;
     const float sv = __fdiv_rn(s_tab[(int64_t)i * k + c], __ldcg(gm + i));
     s_tab[(int64_t)i * k + c] = sv;
-    q_tab[(int64_t)i * k + c] = __fdiv_rn(a_c[c], sv);
+    const float q = __fdiv_rn(a_c[c], sv);
+    q_tab[(int64_t)i * k + c] = __fmul_rn(q, q);
 }
 
 // exp = clamp(floor(log2(amax)) - 2, -127, 127) for a binary32 amax >= 0 (0 -> 0).
@@ -166,6 +168,16 @@ __device__ __forceinline__ void e2m1x2_to_f(uint32_t byte, float& lo, float& hi)
     hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
 }
 
+// e2m1 rounding of (lo, hi) straight back to f16x2 values (round half even,
+// saturating at 6): the nearest grid values, sign included.
+__device__ __forceinline__ uint32_t e2m1_round2(float lo, float hi) {
+    uint32_t h2;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(h2)
+        : "f"(hi), "f"(lo));
+    return h2;
+}
+
 __device__ __forceinline__ uint32_t page_tie(uint32_t nib, float v) {
     const float m = fabsf(v);
     return (m == 0.75f || m == 1.75f || m == 3.5f) ? nib - 2u : nib;
@@ -173,7 +185,10 @@ __device__ __forceinline__ uint32_t page_tie(uint32_t nib, float v) {
 
 // Per element and alpha the page's error term is e = (deq/s - w) * a_c.  Here it
 // is evaluated as (deq - ws) * (a_c/s) with ws = w*s the value that was
-// quantized: algebraically the same product, without a division per element.
+// quantized: algebraically the same product, without a division per element;
+// its square is formed as (e2m1(v) - v)^2 * (a_c/s)^2 per element (v = ws *
+// 2^-exp), summed over the lane's 8 columns of one block row and scaled by
+// 2^exp twice (two steps, so that an exact zero stays zero under a huge scale).
 // deq - ws is exact: with v = ws * 2^-exp (exact), deq - ws = (e2m1(v) - v) *
 // 2^exp and e2m1(v) - v is an exact difference (the two lie within a factor two
 // of each other, or e2m1(v) = 0).  The terms therefore differ from the page's
@@ -203,57 +218,67 @@ __global__ void __launch_bounds__(kThreads) awq_err(const uint16_t* __restrict__
         const int64_t col = (it - rb * col_chunks) * 256 + 8 * lane;
         const int64_t r0 = rb * kRowsPerLane;
         const bool cval = col < k;  // k % 32 == 0: a lane quad is valid or not as a whole
-        uint4 wv[kRowsPerLane];
+        // the lane's 4 x 8 weights as binary32 pairs, shared by every alpha
+        wq::f2_t wf[kRowsPerLane][4];
 #pragma unroll
         for (int q = 0; q < kRowsPerLane; ++q) {
             const int64_t r = r0 + q;
-            wv[q] = (cval && r < rows) ? wq::ld_stream(w + (r * row_stride) * k + col)
-                                       : make_uint4(0, 0, 0, 0);
+            const uint4 u = (cval && r < rows) ? wq::ld_stream(w + (r * row_stride) * k + col)
+                                               : make_uint4(0, 0, 0, 0);
+            wf[q][0] = wq::bf2_to_f2(u.x);
+            wf[q][1] = wq::bf2_to_f2(u.y);
+            wf[q][2] = wq::bf2_to_f2(u.z);
+            wf[q][3] = wq::bf2_to_f2(u.w);
         }
 #pragma unroll
         for (int i = 0; i < kMaxAlpha; ++i) {
             if (i >= n_alpha) break;
-            float s[8], qa[8];
+            wq::f2_t S[4], Q[4];
             {
                 const int64_t off = (int64_t)i * k + (cval ? col : 0);
                 const float4 s0 = __ldg(reinterpret_cast<const float4*>(s_tab + off));
                 const float4 s1 = __ldg(reinterpret_cast<const float4*>(s_tab + off) + 1);
                 const float4 q0 = cval ? __ldg(reinterpret_cast<const float4*>(q_tab + off)) : make_float4(0, 0, 0, 0);
                 const float4 q1 = cval ? __ldg(reinterpret_cast<const float4*>(q_tab + off) + 1) : make_float4(0, 0, 0, 0);
-                s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
-                s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
-                qa[0] = q0.x; qa[1] = q0.y; qa[2] = q0.z; qa[3] = q0.w;
-                qa[4] = q1.x; qa[5] = q1.y; qa[6] = q1.z; qa[7] = q1.w;
+                S[0] = wq::f2(s0.x, s0.y); S[1] = wq::f2(s0.z, s0.w);
+                S[2] = wq::f2(s1.x, s1.y); S[3] = wq::f2(s1.z, s1.w);
+                Q[0] = wq::f2(q0.x, q0.y); Q[1] = wq::f2(q0.z, q0.w);
+                Q[2] = wq::f2(q1.x, q1.y); Q[3] = wq::f2(q1.z, q1.w);
             }
             float part = 0.0f;
 #pragma unroll
             for (int q = 0; q < kRowsPerLane; ++q) {
-                const uint32_t u[4] = {wv[q].x, wv[q].y, wv[q].z, wv[q].w};
-                float ws[8];
-                float amax = 0.0f;
+                wq::f2_t ws[4];
+                float am[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    ws[2 * j] = __fmul_rn(wq::bf_lo(u[j]), s[2 * j]);
-                    ws[2 * j + 1] = __fmul_rn(wq::bf_hi(u[j]), s[2 * j + 1]);
-                    amax = fmaxf(amax, fmaxf(fabsf(ws[2 * j]), fabsf(ws[2 * j + 1])));
+                    ws[j] = wq::mul2(wf[q][j], S[j]);
+                    am[j] = fmaxf(fabsf(ws[j].x), fabsf(ws[j].y));
                 }
+                float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));  // a tree: short chain
                 amax = fmaxf(amax, wq::shfl_xor(amax, 1));
                 amax = fmaxf(amax, wq::shfl_xor(amax, 2));
                 const int ex = exp_from_f32(amax);
                 const float inv = __uint_as_float((uint32_t)(127 - ex) << 23);  // 2^-exp, normal
                 const float sc = __uint_as_float(ex == -127 ? 0x00400000u : (uint32_t)(ex + 127) << 23);
+                const wq::f2_t INV = wq::f2(inv, inv);
+                wq::f2_t loc = wq::f2(0.0f, 0.0f);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float v0 = __fmul_rn(ws[2 * j], inv), v1 = __fmul_rn(ws[2 * j + 1], inv);
-                    uint32_t b = e2m1x2(v0, v1);
-                    if (TIE == WQ_TIE_PAGE_LITERAL) b = page_tie(b & 15u, v0) | (page_tie(b >> 4, v1) << 4);
-                    float m0, m1;
-                    e2m1x2_to_f(b, m0, m1);
-                    const float e0 = __fmul_rn(__fmul_rn(__fsub_rn(m0, v0), sc), qa[2 * j]);
-                    const float e1 = __fmul_rn(__fmul_rn(__fsub_rn(m1, v1), sc), qa[2 * j + 1]);
-                    part = __fmaf_rn(e0, e0, part);
-                    part = __fmaf_rn(e1, e1, part);
+                    const wq::f2_t v = wq::mul2(ws[j], INV);
+                    wq::f2_t m;
+                    if (TIE == WQ_TIE_PAGE_LITERAL) {
+                        uint32_t b = e2m1x2(v.x, v.y);
+                        b = page_tie(b & 15u, v.x) | (page_tie(b >> 4, v.y) << 4);
+                        e2m1x2_to_f(b, m.x, m.y);
+                    } else {
+                        const uint32_t h2 = e2m1_round2(v.x, v.y);
+                        m = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+                    }
+                    const wq::f2_t d = wq::fma2(v, wq::f2(-1.0f, -1.0f), m);  // m - v, exact
+                    loc = wq::fma2(wq::mul2(d, d), Q[j], loc);
                 }
+                part = __fadd_rn(part, __fmul_rn(__fmul_rn(__fadd_rn(loc.x, loc.y), sc), sc));
             }
             acc[i].add(part);
         }
