@@ -330,6 +330,17 @@ def ncu_traffic(phase: str, launches: int):
     return e.get("dram_bytes_per_step") / launches if e.get("dram_bytes_per_step") else None
 
 
+# ---------------------------------------------------------------- ranks
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks (the slowest replica sets the job's time);
+    x itself when there is no process group."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------- our arm
 def l2_flusher(dev):
     """Evict L2 (129 MB) between steps: write a 256 MB buffer, then read another
@@ -449,11 +460,7 @@ def run_ours(args, rank, world, dist):
         wall = time.perf_counter() - wall0
     if dist is not None:
         dist.barrier()
-    ms = statistics.mean(step_ms)
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(step_ms), dist, dev)
 
     weight_bytes = sum(p[3] for p in phases)
     value = world * weight_bytes / (ms * 1e-3) / 1e9
@@ -593,11 +600,7 @@ def run_e2e(args, wl, dev, dist, world):
         step()
     b.record(stream)
     torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(a.elapsed_time(b) / args.steps, dist, dev)
     wbytes = sum(p[3] for p in phases)
     return {"value": round(world * wbytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
