@@ -70,6 +70,7 @@ def _load():
                 "orc_awq_prepare_scales": (None, [P, I64, P, I, P, P]),
                 "orc_awq_search": (None, [P, I64, I64, P, P, I, I, I, P, P, P, P]),
                 "orc_quant_snr": (None, [P, P, I, I, I64, I64, P, P]),
+                "orc_awq_fold": (None, [P, I64, I64, P, I, I, P]),
                 "orc_uintx_packed_bytes": (I64, [I64, I]),
                 "orc_uintx_pack": (None, [P, I64, I, P]),
                 "orc_uintx_unpack": (None, [P, I64, I, P]),
@@ -242,6 +243,21 @@ def quant_snr(w, deq, deq_kn: bool = False):
     _load().orc_quant_snr(_p(w), _p(deq), int(is_bf16), int(deq_kn), n, k, ctypes.byref(snr),
                           ctypes.byref(rel))
     return snr.value, rel.value
+
+
+# --------------------------------------------------------------------------- AWQ fold
+def awq_fold(w, s, axis: int, op: int) -> np.ndarray:
+    """(W.float() * s or / s) rounded to bf16, per column (axis 0, s [k]) or per
+    row (axis 1, s [n]); op 0 multiplies, op 1 divides.  -> uint16 bf16 bits."""
+    w = _u16(w)
+    if w.ndim == 1:
+        w = w.reshape(1, -1)
+    n, k = w.shape
+    s = np.ascontiguousarray(s, np.float32).reshape(-1)
+    assert s.size == (k if axis == 0 else n)
+    out = np.empty_like(w)
+    _load().orc_awq_fold(_p(w), n, k, _p(s), axis, op, _p(out))
+    return out
 
 
 # --------------------------------------------------------------------------- uintx

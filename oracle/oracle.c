@@ -446,6 +446,25 @@ void orc_quant_snr(const uint16_t* w, const void* deq, int deq_bf16, int deq_kn,
     if (rel_err) *rel_err = sqrt(se) / sqrt(sw);
 }
 
+/* The AWQ fold of quantize_dflash_mxfp4.py's main(): once search_scale has
+ * chosen s, the weights are rewritten as (W.float() * s).to(bfloat16) (columns
+ * of q/k/v, gate/up, the conv kernel projections, down), (norm.float() /
+ * s).to(bfloat16) (the norm weights, a [1, k] case) and (up.float() /
+ * s.unsqueeze(1)).to(bfloat16) (rows of up).  Each element: one binary32
+ * multiply or IEEE division of the exact bf16 value by s, then one rounding to
+ * bf16.  axis 0: s has k entries, one per column; axis 1: s has n entries, one
+ * per row.  op 0: multiply; op 1: divide.  out may equal w. */
+void orc_awq_fold(const uint16_t* w, int64_t n, int64_t k, const float* s, int axis, int op,
+                  uint16_t* out) {
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t c = 0; c < k; ++c) {
+            const float x = orc_bf16_to_f32(w[r * k + c]);
+            const float sv = axis == 0 ? s[c] : s[r];
+            const float y = op == 0 ? x * sv : x / sv;
+            out[r * k + c] = orc_f32_to_bf16(y);
+        }
+}
+
 /* ------------------------------------------------------------------------- */
 /* [UX] uintx_quant.py                                                        */
 /* ------------------------------------------------------------------------- */

@@ -45,6 +45,8 @@ void orc_awq_search(const uint16_t* w, int64_t n, int64_t k, const float* a, con
                     float* best_alpha, double* errs);
 void orc_quant_snr(const uint16_t* w, const void* deq, int deq_bf16, int deq_kn, int64_t n,
                    int64_t k, double* snr_db, double* rel_err);
+void orc_awq_fold(const uint16_t* w, int64_t n, int64_t k, const float* s, int axis, int op,
+                  uint16_t* out);
 
 int64_t orc_uintx_packed_bytes(int64_t numel, int nbits);
 void orc_uintx_pack(const uint8_t* codes, int64_t numel, int nbits, uint8_t* out);

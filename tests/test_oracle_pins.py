@@ -588,3 +588,85 @@ def test_awq_error_definition_small():
     np.testing.assert_allclose(errs, want, rtol=1e-12)
     assert bi == int(np.argmin(want)) and ba == ALPHAS[bi]
     assert np.array_equal(best_s, s_all[bi])
+
+
+# --------------------------------------------------------------------------- AWQ fold
+# quantize_dflash_mxfp4.py, main(): (W.float() * s).to(bfloat16) on columns,
+# (norm.float() / s).to(bfloat16), (up.float() / s.unsqueeze(1)).to(bfloat16) on rows.
+
+def _fold_inputs(seed, n, k):
+    rng = np.random.default_rng(seed)
+    w = round_bf16(rng.normal(0, 0.02, (n, k)) * np.exp2(rng.integers(-30, 30, (n, k))))
+    s_k = (np.exp(rng.normal(0, 1, k)) * np.exp2(rng.integers(-20, 20, k))).astype(np.float32)
+    s_n = (np.exp(rng.normal(0, 1, n)) * np.exp2(rng.integers(-20, 20, n))).astype(np.float32)
+    return w, s_k, s_n
+
+
+@pytest.mark.parametrize("op", [0, 1])
+def test_awq_fold_matches_torch_expression(op):
+    """P-F1: the page's own expression run by CPU torch, per column and per row."""
+    torch = pytest.importorskip("torch")
+    w, s_k, s_n = _fold_inputs(31 + op, 24, 64)
+    wt = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16)
+    for axis, s in ((0, s_k), (1, s_n)):
+        st = torch.from_numpy(s)
+        st = st if axis == 0 else st.unsqueeze(1)
+        ref = (wt.float() * st) if op == 0 else (wt.float() / st)
+        ref = ref.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(oracle.awq_fold(w, s, axis, op), ref)
+
+
+def test_awq_fold_rounds_twice():
+    """P-F2: binary32 product first, then bf16 (the page's .float() * s then
+    .to(bfloat16)).  With w = W/128 (W odd) and s = m/2^23 the exact product is
+    W*m*2^-30.  When it lies less than half a binary32 ulp (64 units) below a bf16
+    midpoint whose upper neighbour is the even one, binary32 rounds it up onto
+    the midpoint and bf16 then rounds the tie up, while a single rounding to bf16
+    would go down.  Such (W, m) are built here; the values are checked with exact
+    rational arithmetic."""
+    from fractions import Fraction as F
+
+    def rn(x: F, bits: int) -> F:  # nearest even with `bits` significant bits, x in [1, 2)
+        scaled = x * 2 ** (bits - 1)
+        fl = scaled.numerator // scaled.denominator
+        rem = scaled - fl
+        if rem > F(1, 2) or (rem == F(1, 2) and fl % 2 == 1):
+            fl += 1
+        return F(fl, 2 ** (bits - 1))
+
+    cases = 0
+    for W in range(129, 160, 2):                 # bf16 w = W/128 in (1, 1.25)
+        for j in range(1, 127, 2):               # midpoint 1 + (2j+1) 2^-8, upper neighbour even
+            M = 2 ** 30 + (2 * j + 1) * 2 ** 22
+            r = M % W
+            m = (M - r) // W
+            if not (0 < r < 64 and 2 ** 23 <= m < 2 ** 24):
+                continue
+            w, sv = F(W, 128), F(m, 2 ** 23)
+            once, twice = rn(w * sv, 8), rn(rn(w * sv, 24), 8)
+            assert once != twice
+            got = oracle.awq_fold(np.array([[0x3F80 + (W - 128)]], np.uint16),
+                                  np.array([float(sv)], np.float32), 0, 0)
+            assert F(float(oracle.bf16_bits_to_f32(got)[0, 0])) == twice
+            cases += 1
+    assert cases >= 3
+
+
+def test_awq_fold_power_of_two_scales_are_exact():
+    """P-F3: s = 2^j scales every finite bf16 exactly (no overflow/underflow here)."""
+    rng = np.random.default_rng(33)
+    w = round_bf16(rng.normal(0, 1, (8, 32)))
+    j = rng.integers(-8, 9, 32)
+    s = np.exp2(j).astype(np.float32)
+    want = round_bf16(oracle.bf16_bits_to_f32(w) * s)
+    assert np.array_equal(oracle.awq_fold(w, s, 0, 0), want)
+    assert np.array_equal(oracle.awq_fold(w, (1.0 / s).astype(np.float32), 0, 1), want)
+
+
+def test_awq_fold_rows_are_transposed_columns():
+    """P-F4: folding rows of W equals folding columns of W^T, transposed back."""
+    w, _, s_n = _fold_inputs(34, 16, 40)
+    for op in (0, 1):
+        a = oracle.awq_fold(w, s_n, 1, op)
+        b = oracle.awq_fold(np.ascontiguousarray(w.T), s_n, 0, op).T
+        assert np.array_equal(a, b)
