@@ -749,6 +749,11 @@ def run_single(args):
         re = torch.empty((), dtype=torch.float64, device=dev)
         call = lambda: wq.quant_snr(w, d, "nk", snr_db=sn, rel_err=re, ws=ws)
         alg = n * k * 4
+    elif name == "awq_fold":
+        s_k = synth.awq_activation(k, device=dev).float().contiguous()
+        out = torch.empty_like(w)
+        call = lambda: wq.awq_fold(w, s_k, 0, 0, out=out)
+        alg = n * k * (2 + 2) + 4 * k
     elif name == "awq_search":
         a = synth.awq_activation(k, device=dev)
         call = lambda: wq.awq_search(w, a, synth.ALPHAS, 2048)

@@ -206,6 +206,26 @@ wq_status awq_search_static_scratch(const uint16_t* w, int64_t n, int64_t k, con
                                     int tie_mode, float* best_s, int32_t* best_idx,
                                     float* best_alpha, double* errs, void* stream);
 
+/* awq_fold (quantize_dflash_mxfp4.py, main(): the fold after search_scale --
+ * norm weights / s, conv kernel projections, q/k/v, gate/up and down columns
+ * * s, up's rows / down's s).
+ * In:  w    bf16 [n, k] (a norm weight is the case n = 1), 16-byte aligned; k % 8 == 0.
+ *      s    binary32 device array: k entries (axis WQ_FOLD_COLUMNS, 16-byte
+ *           aligned) or n entries (axis WQ_FOLD_ROWS).
+ *      op   WQ_FOLD_MUL or WQ_FOLD_DIV.
+ * Out: out  bf16 [n, k], 16-byte aligned; may be w itself (in-place fold).
+ * Math per element: bf16(binary32(w op s)), op a binary32 multiply or IEEE
+ * division, each rounded to nearest even -- the page's (W.float() * s).to(
+ * torch.bfloat16) with its two roundings; overflow gives inf as the page's
+ * cast does.  s is meant to be finite and nonzero (NaN bit patterns are not
+ * specified). */
+#define WQ_FOLD_COLUMNS 0
+#define WQ_FOLD_ROWS 1
+#define WQ_FOLD_MUL 0
+#define WQ_FOLD_DIV 1
+wq_status awq_fold(const uint16_t* w, int64_t n, int64_t k, const float* s, int axis, int op,
+                   uint16_t* out, void* stream);
+
 /* ---------------------------------------------------------------- uintx
  * uintx_packed_bytes: size of the packed buffer for numel codes of nbits bits:
  * the sum over the power-of-two shards k in {4, 2, 1} present in nbits of

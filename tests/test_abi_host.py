@@ -85,6 +85,17 @@ def test_argument_errors_return_codes(L):
     assert L.awq_search(BAD, 64, 64, BAD, al, 17, 16, 0, BAD, BAD, BAD, BAD, BAD, 1 << 30, None) == 5
 
 
+def test_awq_fold_argument_errors(L):
+    assert L.awq_fold(BAD, 4, 60, BAD, 0, 0, BAD, None) == 2     # k % 8 != 0
+    assert L.awq_fold(BAD, -1, 64, BAD, 0, 0, BAD, None) == 2
+    assert L.awq_fold(BAD, 4, 64, BAD, 2, 0, BAD, None) == 5     # no such axis
+    assert L.awq_fold(BAD, 4, 64, BAD, 0, 3, BAD, None) == 5     # no such op
+    assert L.awq_fold(BAD, 4, 64, None, 0, 0, BAD, None) == 1
+    assert L.awq_fold(MIS, 4, 64, BAD, 0, 0, BAD, None) == 4
+    assert L.awq_fold(BAD, 4, 64, p(0x1004), 0, 0, BAD, None) == 4   # column scales need 16 B
+    assert L.awq_fold(None, 0, 64, None, 1, 1, None, None) == 0      # empty: nothing launched
+
+
 def test_empty_inputs_are_ok_without_gpu(L):
     assert L.mxfp4_quantize(None, 0, 64, 0, None, None, None) == 0
     assert L.uintx_dequantize(None, None, None, 3, 0, 4, 64, 1, None, None) == 0

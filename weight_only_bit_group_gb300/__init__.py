@@ -88,6 +88,7 @@ def lib():
                 "uintx_quantize": (I, [P, I64, I64, I, I, P, P, P, P]),
                 "uintx_dequantize": (I, [P, P, P, I64, I64, I, I, I, P, P]),
                 "quant_snr": (I, [P, P, I, I, I64, I64, P, P, P, SZ, P]),
+                "awq_fold": (I, [P, I64, I64, P, I, I, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -252,6 +253,20 @@ def uintx_dequantize(packed, scale, zp, n, k, nbits, group=64, out_dtype=torch.b
 
 
 # ------------------------------------------------------------------ SNR
+def awq_fold(w, s, axis: int = 0, op: int = 0, *, out=None):
+    """quantize_dflash_mxfp4.py main()'s fold on the GPU: (w.float() * s or / s)
+    rounded to bf16, s per column (axis 0, [K]) or per row (axis 1, [N]); op 0
+    multiplies, op 1 divides.  out may be w (in place).  w: bf16 [N, K] or [K]."""
+    _u16(w)
+    w2 = w.view(1, -1) if w.dim() == 1 else w
+    n, k = w2.shape
+    assert s.dtype == torch.float32 and s.is_contiguous()
+    if out is None:
+        out = torch.empty_like(w)
+    _check(lib().awq_fold(_ptr(w), n, k, _ptr(s), axis, op, _ptr(out), _stream(w.device)), "awq_fold")
+    return out
+
+
 def quant_snr(w, deq, layout="nk", *, snr_db=None, rel_err=None, ws=None):
     """Reconstruction SNR (dB) and relative error of deq against w -> two 0-dim f64 tensors."""
     _u16(w)
