@@ -168,6 +168,21 @@ def gptq_dequantize(qweight, qzeros, scales, n: int, k: int, group: int, sym: bo
     return out
 
 
+def gptq_linear(x, qweight, qzeros, scales, n: int, k: int, group: int, sym: bool):
+    """The consumer of an exported GPTQ checkpoint (export_gptq_cpu.py module
+    docstring: vLLM's W4A16 uint4b8 layer): y = x @ deq(W)^T with deq the
+    dequantized weight [n, k] of the docstring's rule and x bf16 [m, k].  Every
+    product x * deq is exact in binary64 and the sums are binary64 (matmul), so
+    this is the exact result up to binary64 rounding.  Also returns
+    sum_k |x * deq| per output, the scale of the rounding error bound of any
+    binary32 evaluation.  -> (y f64 [m, n], mag f64 [m, n])."""
+    deq = gptq_dequantize(qweight, qzeros, scales, n, k, group, sym).astype(np.float64)
+    xf = bf16_bits_to_f32(_u16(x)).astype(np.float64)
+    if xf.ndim == 1:
+        xf = xf.reshape(1, -1)
+    return xf @ deq.T, np.abs(xf) @ np.abs(deq).T
+
+
 # --------------------------------------------------------------------------- MXFP4
 def mxfp4_quantize(w, tie_mode: int = TIE_HALF_EVEN):
     """bf16 [N,K] -> (packed u8 [N,K/2], e8m0 u8 [N,K/32])."""

@@ -670,3 +670,44 @@ def test_awq_fold_rows_are_transposed_columns():
         a = oracle.awq_fold(w, s_n, 1, op)
         b = oracle.awq_fold(np.ascontiguousarray(w.T), s_n, 0, op).T
         assert np.array_equal(a, b)
+
+
+# --------------------------------------------------------------------------- GPTQ consumer
+def test_gptq_linear_one_hot_rows_pick_dequantized_columns():
+    """P-L1: x = e_j (one-hot bf16 1.0) gives y[:, n] = deq[n, j] for every n:
+    pins the orientation of the product (deq is [n, k], y = x deq^T), checked
+    against the module-docstring dequant words of the hand-packed golden."""
+    rng = np.random.default_rng(51)
+    w = round_bf16(rng.normal(0, 0.02, (16, 256)))
+    for sym in (True, False):
+        qw, qz, sc, _, _ = oracle.gptq_quantize(w, 128, sym)
+        codes = np.array([[(int(qw[kk // 8, nn]) >> (4 * (kk % 8))) & 15 for kk in range(256)]
+                          for nn in range(16)])
+        sc16 = sc.view(np.float16).astype(np.float64)  # [k/g, n]
+        if sym:
+            zp = np.full((2, 16), 8)
+        else:
+            zp = np.array([[(int(qz[g, nn // 8]) >> (4 * (nn % 8))) & 15 for nn in range(16)] for g in range(2)])
+        for j in (0, 5, 127, 128, 255):
+            x = np.zeros((1, 256), np.uint16)
+            x[0, j] = 0x3F80
+            y, _ = oracle.gptq_linear(x, qw, qz, sc, 16, 256, 128, sym)
+            g = j // 128
+            want = (codes[:, j] - zp[g]) * sc16[g]
+            np.testing.assert_array_equal(y[0], want)
+
+
+def test_gptq_linear_rows_are_independent_and_scale_exactly():
+    """P-L2: each row of x gives its own output row (stacking rows stacks
+    outputs), and a power-of-two factor on x scales y exactly."""
+    rng = np.random.default_rng(52)
+    w = round_bf16(rng.normal(0, 0.02, (24, 256)))
+    qw, qz, sc, _, _ = oracle.gptq_quantize(w, 128, False)
+    x = round_bf16(rng.normal(0, 1, (3, 256)))
+    y, mag = oracle.gptq_linear(x, qw, qz, sc, 24, 256, 128, False)
+    assert y.shape == mag.shape == (3, 24) and np.all(mag >= np.abs(y))
+    for r in range(3):
+        yr, _ = oracle.gptq_linear(x[r:r + 1], qw, qz, sc, 24, 256, 128, False)
+        np.testing.assert_array_equal(yr[0], y[r])
+    y4, _ = oracle.gptq_linear(round_bf16(oracle.bf16_bits_to_f32(x) * 4.0), qw, qz, sc, 24, 256, 128, False)
+    np.testing.assert_array_equal(y4, 4.0 * y)
