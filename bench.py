@@ -749,6 +749,15 @@ def run_single(args):
         re = torch.empty((), dtype=torch.float64, device=dev)
         call = lambda: wq.quant_snr(w, d, "nk", snr_db=sn, rel_err=re, ws=ws)
         alg = n * k * 4
+    elif name == "gptq_linear":
+        r = wq.gptq_quantize_asym(w, GROUP_GPTQ, False)
+        xg = torch.Generator().manual_seed(7)
+        xv = torch.randn(1, k, generator=xg).to(torch.bfloat16).to(dev)
+        y = torch.empty(1, n, dtype=torch.float32, device=dev)
+        lws = torch.zeros(wq.lib().gptq_linear_workspace_bytes(1, n), dtype=torch.uint8, device=dev)
+        call = lambda: wq.gptq_linear(xv, r["qweight"], r["qzeros"], r["scales"], n, k, GROUP_GPTQ,
+                                      False, out=y, ws=lws)
+        alg = n * k * 0.5 + (n * k // GROUP_GPTQ) * 2.5 + 2 * k + 4 * n
     elif name == "awq_fold":
         s_k = synth.awq_activation(k, device=dev).float().contiguous()
         out = torch.empty_like(w)
@@ -761,13 +770,20 @@ def run_single(args):
     else:
         raise SystemExit(f"unknown kernel {name}")
     flush_l2 = l2_flusher(dev)
+    call()
+    torch.cuda.synchronize()
+    # the call (its memsets and kernels) captured once: replays time the device
+    # work without host launch gaps between the call's launches
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
     times = []
     for i in range(args.warmup + args.steps):
         flush_l2()
         a_ = torch.cuda.Event(enable_timing=True)
         b_ = torch.cuda.Event(enable_timing=True)
         a_.record()
-        call()
+        graph.replay()
         b_.record()
         torch.cuda.synchronize()
         if i >= args.warmup:

@@ -96,6 +96,19 @@ def test_awq_fold_argument_errors(L):
     assert L.awq_fold(None, 0, 64, None, 1, 1, None, None) == 0      # empty: nothing launched
 
 
+def test_gptq_linear_argument_errors(L):
+    ws = L.gptq_linear_workspace_bytes(1, 4096)
+    assert ws >= 64 * 4096 * 4 and L.gptq_linear_workspace_bytes(9, 4096) == 0
+    assert L.gptq_linear(BAD, 9, BAD, BAD, BAD, 64, 128, 128, 1, 0, BAD, BAD, 1 << 30, None) == 5
+    assert L.gptq_linear(BAD, 1, BAD, BAD, BAD, 64, 100, 128, 1, 0, BAD, BAD, 1 << 30, None) == 2
+    assert L.gptq_linear(BAD, 1, BAD, BAD, BAD, 64, 128, 96, 1, 0, BAD, BAD, 1 << 30, None) == 5
+    assert L.gptq_linear(BAD, 1, BAD, BAD, BAD, 64, 128, 128, 1, 7, BAD, BAD, 1 << 30, None) == 3
+    assert L.gptq_linear(BAD, 1, BAD, None, BAD, 64, 128, 128, 0, 0, BAD, BAD, 1 << 30, None) == 1
+    assert L.gptq_linear(BAD, 1, BAD, BAD, BAD, 64, 128, 128, 1, 0, BAD, BAD, 16, None) == 6
+    assert L.gptq_linear(MIS, 1, BAD, BAD, BAD, 64, 128, 128, 1, 0, BAD, BAD, 1 << 30, None) == 4
+    assert L.gptq_linear(None, 0, None, None, None, 64, 128, 128, 1, 0, None, None, 0, None) == 0
+
+
 def test_empty_inputs_are_ok_without_gpu(L):
     assert L.mxfp4_quantize(None, 0, 64, 0, None, None, None) == 0
     assert L.uintx_dequantize(None, None, None, 3, 0, 4, 64, 1, None, None) == 0

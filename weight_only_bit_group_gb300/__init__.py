@@ -89,6 +89,8 @@ def lib():
                 "uintx_dequantize": (I, [P, P, P, I64, I64, I, I, I, P, P]),
                 "quant_snr": (I, [P, P, I, I, I64, I64, P, P, P, SZ, P]),
                 "awq_fold": (I, [P, I64, I64, P, I, I, P, P]),
+                "gptq_linear_workspace_bytes": (SZ, [I64, I64]),
+                "gptq_linear": (I, [P, I64, P, P, P, I64, I64, I, I, I, P, P, SZ, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -253,6 +255,25 @@ def uintx_dequantize(packed, scale, zp, n, k, nbits, group=64, out_dtype=torch.b
 
 
 # ------------------------------------------------------------------ SNR
+def gptq_linear(x, qweight, qzeros, scales, n, k, group=128, sym=True, out_dtype=torch.float32,
+                *, out=None, ws=None):
+    """y = x deq(W)^T for a decode batch (x bf16 [m, k], 1 <= m <= 8) straight from
+    the GPTQ tensors; y binary32 or bf16 [m, n]."""
+    _u16(x)
+    x2 = x.view(1, -1) if x.dim() == 1 else x
+    m = x2.shape[0]
+    dt = WQ_DTYPE_BF16 if out_dtype == torch.bfloat16 else WQ_DTYPE_F32
+    if out is None:
+        out = torch.empty((m, n), dtype=out_dtype, device=x.device)
+    nbytes = int(lib().gptq_linear_workspace_bytes(m, n))
+    if ws is None:  # zeroed once, as the ABI requires; reusable afterwards
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=x.device)
+    _check(lib().gptq_linear(_ptr(x2), m, _ptr(qweight), _ptr(qzeros), _ptr(scales), n, k, group,
+                             int(sym), dt, _ptr(out), _ptr(ws), ws.numel(), _stream(x.device)),
+           "gptq_linear")
+    return out
+
+
 def awq_fold(w, s, axis: int = 0, op: int = 0, *, out=None):
     """quantize_dflash_mxfp4.py main()'s fold on the GPU: (w.float() * s or / s)
     rounded to bf16, s per column (axis 0, [K]) or per row (axis 1, [N]); op 0
