@@ -43,6 +43,17 @@ __global__ void __launch_bounds__(kThreads) gptq_linear_kernel(
     const int len = (int)((g1 - g0) * G);  // this slice's input channels
     const int S = gridDim.y;
 
+    const int64_t col = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const bool colv = col < n;
+    constexpr int WPG = G / 8;  // qweight words per group
+    // the first group's words are requested before x is staged (independent
+    // loads in flight together); each later group's while the previous is summed
+    uint32_t nx[WPG];
+    if (colv) {
+#pragma unroll
+        for (int r = 0; r < WPG; ++r) nx[r] = (uint32_t)__ldg(qweight + (g0 * WPG + r) * n + col);
+    }
+
     // x[m][g0*G .. g1*G) -> binary32 in shared memory (8 values per thread step)
     for (int i = threadIdx.x; i < M * len / 8; i += kThreads) {
         const int m = i / (len / 8), c = i % (len / 8);
@@ -53,17 +64,18 @@ __global__ void __launch_bounds__(kThreads) gptq_linear_kernel(
     }
     __syncthreads();
 
-    const int64_t col = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const bool colv = col < n;
     float acc[M];
 #pragma unroll
     for (int m = 0; m < M; ++m) acc[m] = 0.0f;
     if (colv) {
-        constexpr int WPG = G / 8;  // qweight words per group
         for (int64_t g = g0; g < g1; ++g) {
             uint32_t wd[WPG];
 #pragma unroll
-            for (int r = 0; r < WPG; ++r) wd[r] = (uint32_t)__ldg(qweight + (g * WPG + r) * n + col);
+            for (int r = 0; r < WPG; ++r) wd[r] = nx[r];
+            if (g + 1 < g1) {
+#pragma unroll
+                for (int r = 0; r < WPG; ++r) nx[r] = (uint32_t)__ldg(qweight + ((g + 1) * WPG + r) * n + col);
+            }
             const float s = __half2float(__ushort_as_half(__ldg(scales + g * n + col)));
             float zp = 8.0f;
             if (!SYM) zp = (float)((__ldg(qzeros + g * (n / 8) + col / 8) >> (4 * (col & 7))) & 15);
