@@ -155,6 +155,39 @@ def test_gptq_layer_full_size_sym_sampled():
         # asym test and on the small configs.
 
 
+def _sampled_gptq(w, group, sym, seed):
+    """GPU on the whole tensor; oracle on 8 blocks of 8 output channels (their
+    qweight columns, scales, and asym qzeros words) -- the blocks keep the qzeros
+    packing along N intact."""
+    n, k = w.shape
+    fn = wq.gptq_quantize_sym if sym else wq.gptq_quantize_asym
+    r = fn(w.to(DEV), group=group, snr=False)
+    rng = np.random.default_rng(seed)
+    blocks = np.sort(rng.choice(n // 8, size=8, replace=False))
+    cols = np.concatenate([np.arange(8 * b, 8 * b + 8) for b in blocks])
+    qw, qz, sc, gi, _ = oracle.gptq_quantize(w[cols], group, sym)
+    assert np.array_equal(npy(r["qweight"])[:, cols], qw)
+    assert np.array_equal(u16(r["scales"])[:, cols], sc)
+    assert np.array_equal(npy(r["qzeros"])[:, blocks], qz)
+    assert np.array_equal(npy(r["g_idx"]), gi)
+
+
+@pytest.mark.parametrize("sym", [True, False])
+def test_gptq_lm_head_shape_sampled(sym):
+    """export_gptq_cpu.py --quantize-lm-head: the lm_head [131072, 2048]
+    (268,435,456 weights), group 128."""
+    w = synth.outlier_columns_bf16(131072, 2048, 0.02, 0.005, 20.0, 71, device="cpu")
+    _sampled_gptq(w, 128, sym, 72)
+
+
+@pytest.mark.parametrize("group", [32, 64, 256])
+def test_gptq_other_groups_large_sampled(group):
+    """The --group values other than the default on the gate_proj shape."""
+    w = synth.outlier_columns_bf16(14336, 4096, 0.02, 0.005, 20.0, 73 + group, device="cpu")
+    for sym in (True, False):
+        _sampled_gptq(w, group, sym, 74 + group)
+
+
 # ------------------------------------------------------------------ MXFP4
 def check_mxfp4(w: torch.Tensor, tie_mode: int, ref=None):
     packed, e8 = wq.mxfp4_quantize(w.to(DEV), tie_mode)
