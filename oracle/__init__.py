@@ -213,6 +213,17 @@ def mxfp4_dequantize(packed, e8m0) -> np.ndarray:
     return out
 
 
+def mxfp4_linear(x, packed, e8m0):
+    """The consumer of MXFP4 weights (the drafter served quantized: y = x @ deq(W)^T)
+    with deq from dequantize_mxfp4 and x bf16 [m, k]; every product is exact in
+    binary64 and the sums are binary64.  -> (y f64 [m, n], sum_k |x deq| f64 [m, n])."""
+    deq = mxfp4_dequantize(packed, e8m0).astype(np.float64)
+    xf = bf16_bits_to_f32(_u16(x)).astype(np.float64)
+    if xf.ndim == 1:
+        xf = xf.reshape(1, -1)
+    return xf @ deq.T, np.abs(xf) @ np.abs(deq).T
+
+
 # --------------------------------------------------------------------------- AWQ
 def awq_prepare_scales(a: np.ndarray, alphas):
     a = np.ascontiguousarray(a, np.float32)

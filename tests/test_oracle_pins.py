@@ -711,3 +711,21 @@ def test_gptq_linear_rows_are_independent_and_scale_exactly():
         np.testing.assert_array_equal(yr[0], y[r])
     y4, _ = oracle.gptq_linear(round_bf16(oracle.bf16_bits_to_f32(x) * 4.0), qw, qz, sc, 24, 256, 128, False)
     np.testing.assert_array_equal(y4, 4.0 * y)
+
+
+def test_mxfp4_linear_one_hot_rows_pick_dequantized_columns():
+    """P-L3: x = e_j gives y[:, n] = +-E2M1[code] * 2^(e8m0 - 127) of weight
+    (n, j), decoded here by hand from the packed nibble (even k low nibble) and
+    the block's E8M0 byte: pins the orientation of the consumer's product."""
+    rng = np.random.default_rng(53)
+    w = round_bf16(rng.normal(0, 0.02, (12, 96)))
+    p, e = oracle.mxfp4_quantize(w)
+    for j in (0, 1, 31, 32, 95):
+        x = np.zeros((1, 96), np.uint16)
+        x[0, j] = 0x3F80
+        y, _ = oracle.mxfp4_linear(x, p, e)
+        byte = p[:, j // 2].astype(int)
+        code = (byte >> 4) if j % 2 else (byte & 15)
+        mag = np.array([E2M1[c & 7] for c in code]) * np.where(code & 8, -1.0, 1.0)
+        want = mag * np.exp2(e[:, j // 32].astype(float) - 127)
+        np.testing.assert_array_equal(y[0], want)
