@@ -762,6 +762,12 @@ def run_single(args):
         call = lambda: wq.gptq_linear(xv, r["qweight"], r["qzeros"], r["scales"], n, k, GROUP_GPTQ,
                                       False, out=y, ws=lws)
         alg = n * k * 0.5 + (n * k // GROUP_GPTQ) * 2.5 + 2 * k + 4 * n
+    elif name == "mxfp4_linear":
+        p, e = wq.mxfp4_quantize(w)
+        xv = torch.randn(1, k, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16).to(dev)
+        y = torch.empty(1, n, dtype=torch.float32, device=dev)
+        call = lambda: wq.mxfp4_linear(xv, p, e, out=y)
+        alg = n * k * (0.5 + 1 / 32) + 2 * k + 4 * n
     elif name == "awq_fold":
         s_k = synth.awq_activation(k, device=dev).float().contiguous()
         out = torch.empty_like(w)

@@ -243,6 +243,22 @@ wq_status gptq_linear(const uint16_t* x, int64_t m, const int32_t* qweight, cons
                       int out_dtype, void* out, void* workspace, size_t workspace_bytes,
                       void* stream);
 
+/* mxfp4_linear (quantize_dflash_mxfp4.py: the drafter's linears are served in
+ * MXFP4; deq as dequantize_mxfp4) -- the consumer for decode batches:
+ * y = x deq(W)^T without materialising deq.  No workspace.
+ * In:  x       bf16 [m, k], 16-byte aligned, 1 <= m <= 8; k % 32 == 0.
+ *      packed  u8 [n, k/2] and e8m0 u8 [n, k/32] as produced by mxfp4_quantize
+ *              (packed 16-byte aligned).
+ * Out: out     [m, n] binary32 or bf16 (the binary32 result rounded to nearest even).
+ * Math: per 8 weights the products x * (+-e2m1 value) are exact and summed in
+ * binary32, multiplied by 2^(e8m0 - 127) and added in binary32; the sums over
+ * lanes and warps run in a fixed order, so the result is the same from run to
+ * run and within (k + 2) * 2^-24 * sum_k |x * deq| of the exact value while no
+ * block scale leaves the normal binary32 range (E8M0 bytes below 24 add at most
+ * 2^-149 per block of absolute error; 255 gives inf as dequantize_mxfp4 does). */
+wq_status mxfp4_linear(const uint16_t* x, int64_t m, const uint8_t* packed, const uint8_t* e8m0,
+                       int64_t n, int64_t k, int out_dtype, void* out, void* stream);
+
 #define WQ_FOLD_COLUMNS 0
 #define WQ_FOLD_ROWS 1
 #define WQ_FOLD_MUL 0

@@ -109,6 +109,15 @@ def test_gptq_linear_argument_errors(L):
     assert L.gptq_linear(None, 0, None, None, None, 64, 128, 128, 1, 0, None, None, 0, None) == 0
 
 
+def test_mxfp4_linear_argument_errors(L):
+    assert L.mxfp4_linear(BAD, 1, BAD, BAD, 64, 48, 0, BAD, None) == 2     # k % 32 != 0
+    assert L.mxfp4_linear(BAD, 9, BAD, BAD, 64, 64, 0, BAD, None) == 5     # m > 8
+    assert L.mxfp4_linear(BAD, 1, BAD, BAD, 64, 64, 5, BAD, None) == 3
+    assert L.mxfp4_linear(BAD, 1, None, BAD, 64, 64, 0, BAD, None) == 1
+    assert L.mxfp4_linear(MIS, 1, BAD, BAD, 64, 64, 0, BAD, None) == 4
+    assert L.mxfp4_linear(None, 0, None, None, 64, 64, 0, None, None) == 0
+
+
 def test_empty_inputs_are_ok_without_gpu(L):
     assert L.mxfp4_quantize(None, 0, 64, 0, None, None, None) == 0
     assert L.uintx_dequantize(None, None, None, 3, 0, 4, 64, 1, None, None) == 0

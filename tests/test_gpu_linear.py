@@ -74,3 +74,29 @@ def test_gptq_linear_empty_k_writes_zeros():
     e = torch.empty(0, dtype=torch.int32, device=DEV)
     wq.gptq_linear(x, e, e, torch.empty(0, dtype=torch.float16, device=DEV), 64, 0, 128, True, out=y)
     assert torch.count_nonzero(y) == 0
+
+
+# ------------------------------------------------------------------ MXFP4 consumer
+def check_mx(x, p, e, out_dtype=torch.float32):
+    y = wq.mxfp4_linear(x.to(DEV), p, e, out_dtype)
+    ref, mag = oracle.mxfp4_linear(x, p.cpu().numpy(), e.cpu().numpy())
+    k = x.shape[-1]
+    got = y.float().cpu().numpy().astype(np.float64)
+    bound = (k + 2) * U * mag
+    if out_dtype == torch.bfloat16:
+        bound = bound + 2.0 ** -8 * (np.abs(ref) + bound)
+    err = np.abs(got - ref)
+    assert np.all(err <= bound + 1e-30), float((err / (bound + 1e-30)).max())
+    return y
+
+
+@pytest.mark.parametrize("shape", [(10, 96), (257, 1056), (4096, 4096), (14336, 4096), (4096, 14336)])
+def test_mxfp4_linear(shape):
+    n, k = shape
+    w = synth.outlier_columns_bf16(n, k, 0.02, 0.005, 20.0, 80 + n, device=DEV)
+    p, e = wq.mxfp4_quantize(w)
+    for m in (1, 3, 8):
+        y1 = check_mx(acts(m, k, 81 + m), p, e)
+        y2 = wq.mxfp4_linear(acts(m, k, 81 + m).to(DEV), p, e)
+        assert torch.equal(y1, y2)
+    check_mx(acts(2, k, 82), p, e, torch.bfloat16)

@@ -91,6 +91,7 @@ def lib():
                 "awq_fold": (I, [P, I64, I64, P, I, I, P, P]),
                 "gptq_linear_workspace_bytes": (SZ, [I64, I64]),
                 "gptq_linear": (I, [P, I64, P, P, P, I64, I64, I, I, I, P, P, SZ, P]),
+                "mxfp4_linear": (I, [P, I64, P, P, I64, I64, I, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -271,6 +272,21 @@ def gptq_linear(x, qweight, qzeros, scales, n, k, group=128, sym=True, out_dtype
     _check(lib().gptq_linear(_ptr(x2), m, _ptr(qweight), _ptr(qzeros), _ptr(scales), n, k, group,
                              int(sym), dt, _ptr(out), _ptr(ws), ws.numel(), _stream(x.device)),
            "gptq_linear")
+    return out
+
+
+def mxfp4_linear(x, packed, e8m0, out_dtype=torch.float32, *, out=None):
+    """y = x deq(W)^T for a decode batch (x bf16 [m, k], 1 <= m <= 8) straight from
+    the MXFP4 codes [n, k/2] and E8M0 bytes [n, k/32]; y binary32 or bf16 [m, n]."""
+    _u16(x)
+    x2 = x.view(1, -1) if x.dim() == 1 else x
+    m, k = x2.shape
+    n = packed.shape[0]
+    dt = WQ_DTYPE_BF16 if out_dtype == torch.bfloat16 else WQ_DTYPE_F32
+    if out is None:
+        out = torch.empty((m, n), dtype=out_dtype, device=x.device)
+    _check(lib().mxfp4_linear(_ptr(x2), m, _ptr(packed), _ptr(e8m0), n, k, dt, _ptr(out),
+                              _stream(x.device)), "mxfp4_linear")
     return out
 
 

@@ -194,7 +194,161 @@ wq_status dispatch_g(int group, int64_t m, const uint16_t* x, const int32_t* qw,
     }
 }
 
+// ------------------------------------------------------------------ MXFP4
+// y = x deq(W)^T from the packed e2m1 codes [n, k/2] and the E8M0 bytes
+// [n, k/32] (quantize_dflash_mxfp4.py: the drafter's linears are served in this
+// format; deq as dequantize_mxfp4).  A CTA of 4 warps owns kRowsMx output rows
+// and all of k; the warps take interleaved K steps; lane = WPL consecutive
+// weights of one 32-weight block (one 16-, 8- or 4-byte code load and one E8M0
+// byte per row), with all rows' loads issued together and the lane's x values
+// converted once and reused for every row.  WPL is 32 for m <= 2, 16 for m <= 4
+// and 8 above (the x values of a lane stay in registers).  Codes -> f16x2 by
+// the hardware e2m1 conversion (exact); products with x are exact in binary32
+// and summed per lane and block, times 2^(e - 127), added per row; then
+// fixed-order warp shuffles and a shared-memory sum over the 4 warps
+// (deterministic, no workspace).
+
+constexpr int kRowsMx = 8;
+constexpr int kThreadsMx = 128;
+
+__device__ __forceinline__ wq::f2_t e2m1_pair(uint32_t byte) {
+    uint32_t h2;
+    const uint16_t in = (uint16_t)byte;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "h"(in));
+    return __half22float2(*reinterpret_cast<const __half2*>(&h2));  // (low nibble, high nibble)
+}
+
+template <int NW>
+__device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&w)[NW]) {
+    if (NW == 4) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+        w[0] = v.x; w[NW > 1 ? 1 : 0] = v.y; w[NW > 2 ? 2 : 0] = v.z; w[NW > 3 ? 3 : 0] = v.w;
+    } else if (NW == 2) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+        w[0] = v.x; w[NW > 1 ? 1 : 0] = v.y;
+    } else {
+        w[0] = __ldg(reinterpret_cast<const uint32_t*>(p));
+    }
+}
+
+template <int M, int WPL>
+__global__ void __launch_bounds__(kThreadsMx) mxfp4_linear_kernel(const uint16_t* __restrict__ x,
+                                                                  const uint8_t* __restrict__ packed,
+                                                                  const uint8_t* __restrict__ e8m0,
+                                                                  int64_t n, int64_t k, int out_bf16,
+                                                                  void* __restrict__ out) {
+    constexpr int WARPS = kThreadsMx / 32;
+    constexpr int NW = WPL / 8;  // 32-bit code words (8 codes) per lane and row
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t r0 = (int64_t)blockIdx.x * kRowsMx;
+    float acc[kRowsMx][M];
+#pragma unroll
+    for (int r = 0; r < kRowsMx; ++r)
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
+    for (int64_t kk = ((int64_t)warp * 32 + lane) * WPL; kk < k; kk += (int64_t)WARPS * 32 * WPL) {
+        // every row's codes and scale byte requested before any is decoded (rows
+        // past n read row n - 1 and are never written)
+        uint32_t w[kRowsMx][NW], eb[kRowsMx];
+#pragma unroll
+        for (int r = 0; r < kRowsMx; ++r) {
+            const int64_t row = min(r0 + r, n - 1);
+            load_words<NW>(packed + row * (k / 2) + kk / 2, w[r]);
+            eb[r] = __ldg(e8m0 + row * (k / 32) + kk / 32);
+        }
+        wq::f2_t xv[M][WPL / 2];
+#pragma unroll
+        for (int m = 0; m < M; ++m)
+#pragma unroll
+            for (int q = 0; q < WPL / 8; ++q) {
+                const uint4 u = *reinterpret_cast<const uint4*>(x + m * k + kk + 8 * q);
+                xv[m][4 * q + 0] = wq::bf2_to_f2(u.x);
+                xv[m][4 * q + 1] = wq::bf2_to_f2(u.y);
+                xv[m][4 * q + 2] = wq::bf2_to_f2(u.z);
+                xv[m][4 * q + 3] = wq::bf2_to_f2(u.w);
+            }
+#pragma unroll
+        for (int r = 0; r < kRowsMx; ++r) {
+            const uint32_t e = eb[r];
+            const float sc = __uint_as_float(e == 0 ? 0x00400000u : (e << 23));  // 2^(e-127); 255 -> inf
+            wq::f2_t pm[M];
+#pragma unroll
+            for (int m = 0; m < M; ++m) pm[m] = wq::f2(0.0f, 0.0f);
+#pragma unroll
+            for (int q = 0; q < NW; ++q)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const wq::f2_t c = e2m1_pair((w[r][q] >> (8 * j)) & 0xffu);
+#pragma unroll
+                    for (int m = 0; m < M; ++m) pm[m] = wq::fma2(c, xv[m][4 * q + j], pm[m]);
+                }
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[r][m] = __fmaf_rn(__fadd_rn(pm[m].x, pm[m].y), sc, acc[r][m]);
+        }
+    }
+    __shared__ float red[WARPS][kRowsMx][kMaxM];
+#pragma unroll
+    for (int r = 0; r < kRowsMx; ++r)
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            float v = acc[r][m];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0) red[warp][r][m] = v;
+        }
+    __syncthreads();
+    if (threadIdx.x < kRowsMx * M) {
+        const int r = threadIdx.x / M, m = threadIdx.x % M;
+        const int64_t row = r0 + r;
+        if (row < n) {
+            float y = 0.0f;
+#pragma unroll
+            for (int w2 = 0; w2 < WARPS; ++w2) y = __fadd_rn(y, red[w2][r][m]);
+            if (out_bf16)
+                reinterpret_cast<uint16_t*>(out)[m * n + row] = (uint16_t)wq::f_to_bf(y);
+            else
+                reinterpret_cast<float*>(out)[m * n + row] = y;
+        }
+    }
+}
+
+template <int M>
+wq_status launch_mx_linear(const uint16_t* x, const uint8_t* packed, const uint8_t* e8m0, int64_t n,
+                           int64_t k, int out_bf16, void* out, cudaStream_t st) {
+    constexpr int WPL = M <= 2 ? 32 : (M <= 4 ? 16 : 8);
+    const int64_t grid = (n + kRowsMx - 1) / kRowsMx;
+    mxfp4_linear_kernel<M, WPL><<<(unsigned)grid, kThreadsMx, 0, st>>>(x, packed, e8m0, n, k, out_bf16, out);
+    return wqh::check_launch();
+}
+
 }  // namespace
+
+extern "C" wq_status mxfp4_linear(const uint16_t* x, int64_t m, const uint8_t* packed,
+                                  const uint8_t* e8m0, int64_t n, int64_t k, int out_dtype,
+                                  void* out, void* stream) {
+    if (m < 0 || n < 0 || k < 0 || k % 32 != 0) return WQ_ERR_BAD_SHAPE;
+    if (m > kMaxM) return WQ_ERR_UNSUPPORTED;
+    if (out_dtype != WQ_DTYPE_F32 && out_dtype != WQ_DTYPE_BF16) return WQ_ERR_BAD_DTYPE;
+    if ((n + kRowsMx - 1) / kRowsMx >= ((int64_t)1 << 31)) return WQ_ERR_BAD_SHAPE;
+    if (m == 0 || n == 0) return WQ_OK;
+    if (!out) return WQ_ERR_NULL_PTR;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (k == 0)  // an empty sum: y = 0
+        return wqh::cuda_status(cudaMemsetAsync(out, 0, (size_t)(m * n) * (out_dtype == WQ_DTYPE_BF16 ? 2 : 4), st));
+    if (!x || !packed || !e8m0) return WQ_ERR_NULL_PTR;
+    if (!wqh::aligned16(x) || !wqh::aligned16(packed) || !wqh::aligned_to(out, 4)) return WQ_ERR_MISALIGNED;
+    const int ob = out_dtype == WQ_DTYPE_BF16;
+    switch (m) {
+        case 1: return launch_mx_linear<1>(x, packed, e8m0, n, k, ob, out, st);
+        case 2: return launch_mx_linear<2>(x, packed, e8m0, n, k, ob, out, st);
+        case 3: return launch_mx_linear<3>(x, packed, e8m0, n, k, ob, out, st);
+        case 4: return launch_mx_linear<4>(x, packed, e8m0, n, k, ob, out, st);
+        case 5: return launch_mx_linear<5>(x, packed, e8m0, n, k, ob, out, st);
+        case 6: return launch_mx_linear<6>(x, packed, e8m0, n, k, ob, out, st);
+        case 7: return launch_mx_linear<7>(x, packed, e8m0, n, k, ob, out, st);
+        default: return launch_mx_linear<8>(x, packed, e8m0, n, k, ob, out, st);
+    }
+}
 
 extern "C" size_t gptq_linear_workspace_bytes(int64_t m, int64_t n) {
     if (m < 1 || m > kMaxM || n < 0) return 0;
