@@ -230,8 +230,8 @@ wq_status awq_search_static_scratch(const uint16_t* w, int64_t n, int64_t k, con
  *      workspace >= gptq_linear_workspace_bytes(m, n), 256-byte aligned,
  *               ZEROED ONCE before its first use (cudaMemset); every completed
  *               call leaves its arrival counters at zero again, so no reset is
- *               needed between calls.  Calls that overlap on the GPU need
- *               separate workspaces.
+ *               needed between calls (zero it again after a call that failed).
+ *               Calls that overlap on the GPU need separate workspaces.
  * Math: deq = (code - zp) * fp16 scale (exact in binary32); per group the
  * products x * (code - zp) (exact) are summed in binary32 and the group sum is
  * multiplied by the scale and added in binary32; K-slices are added in a fixed
