@@ -589,9 +589,9 @@ def run_e2e(args, wl, dev, dist, world):
         for e in joins:
             main.wait_event(e)
 
-    # issued eagerly: the copies dominate, so the host's launches hide behind
-    # them, and stream copies overlap the two directions of the link better than
-    # the same copies as memcpy nodes of a captured graph (3.5 vs 3.8 ms a step)
+    # issued eagerly through the public calls: the copies dominate (the host's
+    # launches hide behind them); capturing the same step as a graph measured no
+    # faster (3.5-3.9 ms a step either way on this link)
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
