@@ -1,0 +1,117 @@
+"""Host side of checkpoint export (no GPU): the safetensors writer checked against
+the file layout parsed independently here, the fused q_k_v split, and the
+quantization_config schemas the serving side reads (export_gptq_cpu.py main();
+quantize_dflash_mxfp4.py main())."""
+import json
+import struct
+
+import numpy as np
+import pytest
+import torch
+
+wq = pytest.importorskip("weight_only_bit_group_gb300")
+from weight_only_bit_group_gb300 import export, synth  # noqa: E402
+
+
+def tensors():
+    g = torch.Generator().manual_seed(3)
+    return {
+        "b.bf16": torch.randn(3, 5, generator=g).to(torch.bfloat16),
+        "a.f16": torch.randn(7, generator=g).to(torch.float16),
+        "c.i32": torch.randint(-2**31, 2**31 - 1, (4, 2), generator=g, dtype=torch.int64).to(torch.int32),
+        "d.u8": torch.randint(0, 256, (9,), generator=g, dtype=torch.int64).to(torch.uint8),
+        "e.f32": torch.randn(2, 2, 2, generator=g),
+        "f.empty": torch.empty(0, 4, dtype=torch.bfloat16),
+        "g.scalar": torch.tensor(2.5, dtype=torch.float64),
+    }
+
+
+def test_safetensors_layout(tmp_path):
+    t = tensors()
+    p = str(tmp_path / "m.safetensors")
+    export.save_safetensors(p, t, metadata={"format": "pt"})
+    raw = open(p, "rb").read()
+    hl = int.from_bytes(raw[:8], "little")
+    assert hl % 8 == 0 and 8 + hl <= len(raw)
+    header = json.loads(raw[8:8 + hl].decode().rstrip(" "))
+    assert header.pop("__metadata__") == {"format": "pt"}
+    names = {"BF16": 2, "F16": 2, "I32": 4, "U8": 1, "F32": 4, "F64": 8}
+    spans = []
+    for name, e in header.items():
+        ref = t[name]
+        assert e["shape"] == list(ref.shape)
+        b, en = e["data_offsets"]
+        assert en - b == ref.numel() * names[e["dtype"]]
+        blob = raw[8 + hl + b:8 + hl + en]
+        # little-endian element bytes, row-major
+        if e["dtype"] in ("BF16", "F16"):
+            want = ref.contiguous().view(torch.int16).numpy().astype("<i2").tobytes()
+        else:
+            want = ref.numpy().astype(ref.numpy().dtype.newbyteorder("<")).tobytes()
+        assert blob == want, name
+        spans.append((b, en))
+    spans.sort()
+    assert spans[0][0] == 0 and all(x[1] == y[0] for x, y in zip(spans, spans[1:]))
+    assert 8 + hl + spans[-1][1] == len(raw)
+
+
+def test_safetensors_round_trip(tmp_path):
+    t = tensors()
+    p = str(tmp_path / "m.safetensors")
+    export.save_safetensors(p, t)
+    back, meta = export.load_safetensors(p)
+    assert meta == {} and set(back) == set(t)
+    for n in t:
+        assert back[n].dtype == t[n].dtype and back[n].shape == t[n].shape
+        assert torch.equal(back[n], t[n]), n
+
+
+def test_split_fused_qkv():
+    state, cfg = synth.tiny_decoder_state(n_layers=1)
+    hd = cfg["head_dim"]
+    qd, kvd = cfg["num_attention_heads"] * hd, cfg["num_key_value_heads"] * hd
+    fused = state["model.layers.0.self_attn.q_k_v_proj.weight"]
+    s = export.split_fused_qkv(state, qd, kvd)
+    assert "model.layers.0.self_attn.q_k_v_proj.weight" not in s
+    assert "model.layers.0.self_attn.q_k_v_proj.weight" in state  # caller's dict untouched
+    for part, lo, hi in (("q_proj", 0, qd), ("k_proj", qd, qd + kvd), ("v_proj", qd + kvd, qd + 2 * kvd)):
+        assert torch.equal(s[f"model.layers.0.self_attn.{part}.weight"], fused[lo:hi])
+    assert hi == fused.shape[0]
+    rest = {n for n in state if "q_k_v_proj" not in n}
+    assert all(s[n] is state[n] for n in rest)
+    # every quantized projection is one the page names; norms and the table pass through
+    targets = [n for n in s if n.endswith(export.GPTQ_TARGET_SUFFIXES)]
+    assert len(targets) == 7
+
+
+def test_gptq_config_schema():
+    c = export.gptq_quantization_config(64, True, True)
+    assert c == {"quant_method": "gptq", "bits": 4, "group_size": 64, "desc_act": False, "sym": False,
+                 "true_sequential": True, "checkpoint_format": "gptq", "lm_head": True}
+    assert export.gptq_quantization_config(128, False, False)["sym"] is True
+
+
+def test_quark_config_schema():
+    c = export.quark_mxfp4_quantization_config()
+    assert c["quant_method"] == "quark" and c["export"]["weight_format"] == "real_quantized"
+    w, x = c["global_quant_config"]["weight"], c["global_quant_config"]["input_tensors"]
+    for spec in (w, x):
+        assert (spec["dtype"], spec["group_size"], spec["scale_format"], spec["round_method"],
+                spec["qscheme"]) == ("fp4", 32, "e8m0", "half_even", "per_group")
+    assert w["is_dynamic"] is False and x["is_dynamic"] is True
+    json.dumps(c)  # serialisable as written
+
+
+def test_mxfp4_targets():
+    t = export.mxfp4_targets(2)
+    assert len(t) == 15 and t[-1] == "fc.weight"
+    st, act, cfg = synth.tiny_drafter_state(n_layers=2)
+    assert set(t) <= set(st)
+    assert len(act) == 6
+
+
+def test_cli_requires_arguments():
+    with pytest.raises(SystemExit):
+        export.main(["gptq"])
+    with pytest.raises(SystemExit):
+        export.main([])

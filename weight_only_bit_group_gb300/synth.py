@@ -114,3 +114,75 @@ def uintx_layers(n_layers: int = 8, seed: int = 5, device="cpu", shapes=LAYER_SH
             out.append((f"layers.{layer}.{name}",
                         normal_bf16((n, k), 0.02, seed + 100 * layer + i, device)))
     return out
+
+
+def tiny_decoder_state(seed: int = 7, n_layers: int = 2, hidden: int = 256, heads: int = 4,
+                       kv_heads: int = 2, head_dim: int = 64, inter: int = 512, vocab: int = 1024):
+    """A small decoder's bf16 state dict under the GPTQ exporter's tensor names,
+    with the fused q_k_v projection [(heads + 2 kv_heads) * head_dim, hidden],
+    plus the config fields the exporter reads.  -> (state, config)."""
+    st, i = {}, 0
+
+    def w(shape, std=0.02):
+        nonlocal i
+        i += 1
+        if len(shape) == 2:
+            return outlier_columns_bf16(shape[0], shape[1], std, 0.005, 20.0, seed * 100 + i)
+        return (1.0 + normal_f32(shape, 0.1, seed * 100 + i)).to(torch.bfloat16)
+
+    qkv = (heads + 2 * kv_heads) * head_dim
+    st["model.embedding.weight"] = w((vocab, hidden))
+    st["model.norm.weight"] = w((hidden,))
+    for l in range(n_layers):
+        P = f"model.layers.{l}"
+        st[f"{P}.input_layernorm.weight"] = w((hidden,))
+        st[f"{P}.post_attention_layernorm.weight"] = w((hidden,))
+        st[f"{P}.self_attn.q_k_v_proj.weight"] = w((qkv, hidden))
+        st[f"{P}.self_attn.out_proj.weight"] = w((hidden, heads * head_dim))
+        st[f"{P}.mlp.gate_proj.weight"] = w((inter, hidden))
+        st[f"{P}.mlp.up_proj.weight"] = w((inter, hidden))
+        st[f"{P}.mlp.down_proj.weight"] = w((hidden, inter))
+    cfg = {"hidden_size": hidden, "num_attention_heads": heads, "num_key_value_heads": kv_heads,
+           "head_dim": head_dim, "intermediate_size": inter, "num_hidden_layers": n_layers,
+           "vocab_size": vocab, "tie_word_embeddings": True}
+    return st, cfg
+
+
+def tiny_drafter_state(seed: int = 9, n_layers: int = 2, hidden: int = 256, q_dim: int = 256,
+                       kv_dim: int = 64, inter: int = 512, taps: int = 8, target_hidden: int = 512):
+    """A small drafter's bf16 state dict under the MXFP4 exporter's tensor names
+    (separate q/k/v, dynamic-conv kernel projections, fc over the target's
+    hidden states) and its per-channel activation statistics mean |x| ~
+    LogNormal(0, 1).  -> (state, act, config)."""
+    st, act, i = {}, {}, 0
+
+    def w(shape, std=0.02):
+        nonlocal i
+        i += 1
+        if len(shape) == 2:
+            return outlier_columns_bf16(shape[0], shape[1], std, 0.005, 20.0, seed * 100 + i)
+        return (1.0 + normal_f32(shape, 0.1, seed * 100 + i)).to(torch.bfloat16)
+
+    def a(k):
+        nonlocal i
+        i += 1
+        return normal_f32((k,), 1.0, seed * 100 + i).exp_()
+
+    st["fc.weight"] = w((hidden, target_hidden))
+    for l in range(n_layers):
+        P = f"layers.{l}"
+        st[f"{P}.input_layernorm.weight"] = w((hidden,))
+        st[f"{P}.post_attention_layernorm.weight"] = w((hidden,))
+        st[f"{P}.attention_conv.kernel_projection.weight"] = w((taps, hidden))
+        st[f"{P}.mlp_conv.kernel_projection.weight"] = w((taps, hidden))
+        st[f"{P}.self_attn.q_proj.weight"] = w((q_dim, hidden))
+        st[f"{P}.self_attn.k_proj.weight"] = w((kv_dim, hidden))
+        st[f"{P}.self_attn.v_proj.weight"] = w((kv_dim, hidden))
+        st[f"{P}.self_attn.o_proj.weight"] = w((hidden, q_dim))
+        st[f"{P}.mlp.gate_proj.weight"] = w((inter, hidden))
+        st[f"{P}.mlp.up_proj.weight"] = w((inter, hidden))
+        st[f"{P}.mlp.down_proj.weight"] = w((hidden, inter))
+        act[f"{P}.self_attn.qkv_proj"] = a(hidden)
+        act[f"{P}.mlp.gate_up_proj"] = a(hidden)
+        act[f"{P}.mlp.down_proj"] = a(inter)
+    return st, act, {"num_hidden_layers": n_layers, "hidden_size": hidden}
