@@ -72,6 +72,16 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def bf16_peak():
+    """Dense bf16 tensor throughput (TFLOP/s) for a kernel timed alone: the measured
+    burst figure, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            return float(json.load(fh)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     def __init__(self, index: int):
@@ -762,6 +772,16 @@ def run_single(args):
         call = lambda: wq.gptq_linear(xv, r["qweight"], r["qzeros"], r["scales"], n, k, GROUP_GPTQ,
                                       False, out=y, ws=lws)
         alg = n * k * 0.5 + (n * k // GROUP_GPTQ) * 2.5 + 2 * k + 4 * n
+    elif name == "gptq_gemm":
+        # prefill batch of args.m tokens on the tensor cores; reported against the
+        # measured dense bf16 peak (the contraction bound), not HBM
+        r = wq.gptq_quantize_asym(w, GROUP_GPTQ, False)
+        xv = torch.randn(args.m, k, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16).to(dev)
+        y = torch.empty(args.m, n, dtype=torch.float32, device=dev)
+        call = lambda: wq.gptq_gemm(xv, r["qweight"], r["qzeros"], r["scales"], n, k, GROUP_GPTQ, False,
+                                    out=y)
+        alg = n * k * 0.5 + (n * k // GROUP_GPTQ) * 2.5 + 2 * args.m * k + 4 * args.m * n
+        flops = 2.0 * args.m * n * k
     elif name == "mxfp4_linear":
         p, e = wq.mxfp4_quantize(w)
         xv = torch.randn(1, k, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16).to(dev)
@@ -800,8 +820,13 @@ def run_single(args):
             times.append(a_.elapsed_time(b_))
     t = statistics.mean(times)
     peak, kind = peaks()
-    print(json.dumps({"kernel": name, "shape": [n, k], "ms": round(t, 4),
-                      "alg_GBps": round(alg / t / 1e6, 1), "frac_of_" + kind: round(alg / t / 1e6 / peak, 4)}))
+    line = {"kernel": name, "shape": [n, k], "ms": round(t, 4),
+            "alg_GBps": round(alg / t / 1e6, 1), "frac_of_" + kind: round(alg / t / 1e6 / peak, 4)}
+    if name == "gptq_gemm":
+        tf_peak, tf_kind = bf16_peak()
+        line.update({"m": args.m, "tflops": round(flops / t / 1e9, 1),
+                     "tflops_frac_of_" + tf_kind: round(flops / t / 1e9 / tf_peak, 4)})
+    print(json.dumps(line))
 
 
 def main():
@@ -811,6 +836,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--kernel", default=None, help="time one kernel alone (see run_single)")
     ap.add_argument("--shape", default="16384x8192")
+    ap.add_argument("--m", type=int, default=512, help="tokens for --kernel gptq_gemm")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="issue every call eagerly instead of a CUDA graph")

@@ -243,6 +243,28 @@ wq_status gptq_linear(const uint16_t* x, int64_t m, const int32_t* qweight, cons
                       int out_dtype, void* out, void* workspace, size_t workspace_bytes,
                       void* stream);
 
+/* gptq_gemm (export_gptq_cpu.py module docstring: the W4A16 uint4b8 layer that
+ * serves the checkpoint, here for prefill batches) -- y = x deq(W)^T on the
+ * tensor cores (tcgen05), any m >= 1, without materialising deq.
+ * In:  x        bf16 [m, k], 16-byte aligned, m < 65535 * 128.
+ *      qweight  i32 [k/8, n], 16-byte aligned; qzeros i32 [k/group, n/8] (may be
+ *               NULL for sym); scales fp16 [k/group, n]; all as produced by
+ *               gptq_quantize_*; group 32, 64, 128 or 256; n % 8 == 0.
+ * Out: out      [m, n], binary32 (WQ_DTYPE_F32) or bf16 (WQ_DTYPE_BF16: the
+ *               binary32 result rounded to nearest even); no workspace.
+ * Math: the tensor cores multiply x by the integers (code - zp), exact in bf16,
+ * so each product is exact; each group's products are summed in binary32 by
+ * the MMA, and the group sums are folded in group order as y = fma(P_g,
+ * scale_g, y).  The MMA's internal additions are not documented as
+ * round-to-nearest, so the bound allows one binary32 ulp for each of them:
+ * |y - exact| <= (k + 2) * 2^-23 * sum_k |x * deq|; the result is the same from
+ * run to run.  k == 0 writes zeros.
+ * Device errors: a device-side wait that runs out records WQ_ERR_DEVICE_TIMEOUT
+ * for wq_device_status; out is then unspecified. */
+wq_status gptq_gemm(const uint16_t* x, int64_t m, const int32_t* qweight, const int32_t* qzeros,
+                    const uint16_t* scales, int64_t n, int64_t k, int group, int sym, int out_dtype,
+                    void* out, void* stream);
+
 /* mxfp4_linear (quantize_dflash_mxfp4.py: the drafter's linears are served in
  * MXFP4; deq as dequantize_mxfp4) -- the consumer for decode batches:
  * y = x deq(W)^T without materialising deq.  No workspace.

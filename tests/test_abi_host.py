@@ -109,6 +109,19 @@ def test_gptq_linear_argument_errors(L):
     assert L.gptq_linear(None, 0, None, None, None, 64, 128, 128, 1, 0, None, None, 0, None) == 0
 
 
+def test_gptq_gemm_argument_errors(L):
+    assert L.gptq_gemm(BAD, 16, BAD, BAD, BAD, 64, 128, 96, 1, 0, BAD, None) == 5      # group
+    assert L.gptq_gemm(BAD, 16, BAD, BAD, BAD, 64, 100, 128, 1, 0, BAD, None) == 2     # k % group
+    assert L.gptq_gemm(BAD, 16, BAD, BAD, BAD, 60, 128, 128, 1, 0, BAD, None) == 2     # n % 8
+    assert L.gptq_gemm(BAD, -1, BAD, BAD, BAD, 64, 128, 128, 1, 0, BAD, None) == 2
+    assert L.gptq_gemm(BAD, 16, BAD, BAD, BAD, 64, 128, 128, 1, 7, BAD, None) == 3
+    assert L.gptq_gemm(BAD, 16, BAD, None, BAD, 64, 128, 128, 0, 0, BAD, None) == 1    # asym needs qzeros
+    assert L.gptq_gemm(BAD, 16, BAD, BAD, BAD, 64, 128, 128, 1, 0, None, None) == 1
+    assert L.gptq_gemm(MIS, 16, BAD, BAD, BAD, 64, 128, 128, 1, 0, BAD, None) == 4
+    assert L.gptq_gemm(BAD, 16, MIS, BAD, BAD, 64, 128, 128, 1, 0, BAD, None) == 4
+    assert L.gptq_gemm(None, 0, None, None, None, 64, 128, 128, 1, 0, None, None) == 0
+
+
 def test_mxfp4_linear_argument_errors(L):
     assert L.mxfp4_linear(BAD, 1, BAD, BAD, 64, 48, 0, BAD, None) == 2     # k % 32 != 0
     assert L.mxfp4_linear(BAD, 9, BAD, BAD, 64, 64, 0, BAD, None) == 5     # m > 8

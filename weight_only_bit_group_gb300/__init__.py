@@ -92,6 +92,7 @@ def lib():
                 "gptq_linear_workspace_bytes": (SZ, [I64, I64]),
                 "gptq_linear": (I, [P, I64, P, P, P, I64, I64, I, I, I, P, P, SZ, P]),
                 "mxfp4_linear": (I, [P, I64, P, P, I64, I64, I, P, P]),
+                "gptq_gemm": (I, [P, I64, P, P, P, I64, I64, I, I, I, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -272,6 +273,21 @@ def gptq_linear(x, qweight, qzeros, scales, n, k, group=128, sym=True, out_dtype
     _check(lib().gptq_linear(_ptr(x2), m, _ptr(qweight), _ptr(qzeros), _ptr(scales), n, k, group,
                              int(sym), dt, _ptr(out), _ptr(ws), ws.numel(), _stream(x.device)),
            "gptq_linear")
+    return out
+
+
+def gptq_gemm(x, qweight, qzeros, scales, n, k, group=128, sym=True, out_dtype=torch.float32,
+              *, out=None):
+    """y = x deq(W)^T on the tensor cores for prefill batches (x bf16 [m, k], any
+    m >= 1) straight from the GPTQ tensors; y binary32 or bf16 [m, n]."""
+    _u16(x)
+    x2 = x.view(1, -1) if x.dim() == 1 else x
+    m = x2.shape[0]
+    dt = WQ_DTYPE_BF16 if out_dtype == torch.bfloat16 else WQ_DTYPE_F32
+    if out is None:
+        out = torch.empty((m, n), dtype=out_dtype, device=x.device)
+    _check(lib().gptq_gemm(_ptr(x2), m, _ptr(qweight), _ptr(qzeros), _ptr(scales), n, k, group,
+                           int(sym), dt, _ptr(out), _stream(x.device)), "gptq_gemm")
     return out
 
 

@@ -1,0 +1,517 @@
+// GPTQ W4A16 GEMM for prefill batches on the fifth-generation tensor cores:
+// y[t, n] = sum_k x[t, k] * deq(W)[n, k], with deq the export_gptq_cpu.py rule
+// (module docstring: w = (code - zp) * scale, zp = 8 for the symmetric uint4b8
+// checkpoints, the stored zero point for asym; scale the fp16 group scale).
+//
+// The product is split at the group boundary so that the tensor cores only ever
+// see exact operands: (code - zp) is an integer in [-15, 15], exact in bf16, and
+// x is bf16, so every product x * (code - zp) is exact and the MMA accumulates
+// them in binary32.  Each group's partial sum P_g lands in its own TMEM
+// accumulator; the epilogue folds y += P_g * scale_g with one binary32 FMA per
+// group, in group order.  No bf16-rounded weight is ever formed.
+//
+// One CTA computes 128 output features x 128 tokens over all of K:
+//   warps 0-7   dequant: raw qweight rows (TMA) -> (code - zp) bf16 written into
+//               the 128-byte-swizzled K-major A tile (two threads per feature row)
+//   warps 8-15  epilogue: two warpgroups (token columns 0-63 / 64-127), one
+//               feature row per thread, tcgen05.ld of each group's partial
+//   warp 16     TMA: x tile [128 tokens x 64] (128-byte swizzle) and qweight
+//               rows [8 x 128 features]; owns the TMEM allocation
+//   warp 17     MMA: one thread issues tcgen05.mma (M 128, N 128, K 16) per
+//               16 values of K, commits to the stage and group barriers
+// Every wait is bounded; on a timeout the CTA records WQ_ERR_DEVICE_TIMEOUT in
+// the device status word, lets its copies and MMAs land, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "wq_common.cuh"
+
+namespace {
+
+constexpr int BM = 128;                    // output features per CTA (MMA M)
+constexpr int BT = 128;                    // tokens per CTA (MMA N)
+constexpr int BK = 64;                     // K per pipeline stage
+constexpr int NS = 4;                      // pipeline stages
+constexpr int X_BYTES = BT * BK * 2;       // x tile, bf16, 128-byte swizzle
+constexpr int A_BYTES = BM * BK * 2;       // (code - zp) tile, bf16, same layout
+constexpr int Q_BYTES = (BK / 8) * BM * 4; // raw qweight rows
+constexpr int STAGE = X_BYTES + A_BYTES + Q_BYTES;
+constexpr int BAR_OFF = NS * STAGE;
+// barriers: full[NS] aready[NS] empty[NS] tfull[2] tempty[2] done; then the TMEM
+// address slot and the abort flag
+constexpr int N_BARS = 3 * NS + 5;
+constexpr int SLOT_OFF = BAR_OFF + 8 * N_BARS;
+constexpr int SMEM = SLOT_OFF + 16 + 1024;  // + slack to align the tiles to 1024 bytes
+constexpr int DQ_WARPS = 8;                // dequant warps: two per feature row
+constexpr int EPI_WARP0 = DQ_WARPS;        // first of the 8 epilogue warps
+constexpr int TMA_WARP = EPI_WARP0 + 8;
+constexpr int MMA_WARP = TMA_WARP + 1;
+constexpr int THREADS = (MMA_WARP + 1) * 32;
+constexpr int TMEM_COLS = 2 * BT;          // two group accumulators
+constexpr uint32_t kSpin = 1u << 22;
+static_assert(STAGE % 1024 == 0 && X_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms");
+
+__device__ unsigned g_gemm_status;
+
+// ------------------------------------------------------------------ tcgen05
+__device__ __forceinline__ void tc_alloc(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 operands, binary32 accumulator.
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the mbarrier when every tcgen05 operation issued so far by this
+// thread has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+// 16 consecutive binary32 columns of this warp's 32 TMEM lanes, waited for.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Shared-memory matrix descriptor of a K-major tile stored as 8-row x 128-byte
+// swizzle atoms (the TMA 128-byte swizzle): start address, stride 1024 bytes
+// between 8-row groups, descriptor version 1, swizzle mode 128B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor: binary32 D, bf16 A and B, both K-major, N = BT, M = BM.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BT >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait; false (and the abort flag set) if the phase never completes.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    for (uint32_t i = 0; i < kSpin; ++i) {
+        if (wq::mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && *abort_flag) return false;
+    }
+    *abort_flag = 1;
+    atomicCAS(&g_gemm_status, 0u, (unsigned)WQ_ERR_DEVICE_TIMEOUT);
+    return false;
+}
+// A warp's wait: lane 0 alone polls (hundreds of polling lanes would take the
+// shared-memory pipe from the tensor cores' operand reads and from the MMA
+// thread's own waits), the warp then shares one outcome, so that the
+// warp-collective instructions after it are reached by all lanes or none, and
+// the warp barrier orders the other lanes' reads after lane 0's acquire.
+// Polling with a short sleep between polls, for the warps that are not on the
+// tensor cores' critical path (so the MMA thread's own barrier checks do not
+// queue behind theirs).  Bounded like wait_bar.
+__device__ __forceinline__ bool wait_bar_backoff(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    for (uint32_t i = 0; i < kSpin; ++i) {
+        if (wq::mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u && *abort_flag) return false;
+        __nanosleep(64);
+    }
+    *abort_flag = 1;
+    atomicCAS(&g_gemm_status, 0u, (unsigned)WQ_ERR_DEVICE_TIMEOUT);
+    return false;
+}
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = wait_bar_backoff(bar, parity, abort_flag);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+// Drain wait for work already issued (copies, MMAs): bounded, but it does not
+// give up when another role aborted, because the hardware is still writing.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kSpin; ++i)
+        if (wq::mbar_try_wait(bar, parity)) return;
+    atomicCAS(&g_gemm_status, 0u, (unsigned)WQ_ERR_DEVICE_TIMEOUT);
+}
+
+template <bool SYM, bool BF16OUT, int G>
+__global__ void __launch_bounds__(THREADS, 1)
+gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap qmap,
+                 const int32_t* __restrict__ qzeros, const uint16_t* __restrict__ scales, int m, int n,
+                 int k, void* __restrict__ out) {
+    constexpr int KPG = G / 16;  // MMA K-steps per group (a power of two)
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+    uint8_t* smem = smem_raw + pad;
+    const uint32_t sbase = raw + pad;
+    auto x_at = [&](int s) { return sbase + s * STAGE; };
+    auto a_at = [&](int s) { return sbase + s * STAGE + X_BYTES; };
+    auto q_at = [&](int s) { return smem + s * STAGE + X_BYTES + A_BYTES; };
+    const uint32_t bar0 = sbase + BAR_OFF;
+    auto full = [&](int s) { return bar0 + 8 * s; };
+    auto aready = [&](int s) { return bar0 + 8 * (NS + s); };
+    auto empty = [&](int s) { return bar0 + 8 * (2 * NS + s); };
+    auto tfull = [&](int b) { return bar0 + 8 * (3 * NS + b); };
+    auto tempty = [&](int b) { return bar0 + 8 * (3 * NS + 2 + b); };
+    const uint32_t done = bar0 + 8 * (3 * NS + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SLOT_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SLOT_OFF + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * BM, t0 = blockIdx.y * BT;
+    const int nkb = (k + BK - 1) / BK;
+    const int ngroups = k / G;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            wq::mbar_init(full(s), 1);
+            wq::mbar_init(aready(s), DQ_WARPS);
+            wq::mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            wq::mbar_init(tfull(b), 1);
+            wq::mbar_init(tempty(b), 8);
+        }
+        wq::mbar_init(done, 1);
+        *abort_flag = 0;
+        wq::mbar_fence_init();
+    }
+    if (warp == TMA_WARP) tc_alloc(sbase + SLOT_OFF, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == TMA_WARP) {
+        // ---------------------------------------------------------- TMA
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % NS;
+                const uint32_t u = (uint32_t)(kb / NS);
+                if (!wait_bar(empty(s), (u & 1u) ^ 1u, abort_flag)) break;
+                wq::mbar_expect_tx(full(s), X_BYTES + Q_BYTES);
+                wq::tma_load_2d(x_at(s), &xmap, kb * BK, t0, full(s));
+                wq::tma_load_2d((uint32_t)__cvta_generic_to_shared(q_at(s)), &qmap, n0, kb * (BK / 8),
+                                full(s));
+                ++issued;
+            }
+            // copies still in flight must land before the shared memory is released
+            for (int kb = issued - NS < 0 ? 0 : issued - NS; kb < issued; ++kb)
+                drain_wait(full(kb % NS), (uint32_t)(kb / NS) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        // ---------------------------------------------------------- MMA
+        // One thread issues every MMA, so its instruction stream between two
+        // issues is on the tensor cores' critical path: group boundaries are
+        // compile-time masks of the K-step index and the descriptors advance by
+        // constant offsets (no division, no recomputation).
+        if (lane == 0) {
+            const uint64_t da0 = sw128_desc(a_at(0)), db0 = sw128_desc(x_at(0));
+            // issue MMAs for K steps [ks0, ks1) of stage descriptors (da, db) into
+            // accumulator b; the first one starts the accumulator when `fresh`
+            auto mmas = [&](uint64_t da, uint64_t db, uint32_t b, int ks0, int ks1, bool fresh) {
+#pragma unroll
+                for (int ks = ks0; ks < ks1; ++ks)
+                    tc_mma(tmem + b * BT, da + (uint64_t)(ks * 2), db + (uint64_t)(ks * 2), kIdesc,
+                           (fresh && ks == ks0) ? 0u : 1u);
+            };
+            bool ok = true;
+            for (int kb = 0; kb < nkb && ok; ++kb) {
+                const int s = kb % NS;
+                const uint32_t par = (uint32_t)(kb / NS) & 1u;
+                if (!wait_bar(full(s), par, abort_flag) || !wait_bar(aready(s), par, abort_flag)) break;
+                tc_fence_after();
+                const uint64_t da = da0 + (uint64_t)((s * STAGE) >> 4), db = db0 + (uint64_t)((s * STAGE) >> 4);
+                if constexpr (G >= BK) {
+                    // a group spans G / 64 whole K blocks
+                    constexpr int BPG = G / BK;
+                    const int g = kb / BPG;
+                    const uint32_t b = (uint32_t)g & 1u;
+                    const bool gstart = (kb & (BPG - 1)) == 0;
+                    if (gstart) {
+                        if (!wait_bar(tempty(b), ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag)) break;
+                        tc_fence_after();
+                    }
+                    mmas(da, db, b, 0, BK / 16, gstart);
+                    if ((kb & (BPG - 1)) == BPG - 1) tc_commit(tfull(b));
+                } else {
+                    // G == 32: groups 2kb (accumulator 0, K steps 0-1) and 2kb+1
+                    // (accumulator 1, K steps 2-3; absent in a half-full last block)
+                    const int halves = (k - kb * BK) >= BK ? 2 : 1;
+                    for (int hh = 0; hh < halves && ok; ++hh) {
+                        const int g = 2 * kb + hh;
+                        if (!wait_bar(tempty((uint32_t)hh), ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        mmas(da, db, (uint32_t)hh, 2 * hh, 2 * hh + 2, true);
+                        tc_commit(tfull((uint32_t)hh));
+                    }
+                }
+                tc_commit(empty(s));
+            }
+            // every MMA issued has completed before TMEM can be freed
+            tc_commit(done);
+            drain_wait(done, 0);
+        }
+        __syncwarp();
+    } else if (warp < DQ_WARPS) {
+        // ---------------------------------------------------------- dequant
+        // Two threads per feature row: thread (r, h) converts qweight rows 4h..4h+3
+        // of the stage (32 K values, inside one group for every supported group).
+        const int r = threadIdx.x & (BM - 1), h = threadIdx.x >> 7;
+        const int nrow = n0 + r;
+        const bool rv = nrow < n;
+        // bf16x2 of 128 + zp for this thread's rows of K block kb (loads issued two
+        // blocks ahead of their use)
+        auto zbias = [&](int kb) -> uint32_t {
+            int zp = 8;
+            const int kk = kb * (BK / 8) + 4 * h;
+            if (!SYM && rv && kk * 8 < k)
+                zp = (int)(((uint32_t)__ldg(qzeros + (size_t)(kk * 8 / G) * (n / 8) + nrow / 8) >>
+                            (4 * (nrow & 7))) & 15u);
+            return (uint32_t)(0x4300 + zp) * 0x10001u;
+        };
+        uint32_t zb_cur = zbias(0), zb_next = nkb > 1 ? zbias(1) : 0u;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % NS;
+            const uint32_t zb2 = zb_cur;
+            zb_cur = zb_next;
+            if (kb + 2 < nkb) zb_next = zbias(kb + 2);
+            if (!warp_wait(full(s), (uint32_t)(kb / NS) & 1u, abort_flag)) break;
+            const uint32_t qsrc = (uint32_t)__cvta_generic_to_shared(q_at(s)) + (uint32_t)((4 * h * BM + r) * 4);
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[j]) : "r"(qsrc + j * BM * 4) : "memory");
+            const uint32_t arow = a_at(s) + r * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t t0n = w[j] & 0x0F0F0F0Fu, t1n = (w[j] >> 4) & 0x0F0F0F0Fu;
+                const uint32_t lo = __byte_perm(t0n, t1n, 0x5140);  // codes 0..3 as bytes
+                const uint32_t hi = __byte_perm(t0n, t1n, 0x7362);  // codes 4..7
+                // bytes c | 0x43 << 8 = bf16 of 128 + c; minus 128 + zp is exact
+                const uint32_t d0 = wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4140), zb2);
+                const uint32_t d1 = wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4342), zb2);
+                const uint32_t d2 = wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4140), zb2);
+                const uint32_t d3 = wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4342), zb2);
+                const uint32_t dst = arow + (uint32_t)(((4 * h + j) ^ (r & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(d0), "r"(d1),
+                             "r"(d2), "r"(d3)
+                             : "memory");
+            }
+            // generic-proxy writes become visible to the tensor cores' reads
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(aready(s));
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int quarter = warp & 3, half = (warp - EPI_WARP0) >> 2;
+        const int r = quarter * 32 + lane;
+        const int nrow = n0 + r;
+        const bool rv = nrow < n;
+        float acc[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+        bool ok = true;
+        float sc_next = (rv && ngroups > 0) ? __half2float(__ushort_as_half(scales[nrow])) : 0.f;
+        for (int g = 0; g < ngroups; ++g) {
+            const int b = g & 1;
+            const float sc = sc_next;
+            if (g + 1 < ngroups && rv)
+                sc_next = __half2float(__ushort_as_half(scales[(size_t)(g + 1) * n + nrow]));
+            if (!warp_wait(tfull(b), (uint32_t)(g >> 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t col = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BT + half * 64);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v[16];
+                tc_ld16(col + c * 16, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[c * 16 + i] = __fmaf_rn(v[i], sc, acc[c * 16 + i]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty(b));
+        }
+        if (ok && rv) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const int t = t0 + half * 64 + i;
+                if (t < m) {
+                    if (BF16OUT)
+                        reinterpret_cast<uint16_t*>(out)[(size_t)t * n + nrow] = (uint16_t)wq::f_to_bf(acc[i]);
+                    else
+                        reinterpret_cast<float*>(out)[(size_t)t * n + nrow] = acc[i];
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == TMA_WARP) {
+        tc_fence_after();
+        tc_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+template <bool SYM, bool BF16OUT, int G>
+wq_status launch(const uint16_t* x, int64_t m, const int32_t* qweight, const int32_t* qzeros,
+                 const uint16_t* scales, int64_t n, int64_t k, void* out, cudaStream_t st) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
+    if (!enc) return wqh::cuda_status(cudaErrorNotSupported);
+    CUtensorMap xmap, qmap;
+    {
+        // x [m, k] bf16: boxes of 128 tokens x 64 values, 128-byte swizzle, zeros outside
+        const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)m};
+        const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+        const cuuint32_t box[2] = {BK, BT};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return WQ_ERR_BAD_SHAPE;
+    }
+    {
+        // qweight [k/8, n] int32: boxes of 8 rows x 128 features, unswizzled, zeros outside
+        const cuuint64_t dims[2] = {(cuuint64_t)n, (cuuint64_t)(k / 8)};
+        const cuuint64_t strides[1] = {(cuuint64_t)n * 4};
+        const cuuint32_t box[2] = {BM, BK / 8};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t*>(qweight), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return WQ_ERR_BAD_SHAPE;
+    }
+    const void* fn = (const void*)gptq_gemm_kernel<SYM, BF16OUT, G>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        const wq_status s =
+            wqh::cuda_status(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM));
+        if (s != WQ_OK) return s;
+        attr_set = true;
+    }
+    const dim3 grid((unsigned)((n + BM - 1) / BM), (unsigned)((m + BT - 1) / BT));
+    gptq_gemm_kernel<SYM, BF16OUT, G><<<grid, THREADS, SMEM, st>>>(xmap, qmap, qzeros, scales, (int)m, (int)n,
+                                                                  (int)k, out);
+    return wqh::check_launch();
+}
+
+template <int G>
+wq_status dispatch_rule(bool sym, bool bf, const uint16_t* x, int64_t m, const int32_t* qweight,
+                        const int32_t* qzeros, const uint16_t* scales, int64_t n, int64_t k, void* out,
+                        cudaStream_t st) {
+    if (sym)
+        return bf ? launch<true, true, G>(x, m, qweight, qzeros, scales, n, k, out, st)
+                  : launch<true, false, G>(x, m, qweight, qzeros, scales, n, k, out, st);
+    return bf ? launch<false, true, G>(x, m, qweight, qzeros, scales, n, k, out, st)
+              : launch<false, false, G>(x, m, qweight, qzeros, scales, n, k, out, st);
+}
+
+wq_status dispatch_g(int group, bool sym, bool bf, const uint16_t* x, int64_t m, const int32_t* qweight,
+                     const int32_t* qzeros, const uint16_t* scales, int64_t n, int64_t k, void* out,
+                     cudaStream_t st) {
+    switch (group) {
+        case 32: return dispatch_rule<32>(sym, bf, x, m, qweight, qzeros, scales, n, k, out, st);
+        case 64: return dispatch_rule<64>(sym, bf, x, m, qweight, qzeros, scales, n, k, out, st);
+        case 128: return dispatch_rule<128>(sym, bf, x, m, qweight, qzeros, scales, n, k, out, st);
+        default: return dispatch_rule<256>(sym, bf, x, m, qweight, qzeros, scales, n, k, out, st);
+    }
+}
+
+}  // namespace
+
+namespace wqh {
+// Read and clear this file's device status word (0 when no wait ran out).
+unsigned gemm_status_take() {
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (v != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(zero)) != cudaSuccess) cudaGetLastError();
+    }
+    return v;
+}
+}  // namespace wqh
+
+extern "C" {
+
+wq_status gptq_gemm(const uint16_t* x, int64_t m, const int32_t* qweight, const int32_t* qzeros,
+                    const uint16_t* scales, int64_t n, int64_t k, int group, int sym, int out_dtype,
+                    void* out, void* stream) {
+    if (m < 0 || n < 0 || k < 0) return WQ_ERR_BAD_SHAPE;
+    if (group != 32 && group != 64 && group != 128 && group != 256) return WQ_ERR_UNSUPPORTED;
+    if (k % group != 0 || n % 8 != 0) return WQ_ERR_BAD_SHAPE;
+    if (m >= (1ll << 31) || n >= (1ll << 31) || k >= (1ll << 31) || m > 65535ll * BT)
+        return WQ_ERR_BAD_SHAPE;
+    if (out_dtype != WQ_DTYPE_F32 && out_dtype != WQ_DTYPE_BF16) return WQ_ERR_BAD_DTYPE;
+    if (m == 0 || n == 0) return WQ_OK;
+    if (!out) return WQ_ERR_NULL_PTR;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (k == 0)  // an empty sum: y = 0
+        return wqh::cuda_status(
+            cudaMemsetAsync(out, 0, (size_t)(m * n) * (out_dtype == WQ_DTYPE_BF16 ? 2 : 4), st));
+    if (!x || !qweight || !scales || (!sym && !qzeros)) return WQ_ERR_NULL_PTR;
+    if (!wqh::aligned16(x) || !wqh::aligned16(qweight) || !wqh::aligned_to(scales, 2) ||
+        (!sym && !wqh::aligned_to(qzeros, 4)) || !wqh::aligned_to(out, 4))
+        return WQ_ERR_MISALIGNED;
+    const bool bf = out_dtype == WQ_DTYPE_BF16;
+    return dispatch_g(group, sym != 0, bf, x, m, qweight, qzeros, scales, n, k, out, st);
+}
+
+}  // extern "C"

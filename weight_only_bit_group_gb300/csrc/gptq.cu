@@ -28,6 +28,10 @@
 
 #include "wq_common.cuh"
 
+namespace wqh {
+unsigned gemm_status_take();  // gemm.cu
+}
+
 namespace {
 
 constexpr int kThreads = 256;  // dequant kernels
@@ -638,7 +642,8 @@ extern "C" wq_status wq_device_status(void) {
     unsigned v = 0;
     wq_status s = wqh::cuda_status(cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v)));
     if (s != WQ_OK) return s;
-    if (v == 0) return WQ_OK;
+    const unsigned vg = wqh::gemm_status_take();  // the tensor-core GEMM's own word
+    if (v == 0) return vg ? (wq_status)vg : WQ_OK;
     const unsigned zero = 0;
     s = wqh::cuda_status(cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero)));
     return s != WQ_OK ? s : (wq_status)v;
