@@ -246,7 +246,7 @@ wq_status gptq_linear(const uint16_t* x, int64_t m, const int32_t* qweight, cons
 /* gptq_gemm (export_gptq_cpu.py module docstring: the W4A16 uint4b8 layer that
  * serves the checkpoint, here for prefill batches) -- y = x deq(W)^T on the
  * tensor cores (tcgen05), any m >= 1, without materialising deq.
- * In:  x        bf16 [m, k], 16-byte aligned, m < 65535 * 128.
+ * In:  x        bf16 [m, k], 16-byte aligned.
  *      qweight  i32 [k/8, n], 16-byte aligned; qzeros i32 [k/group, n/8] (may be
  *               NULL for sym); scales fp16 [k/group, n]; all as produced by
  *               gptq_quantize_*; group 32, 64, 128 or 256; n % 8 == 0.

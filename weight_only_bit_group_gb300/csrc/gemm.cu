@@ -34,7 +34,7 @@ namespace {
 constexpr int BM = 128;                    // output features per CTA (MMA M)
 constexpr int BT = 128;                    // tokens per CTA (MMA N)
 constexpr int BK = 64;                     // K per pipeline stage
-constexpr int NS = 4;                      // pipeline stages
+constexpr int NS = 6;                      // pipeline stages
 constexpr int X_BYTES = BT * BK * 2;       // x tile, bf16, 128-byte swizzle
 constexpr int A_BYTES = BM * BK * 2;       // (code - zp) tile, bf16, same layout
 constexpr int Q_BYTES = (BK / 8) * BM * 4; // raw qweight rows
@@ -50,6 +50,7 @@ constexpr int EPI_WARP0 = DQ_WARPS;        // first of the 8 epilogue warps
 constexpr int TMA_WARP = EPI_WARP0 + 8;
 constexpr int MMA_WARP = TMA_WARP + 1;
 constexpr int THREADS = (MMA_WARP + 1) * 32;
+constexpr int kBand = 8;                   // token tiles per rasterisation band
 constexpr int TMEM_COLS = 2 * BT;          // two group accumulators
 constexpr uint32_t kSpin = 1u << 22;
 static_assert(STAGE % 1024 == 0 && X_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms");
@@ -119,47 +120,57 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Bounded wait; false (and the abort flag set) if the phase never completes.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    for (uint32_t i = 0; i < kSpin; ++i) {
-        if (wq::mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && *abort_flag) return false;
-    }
-    *abort_flag = 1;
-    atomicCAS(&g_gemm_status, 0u, (unsigned)WQ_ERR_DEVICE_TIMEOUT);
-    return false;
-}
-// A warp's wait: lane 0 alone polls (hundreds of polling lanes would take the
-// shared-memory pipe from the tensor cores' operand reads and from the MMA
-// thread's own waits), the warp then shares one outcome, so that the
-// warp-collective instructions after it are reached by all lanes or none, and
-// the warp barrier orders the other lanes' reads after lane 0's acquire.
-// Polling with a short sleep between polls, for the warps that are not on the
-// tensor cores' critical path (so the MMA thread's own barrier checks do not
-// queue behind theirs).  Bounded like wait_bar.
-__device__ __forceinline__ bool wait_bar_backoff(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    for (uint32_t i = 0; i < kSpin; ++i) {
-        if (wq::mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u && *abort_flag) return false;
-        __nanosleep(64);
-    }
-    *abort_flag = 1;
-    atomicCAS(&g_gemm_status, 0u, (unsigned)WQ_ERR_DEVICE_TIMEOUT);
-    return false;
-}
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = wait_bar_backoff(bar, parity, abort_flag);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
+// Bounded wait for the phase with parity `parity`: the whole poll loop is one
+// block of PTX (scoped labels), so every lane that executes it polls on its own
+// and no compiler-made convergence barrier surrounds a divergent C++ loop --
+// such barriers cost hundreds of cycles per wait.  mbarrier.try_wait suspends the
+// thread in the barrier unit until the phase completes or a short time limit
+// passes, so a waiting warp takes almost no issue slots.  Returns false after
+// `limit` polls without completion (the caller then aborts).
+constexpr uint32_t kSuspendNs = 100000;  // per poll; the thread wakes when the phase completes
+__device__ __forceinline__ bool poll_bar(uint32_t bar, uint32_t parity, uint32_t limit) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t"
+        ".reg .pred p;\n\t"
+        ".reg .u32 c;\n\t"
+        "mov.u32 c, 0;\n"
+        "WQ_POLL:\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %4;\n\t"
+        "@p bra WQ_DONE;\n\t"
+        "add.u32 c, c, 1;\n\t"
+        "setp.lt.u32 p, c, %3;\n\t"
+        "@p bra WQ_POLL;\n"
+        "WQ_DONE:\n\t"
+        "setp.lt.u32 p, c, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(limit), "r"(kSuspendNs)
+        : "memory");
     return ok != 0;
+}
+// Wait with the abort protocol: polls in slices, gives up early once another
+// role aborted, and records a timeout.  Same outcome on every lane that calls it
+// (callers that need a warp-wide decision combine it with __all_sync).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    for (uint32_t i = 0; i < 512; ++i) {
+        if (poll_bar(bar, parity, 64)) return true;
+        if (*abort_flag) return false;
+    }
+    *abort_flag = 1;
+    atomicCAS(&g_gemm_status, 0u, (unsigned)WQ_ERR_DEVICE_TIMEOUT);
+    return false;
+}
+// A warp's wait: every lane polls (uniform control flow), one warp-wide outcome
+// so that the warp-collective instructions after it run on all lanes or none.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag));
 }
 // Drain wait for work already issued (copies, MMAs): bounded, but it does not
 // give up when another role aborted, because the hardware is still writing.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpin; ++i)
-        if (wq::mbar_try_wait(bar, parity)) return;
-    atomicCAS(&g_gemm_status, 0u, (unsigned)WQ_ERR_DEVICE_TIMEOUT);
+    if (!poll_bar(bar, parity, 16384)) atomicCAS(&g_gemm_status, 0u, (unsigned)WQ_ERR_DEVICE_TIMEOUT);
 }
 
 template <bool SYM, bool BF16OUT, int G>
@@ -187,7 +198,19 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SLOT_OFF + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BM, t0 = blockIdx.y * BT;
+    // Grouped rasterisation of the 1-D grid: consecutive CTAs sweep the feature
+    // tiles of a band of kBand token tiles, so the CTAs resident at one time
+    // spread over several x tiles and several weight tiles instead of all
+    // reading the same x tile (an L2 hot spot).
+    int n0, t0;
+    {
+        const int ntn = (n + BM - 1) / BM, ntt = (m + BT - 1) / BT;
+        const int pid = blockIdx.x, per_band = kBand * ntn;
+        const int band = pid / per_band, first = band * kBand;
+        const int bsz = min(ntt - first, kBand), in = pid - band * per_band;
+        t0 = (first + in % bsz) * BT;
+        n0 = (in / bsz) * BM;
+    }
     const int nkb = (k + BK - 1) / BK;
     const int ngroups = k / G;
 
@@ -290,27 +313,23 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     } else if (warp < DQ_WARPS) {
         // ---------------------------------------------------------- dequant
         // Two threads per feature row: thread (r, h) converts qweight rows 4h..4h+3
-        // of the stage (32 K values, inside one group for every supported group).
+        // of a stage (32 K values, inside one group for every supported group).
+        // Two K blocks per round: one proxy fence and one warp barrier serve both.
         const int r = threadIdx.x & (BM - 1), h = threadIdx.x >> 7;
         const int nrow = n0 + r;
         const bool rv = nrow < n;
-        // bf16x2 of 128 + zp for this thread's rows of K block kb (loads issued two
-        // blocks ahead of their use)
-        auto zbias = [&](int kb) -> uint32_t {
-            int zp = 8;
+        // raw qzeros word of this thread's rows of K block kb (asym); issued one
+        // round before its use and not touched in between, so the load's latency
+        // overlaps a round of work
+        auto zword = [&](int kb) -> uint32_t {
             const int kk = kb * (BK / 8) + 4 * h;
-            if (!SYM && rv && kk * 8 < k)
-                zp = (int)(((uint32_t)__ldg(qzeros + (size_t)(kk * 8 / G) * (n / 8) + nrow / 8) >>
-                            (4 * (nrow & 7))) & 15u);
-            return (uint32_t)(0x4300 + zp) * 0x10001u;
+            if (SYM || !rv || kb >= nkb || kk * 8 >= k) return 0x88888888u;
+            return (uint32_t)__ldg(qzeros + (size_t)(kk * 8 / G) * (n / 8) + nrow / 8);
         };
-        uint32_t zb_cur = zbias(0), zb_next = nkb > 1 ? zbias(1) : 0u;
-        for (int kb = 0; kb < nkb; ++kb) {
+        auto convert = [&](int kb, uint32_t zw) {
             const int s = kb % NS;
-            const uint32_t zb2 = zb_cur;
-            zb_cur = zb_next;
-            if (kb + 2 < nkb) zb_next = zbias(kb + 2);
-            if (!warp_wait(full(s), (uint32_t)(kb / NS) & 1u, abort_flag)) break;
+            const uint32_t zp = (zw >> (4 * (nrow & 7))) & 15u;
+            const uint32_t zb2 = (0x4300u + zp) * 0x10001u;  // bf16x2 of 128 + zp
             const uint32_t qsrc = (uint32_t)__cvta_generic_to_shared(q_at(s)) + (uint32_t)((4 * h * BM + r) * 4);
             uint32_t w[4];
 #pragma unroll
@@ -332,10 +351,24 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                              "r"(d2), "r"(d3)
                              : "memory");
             }
+        };
+        uint32_t za = zword(0), zb = zword(1);
+        for (int kb = 0; kb < nkb; kb += 2) {
+            const bool two = kb + 1 < nkb;
+            if (!warp_wait(full(kb % NS), (uint32_t)(kb / NS) & 1u, abort_flag)) break;
+            if (two && !warp_wait(full((kb + 1) % NS), (uint32_t)((kb + 1) / NS) & 1u, abort_flag)) break;
+            const uint32_t zcur_a = za, zcur_b = zb;
+            za = zword(kb + 2);
+            zb = zword(kb + 3);
+            convert(kb, zcur_a);
+            if (two) convert(kb + 1, zcur_b);
             // generic-proxy writes become visible to the tensor cores' reads
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
-            if (lane == 0) mbar_arrive(aready(s));
+            if (lane == 0) {
+                mbar_arrive(aready(kb % NS));
+                if (two) mbar_arrive(aready((kb + 1) % NS));
+            }
         }
     } else {
         // ---------------------------------------------------------- epilogue
@@ -443,7 +476,7 @@ wq_status launch(const uint16_t* x, int64_t m, const int32_t* qweight, const int
         if (s != WQ_OK) return s;
         attr_set = true;
     }
-    const dim3 grid((unsigned)((n + BM - 1) / BM), (unsigned)((m + BT - 1) / BT));
+    const dim3 grid((unsigned)(((n + BM - 1) / BM) * ((m + BT - 1) / BT)));
     gptq_gemm_kernel<SYM, BF16OUT, G><<<grid, THREADS, SMEM, st>>>(xmap, qmap, qzeros, scales, (int)m, (int)n,
                                                                   (int)k, out);
     return wqh::check_launch();
@@ -497,7 +530,8 @@ wq_status gptq_gemm(const uint16_t* x, int64_t m, const int32_t* qweight, const 
     if (m < 0 || n < 0 || k < 0) return WQ_ERR_BAD_SHAPE;
     if (group != 32 && group != 64 && group != 128 && group != 256) return WQ_ERR_UNSUPPORTED;
     if (k % group != 0 || n % 8 != 0) return WQ_ERR_BAD_SHAPE;
-    if (m >= (1ll << 31) || n >= (1ll << 31) || k >= (1ll << 31) || m > 65535ll * BT)
+    if (m >= (1ll << 31) || n >= (1ll << 31) || k >= (1ll << 31) ||
+        ((n + BM - 1) / BM) * ((m + BT - 1) / BT) >= (1ll << 31))
         return WQ_ERR_BAD_SHAPE;
     if (out_dtype != WQ_DTYPE_F32 && out_dtype != WQ_DTYPE_BF16) return WQ_ERR_BAD_DTYPE;
     if (m == 0 || n == 0) return WQ_OK;
