@@ -91,7 +91,8 @@ const char* wq_last_cuda_error(void);
 const char* wq_version(void);
 
 /* Device-side status of the kernels that wait on hardware events (the GPTQ
- * quantize kernels wait on the mbarriers of their TMA loads).  Every such wait
+ * quantize kernels wait on the mbarriers of their TMA loads; gptq_gemm also on
+ * its dequant, MMA and epilogue hand-offs).  Every such wait
  * is bounded: one that runs out (a load that never lands) makes the kernel skip
  * the rest of its work and record WQ_ERR_DEVICE_TIMEOUT in a per-device status
  * word; the outputs of that call are then incomplete.  This call reads the word
