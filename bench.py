@@ -782,6 +782,14 @@ def run_single(args):
                                     out=y)
         alg = n * k * 0.5 + (n * k // GROUP_GPTQ) * 2.5 + 2 * args.m * k + 4 * args.m * n
         flops = 2.0 * args.m * n * k
+    elif name == "uintx_gemm":
+        # uintx forward (4 bits, group 64) for a batch of args.m tokens on the tensor cores
+        p, sc, z = wq.uintx_quantize(w, NBITS_UINTX)
+        xv = torch.randn(args.m, k, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16).to(dev)
+        y = torch.empty(args.m, n, dtype=torch.float32, device=dev)
+        call = lambda: wq.uintx_gemm(xv, p, sc, z, n, k, NBITS_UINTX, 64, out=y)
+        alg = n * k * (NBITS_UINTX / 8 + 3 / 64) + 2 * args.m * k + 4 * args.m * n
+        flops = 2.0 * args.m * n * k
     elif name == "mxfp4_linear":
         p, e = wq.mxfp4_quantize(w)
         xv = torch.randn(1, k, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16).to(dev)
@@ -822,7 +830,7 @@ def run_single(args):
     peak, kind = peaks()
     line = {"kernel": name, "shape": [n, k], "ms": round(t, 4),
             "alg_GBps": round(alg / t / 1e6, 1), "frac_of_" + kind: round(alg / t / 1e6 / peak, 4)}
-    if name == "gptq_gemm":
+    if name in ("gptq_gemm", "uintx_gemm"):
         tf_peak, tf_kind = bf16_peak()
         line.update({"m": args.m, "tflops": round(flops / t / 1e9, 1),
                      "tflops_frac_of_" + tf_kind: round(flops / t / 1e9 / tf_peak, 4)})
@@ -836,7 +844,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--kernel", default=None, help="time one kernel alone (see run_single)")
     ap.add_argument("--shape", default="16384x8192")
-    ap.add_argument("--m", type=int, default=512, help="tokens for --kernel gptq_gemm")
+    ap.add_argument("--m", type=int, default=512, help="tokens for --kernel gptq_gemm / uintx_gemm")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="issue every call eagerly instead of a CUDA graph")

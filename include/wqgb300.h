@@ -266,6 +266,27 @@ wq_status gptq_gemm(const uint16_t* x, int64_t m, const int32_t* qweight, const 
                     const uint16_t* scales, int64_t n, int64_t k, int group, int sym, int out_dtype,
                     void* out, void* stream);
 
+/* uintx_gemm (uintx_quant.py, UIntXQuantizer.forward: the weight is rebuilt by
+ * _dequantize_native in bf16, then F.linear) -- y = x deq(W)^T on the tensor
+ * cores (tcgen05), any m >= 1, without materialising deq.
+ * In:  x       bf16 [m, k], 16-byte aligned; k % 64 == 0 (WQ_ERR_UNSUPPORTED
+ *              otherwise: the shard reads need 8-element alignment).
+ *      packed, scale (bf16 [n, k/group]), zp (u8 [n, k/group]) as produced by
+ *              uintx_quantize with nbits 2..7 and group 32, 64, 128 or 256;
+ *              packed 16-byte aligned.
+ * Out: out     [m, n], binary32 or bf16 (the binary32 result rounded to nearest
+ *              even); no workspace.
+ * Math: deq = the page's bf16 values ((q - zp) in bf16, times the bf16 scale,
+ * rounded once), exactly as uintx_dequantize writes them; the tensor cores
+ * multiply x by them (exact products) and add all k products in binary32
+ * (addition rounding not documented as round-to-nearest, so the bound allows
+ * one ulp per addition): |y - x deq^T| <= (k + 2) * 2^-23 * sum_k |x * deq|;
+ * the same bits from run to run.  k == 0 writes zeros.  Device errors: as
+ * gptq_gemm. */
+wq_status uintx_gemm(const uint16_t* x, int64_t m, const uint8_t* packed, const uint16_t* scale,
+                     const uint8_t* zp, int64_t n, int64_t k, int nbits, int group, int out_dtype,
+                     void* out, void* stream);
+
 /* mxfp4_linear (quantize_dflash_mxfp4.py: the drafter's linears are served in
  * MXFP4; deq as dequantize_mxfp4) -- the consumer for decode batches:
  * y = x deq(W)^T without materialising deq.  No workspace.

@@ -122,6 +122,18 @@ def test_gptq_gemm_argument_errors(L):
     assert L.gptq_gemm(None, 0, None, None, None, 64, 128, 128, 1, 0, None, None) == 0
 
 
+def test_uintx_gemm_argument_errors(L):
+    assert L.uintx_gemm(BAD, 16, BAD, BAD, BAD, 64, 128, 8, 64, 0, BAD, None) == 5     # nbits 8
+    assert L.uintx_gemm(BAD, 16, BAD, BAD, BAD, 64, 128, 1, 64, 0, BAD, None) == 5     # nbits 1
+    assert L.uintx_gemm(BAD, 16, BAD, BAD, BAD, 64, 128, 4, 48, 0, BAD, None) == 5     # group
+    assert L.uintx_gemm(BAD, 16, BAD, BAD, BAD, 64, 96, 4, 32, 0, BAD, None) == 5      # k % 64
+    assert L.uintx_gemm(BAD, 16, BAD, BAD, BAD, 64, 192, 4, 128, 0, BAD, None) == 2    # k % group
+    assert L.uintx_gemm(BAD, 16, BAD, BAD, BAD, 64, 128, 4, 64, 7, BAD, None) == 3
+    assert L.uintx_gemm(BAD, 16, BAD, None, BAD, 64, 128, 4, 64, 0, BAD, None) == 1
+    assert L.uintx_gemm(BAD, 16, MIS, BAD, BAD, 64, 128, 4, 64, 0, BAD, None) == 4
+    assert L.uintx_gemm(None, 0, None, None, None, 64, 128, 4, 64, 0, None, None) == 0
+
+
 def test_mxfp4_linear_argument_errors(L):
     assert L.mxfp4_linear(BAD, 1, BAD, BAD, 64, 48, 0, BAD, None) == 2     # k % 32 != 0
     assert L.mxfp4_linear(BAD, 9, BAD, BAD, 64, 64, 0, BAD, None) == 5     # m > 8

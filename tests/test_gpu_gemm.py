@@ -101,3 +101,66 @@ def test_gptq_gemm_empty_k_writes_zeros():
     e = torch.empty(0, dtype=torch.int32, device=DEV)
     wq.gptq_gemm(x, e, e, torch.empty(0, dtype=torch.float16, device=DEV), 64, 0, 128, True, out=y)
     assert torch.count_nonzero(y) == 0
+
+
+# ------------------------------------------------------------------ uintx consumer
+def uintx_inputs(n, k, nbits, group, seed):
+    w = synth.normal_bf16((n, k), 0.02, seed)
+    packed, sc, zp, _ = oracle.uintx_quantize(w, nbits, group)  # the oracle's own codes
+    deq = oracle.bf16_bits_to_f32(oracle.uintx_dequantize(packed, sc, zp, n, k, nbits, group))
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(DEV)
+    return t(packed, torch.uint8), t(sc.view(np.int16), torch.bfloat16), t(zp, torch.uint8), deq
+
+
+def check_ux(x, packed, sc, zp, deq, n, k, nbits, group, out_dtype=torch.float32):
+    y = wq.uintx_gemm(x.to(DEV), packed, sc, zp, n, k, nbits, group, out_dtype)
+    xf = oracle.bf16_bits_to_f32(u16x(x)).astype(np.float64)
+    d = deq.astype(np.float64)
+    ref, mag = xf @ d.T, np.abs(xf) @ np.abs(d).T
+    got = y.float().cpu().numpy().astype(np.float64)
+    bound = (k + 2) * U * mag
+    if out_dtype == torch.bfloat16:
+        bound = bound + 2.0 ** -8 * (np.abs(ref) + bound)
+    err = np.abs(got - ref)
+    assert np.all(err <= bound + 1e-30), float((err / (bound + 1e-30)).max())
+    assert wq.device_status() == 0
+    return y
+
+
+def u16x(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("nbits", [2, 3, 4, 5, 6, 7])
+def test_uintx_gemm_bits(nbits):
+    n, k = 264, 1024  # ragged feature tile
+    packed, sc, zp, deq = uintx_inputs(n, k, nbits, 64, 110 + nbits)
+    for m in (1, 40, 128, 200):
+        check_ux(acts(m, k, 111 + m), packed, sc, zp, deq, n, k, nbits, 64)
+    check_ux(acts(33, k, 112), packed, sc, zp, deq, n, k, nbits, 64, torch.bfloat16)
+
+
+@pytest.mark.parametrize("group", [32, 128, 256])
+def test_uintx_gemm_groups(group):
+    n, k = 136, 512
+    for nbits in (3, 7):
+        packed, sc, zp, deq = uintx_inputs(n, k, nbits, group, 113 + group)
+        check_ux(acts(70, k, 114), packed, sc, zp, deq, n, k, nbits, group)
+
+
+@pytest.mark.parametrize("n", [1, 3, 7, 9])
+def test_uintx_gemm_tiny_n_shard_wraps(n):
+    # with n < 8 the shard chunks are shorter than a row: runs wrap inside rows
+    k = 128
+    for nbits in (3, 5, 6, 7):
+        packed, sc, zp, deq = uintx_inputs(n, k, nbits, 64, 115 + n)
+        check_ux(acts(5, k, 116), packed, sc, zp, deq, n, k, nbits, 64)
+
+
+def test_uintx_gemm_layer_shape():
+    n, k, m = 4096, 4096, 256
+    packed, sc, zp, deq = uintx_inputs(n, k, 4, 64, 117)
+    x = acts(m, k, 118)
+    y1 = check_ux(x, packed, sc, zp, deq, n, k, 4, 64)
+    y2 = wq.uintx_gemm(x.to(DEV), packed, sc, zp, n, k, 4, 64)
+    assert torch.equal(y1, y2)

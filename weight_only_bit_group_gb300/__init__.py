@@ -93,6 +93,7 @@ def lib():
                 "gptq_linear": (I, [P, I64, P, P, P, I64, I64, I, I, I, P, P, SZ, P]),
                 "mxfp4_linear": (I, [P, I64, P, P, I64, I64, I, P, P]),
                 "gptq_gemm": (I, [P, I64, P, P, P, I64, I64, I, I, I, P, P]),
+                "uintx_gemm": (I, [P, I64, P, P, P, I64, I64, I, I, I, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -288,6 +289,20 @@ def gptq_gemm(x, qweight, qzeros, scales, n, k, group=128, sym=True, out_dtype=t
         out = torch.empty((m, n), dtype=out_dtype, device=x.device)
     _check(lib().gptq_gemm(_ptr(x2), m, _ptr(qweight), _ptr(qzeros), _ptr(scales), n, k, group,
                            int(sym), dt, _ptr(out), _stream(x.device)), "gptq_gemm")
+    return out
+
+
+def uintx_gemm(x, packed, scale, zp, n, k, nbits, group=64, out_dtype=torch.float32, *, out=None):
+    """uintx_quant.py forward on the tensor cores: y = x deq(W)^T with deq the
+    page's bf16 values (x bf16 [m, k], any m >= 1); y binary32 or bf16 [m, n]."""
+    _u16(x)
+    x2 = x.view(1, -1) if x.dim() == 1 else x
+    m = x2.shape[0]
+    dt = WQ_DTYPE_BF16 if out_dtype == torch.bfloat16 else WQ_DTYPE_F32
+    if out is None:
+        out = torch.empty((m, n), dtype=out_dtype, device=x.device)
+    _check(lib().uintx_gemm(_ptr(x2), m, _ptr(packed), _ptr(scale), _ptr(zp), n, k, nbits, group, dt,
+                            _ptr(out), _stream(x.device)), "uintx_gemm")
     return out
 
 

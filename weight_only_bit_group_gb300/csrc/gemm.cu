@@ -173,11 +173,18 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (!poll_bar(bar, parity, 16384)) atomicCAS(&g_gemm_status, 0u, (unsigned)WQ_ERR_DEVICE_TIMEOUT);
 }
 
-template <bool SYM, bool BF16OUT, int G>
+// UX == 0: GPTQ (qweight rows by TMA, SYM selects the rule, G the group; one
+// accumulator per group, scaled in the epilogue).
+// UX in 2..7: uintx of UX bits (uintx_quant.py): the dequant warps read the bit
+// shards, scale and zero point themselves and write the page's bf16 deq values;
+// one accumulator over all of K (the deq values are the weight, no scaling
+// left); ux_group is the uintx group.
+template <bool SYM, bool BF16OUT, int G, int UX>
 __global__ void __launch_bounds__(THREADS, 1)
 gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap qmap,
                  const int32_t* __restrict__ qzeros, const uint16_t* __restrict__ scales, int m, int n,
-                 int k, void* __restrict__ out) {
+                 int k, void* __restrict__ out, const uint8_t* __restrict__ ux_packed,
+                 const uint8_t* __restrict__ ux_zp, int ux_group) {
     constexpr int KPG = G / 16;  // MMA K-steps per group (a power of two)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
@@ -212,7 +219,7 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         n0 = (in / bsz) * BM;
     }
     const int nkb = (k + BK - 1) / BK;
-    const int ngroups = k / G;
+    const int ngroups = UX ? 1 : k / G;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -242,10 +249,11 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 const int s = kb % NS;
                 const uint32_t u = (uint32_t)(kb / NS);
                 if (!wait_bar(empty(s), (u & 1u) ^ 1u, abort_flag)) break;
-                wq::mbar_expect_tx(full(s), X_BYTES + Q_BYTES);
+                wq::mbar_expect_tx(full(s), UX ? X_BYTES : X_BYTES + Q_BYTES);
                 wq::tma_load_2d(x_at(s), &xmap, kb * BK, t0, full(s));
-                wq::tma_load_2d((uint32_t)__cvta_generic_to_shared(q_at(s)), &qmap, n0, kb * (BK / 8),
-                                full(s));
+                if (UX == 0)
+                    wq::tma_load_2d((uint32_t)__cvta_generic_to_shared(q_at(s)), &qmap, n0, kb * (BK / 8),
+                                    full(s));
                 ++issued;
             }
             // copies still in flight must land before the shared memory is released
@@ -276,7 +284,11 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 if (!wait_bar(full(s), par, abort_flag) || !wait_bar(aready(s), par, abort_flag)) break;
                 tc_fence_after();
                 const uint64_t da = da0 + (uint64_t)((s * STAGE) >> 4), db = db0 + (uint64_t)((s * STAGE) >> 4);
-                if constexpr (G >= BK) {
+                if constexpr (UX != 0) {
+                    // one accumulator over all of K
+                    mmas(da, db, 0u, 0, BK / 16, kb == 0);
+                    if (kb == nkb - 1) tc_commit(tfull(0));
+                } else if constexpr (G >= BK) {
                     // a group spans G / 64 whole K blocks
                     constexpr int BPG = G / BK;
                     const int g = kb / BPG;
@@ -311,6 +323,108 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         }
         __syncwarp();
     } else if (warp < DQ_WARPS) {
+      if constexpr (UX != 0) {
+        // ---------------------------------------------------------- uintx dequant
+        // Thread (r, h) writes K values 32h .. 32h+31 of each K block of feature
+        // row r.  The codes live in power-of-two bit shards (4, 2, 1 bits, in
+        // that order, the first holding the low bits); shard s of L_s bytes puts
+        // element e in byte e mod L_s at bit (e div L_s) * k_s.  With k % 64 == 0
+        // every L_s and every 8-element run start is a multiple of 8, so a run is
+        // one aligned 8-byte load per shard from one chunk.
+        const int r = threadIdx.x & (BM - 1), h = threadIdx.x >> 7;
+        const int nrow = n0 + r;
+        const bool rv = nrow < n;
+        constexpr int NSH = ((UX >> 2) & 1) + ((UX >> 1) & 1) + (UX & 1);
+        const int64_t numel = (int64_t)n * k;
+        int kbits[NSH], boff[NSH];
+        int64_t L[NSH], base[NSH], pos[NSH];
+        int chunk[NSH];
+        {
+            int si = 0, off = 0;
+            int64_t b = 0;
+#pragma unroll
+            for (int kb2 = 4; kb2 >= 1; kb2 >>= 1) {
+                if (UX & kb2) {
+                    kbits[si] = kb2;
+                    boff[si] = off;
+                    L[si] = numel / (8 / kb2);
+                    base[si] = b;
+                    b += L[si];
+                    off += kb2;
+                    ++si;
+                }
+            }
+            const int64_t e0 = (int64_t)nrow * k + 32 * h;  // element of this thread's first run
+#pragma unroll
+            for (int i = 0; i < NSH; ++i) {
+                chunk[i] = rv ? (int)(e0 / L[i]) : 0;
+                pos[i] = rv ? e0 - (int64_t)chunk[i] * L[i] : 0;
+            }
+        }
+        const int ngr = k / ux_group;
+        // raw words of one K block: [run][shard] plus the group's scale and zero point
+        struct Raw {
+            uint64_t w[4][NSH];
+            uint32_t sh[4][NSH];
+            uint32_t sc, zp;
+        };
+        auto fetch = [&](int kb, Raw& o) {
+            // positions advance by 64 elements per K block (wrapping into the next chunk)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int i = 0; i < NSH; ++i) {
+                    int64_t p = pos[i] + 8 * j;
+                    int c = chunk[i];
+                    while (p >= L[i]) { p -= L[i]; ++c; }
+                    o.sh[j][i] = (uint32_t)(c * kbits[i]);
+                    o.w[j][i] = rv ? __ldg(reinterpret_cast<const unsigned long long*>(ux_packed + base[i] + p)) : 0ull;
+                }
+            }
+            const int gi = (kb * BK + 32 * h) / ux_group;
+            o.sc = rv ? (uint32_t)__ldg(scales + (size_t)nrow * ngr + gi) : 0u;
+            o.zp = rv ? (uint32_t)__ldg(ux_zp + (size_t)nrow * ngr + gi) : 0u;
+#pragma unroll
+            for (int i = 0; i < NSH; ++i) {
+                pos[i] += BK;
+                while (pos[i] >= L[i]) { pos[i] -= L[i]; ++chunk[i]; }
+            }
+        };
+        Raw nxt;
+        fetch(0, nxt);
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % NS;
+            const Raw cur = nxt;  // loaded one K block ago
+            if (kb + 1 < nkb) fetch(kb + 1, nxt);
+            if (!warp_wait(full(s), (uint32_t)(kb / NS) & 1u, abort_flag)) break;
+            const uint32_t zb2 = (0x4300u + cur.zp) * 0x10001u;  // bf16x2 of 128 + zp
+            const uint32_t sc2 = cur.sc * 0x10001u;              // bf16x2 of the scale
+            const uint32_t arow = a_at(s) + r * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint64_t q = 0;  // eight code bytes
+#pragma unroll
+                for (int i = 0; i < NSH; ++i) {
+                    const uint64_t mask = (uint64_t)((1u << kbits[i]) - 1u) * 0x0101010101010101ull;
+                    q |= ((cur.w[j][i] >> cur.sh[j][i]) & mask) << boff[i];
+                }
+                const uint32_t lo = (uint32_t)q, hi = (uint32_t)(q >> 32);
+                // bf16 of 128 + q, minus 128 + zp (exact), times the scale: the
+                // page's bf16 sub and bf16 multiply, each rounded once
+                const uint32_t d0 = wq::bmul2(wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4140), zb2), sc2);
+                const uint32_t d1 = wq::bmul2(wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4342), zb2), sc2);
+                const uint32_t d2 = wq::bmul2(wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4140), zb2), sc2);
+                const uint32_t d3 = wq::bmul2(wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4342), zb2), sc2);
+                const uint32_t dst = arow + (uint32_t)(((4 * h + j) ^ (r & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(d0), "r"(d1),
+                             "r"(d2), "r"(d3)
+                             : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(aready(s));
+        }
+      } else {
         // ---------------------------------------------------------- dequant
         // Two threads per feature row: thread (r, h) converts qweight rows 4h..4h+3
         // of a stage (32 K values, inside one group for every supported group).
@@ -370,6 +484,7 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 if (two) mbar_arrive(aready((kb + 1) % NS));
             }
         }
+      }
     } else {
         // ---------------------------------------------------------- epilogue
         const int quarter = warp & 3, half = (warp - EPI_WARP0) >> 2;
@@ -380,11 +495,11 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0.f;
         bool ok = true;
-        float sc_next = (rv && ngroups > 0) ? __half2float(__ushort_as_half(scales[nrow])) : 0.f;
+        float sc_next = UX ? 1.f : ((rv && ngroups > 0) ? __half2float(__ushort_as_half(scales[nrow])) : 0.f);
         for (int g = 0; g < ngroups; ++g) {
             const int b = g & 1;
-            const float sc = sc_next;
-            if (g + 1 < ngroups && rv)
+            const float sc = sc_next;  // uintx: 1 (y = P exactly)
+            if (UX == 0 && g + 1 < ngroups && rv)
                 sc_next = __half2float(__ushort_as_half(scales[(size_t)(g + 1) * n + nrow]));
             if (!warp_wait(tfull(b), (uint32_t)(g >> 1) & 1u, abort_flag)) {
                 ok = false;
@@ -440,9 +555,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
     return fn;
 }
 
-template <bool SYM, bool BF16OUT, int G>
+template <bool SYM, bool BF16OUT, int G, int UX>
 wq_status launch(const uint16_t* x, int64_t m, const int32_t* qweight, const int32_t* qzeros,
-                 const uint16_t* scales, int64_t n, int64_t k, void* out, cudaStream_t st) {
+                 const uint16_t* scales, int64_t n, int64_t k, void* out, cudaStream_t st,
+                 const uint8_t* ux_packed = nullptr, const uint8_t* ux_zp = nullptr, int ux_group = 0) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
     if (!enc) return wqh::cuda_status(cudaErrorNotSupported);
     CUtensorMap xmap, qmap;
@@ -457,7 +573,7 @@ wq_status launch(const uint16_t* x, int64_t m, const int32_t* qweight, const int
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return WQ_ERR_BAD_SHAPE;
     }
-    {
+    if (UX == 0) {
         // qweight [k/8, n] int32: boxes of 8 rows x 128 features, unswizzled, zeros outside
         const cuuint64_t dims[2] = {(cuuint64_t)n, (cuuint64_t)(k / 8)};
         const cuuint64_t strides[1] = {(cuuint64_t)n * 4};
@@ -467,8 +583,10 @@ wq_status launch(const uint16_t* x, int64_t m, const int32_t* qweight, const int
                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return WQ_ERR_BAD_SHAPE;
+    } else {
+        qmap = xmap;  // not read by the uintx kernels
     }
-    const void* fn = (const void*)gptq_gemm_kernel<SYM, BF16OUT, G>;
+    const void* fn = (const void*)gptq_gemm_kernel<SYM, BF16OUT, G, UX>;
     static bool attr_set = false;
     if (!attr_set) {
         const wq_status s =
@@ -477,8 +595,8 @@ wq_status launch(const uint16_t* x, int64_t m, const int32_t* qweight, const int
         attr_set = true;
     }
     const dim3 grid((unsigned)(((n + BM - 1) / BM) * ((m + BT - 1) / BT)));
-    gptq_gemm_kernel<SYM, BF16OUT, G><<<grid, THREADS, SMEM, st>>>(xmap, qmap, qzeros, scales, (int)m, (int)n,
-                                                                  (int)k, out);
+    gptq_gemm_kernel<SYM, BF16OUT, G, UX><<<grid, THREADS, SMEM, st>>>(
+        xmap, qmap, qzeros, scales, (int)m, (int)n, (int)k, out, ux_packed, ux_zp, ux_group);
     return wqh::check_launch();
 }
 
@@ -487,10 +605,17 @@ wq_status dispatch_rule(bool sym, bool bf, const uint16_t* x, int64_t m, const i
                         const int32_t* qzeros, const uint16_t* scales, int64_t n, int64_t k, void* out,
                         cudaStream_t st) {
     if (sym)
-        return bf ? launch<true, true, G>(x, m, qweight, qzeros, scales, n, k, out, st)
-                  : launch<true, false, G>(x, m, qweight, qzeros, scales, n, k, out, st);
-    return bf ? launch<false, true, G>(x, m, qweight, qzeros, scales, n, k, out, st)
-              : launch<false, false, G>(x, m, qweight, qzeros, scales, n, k, out, st);
+        return bf ? launch<true, true, G, 0>(x, m, qweight, qzeros, scales, n, k, out, st)
+                  : launch<true, false, G, 0>(x, m, qweight, qzeros, scales, n, k, out, st);
+    return bf ? launch<false, true, G, 0>(x, m, qweight, qzeros, scales, n, k, out, st)
+              : launch<false, false, G, 0>(x, m, qweight, qzeros, scales, n, k, out, st);
+}
+
+template <int UX>
+wq_status launch_ux(bool bf, const uint16_t* x, int64_t m, const uint8_t* packed, const uint16_t* scale,
+                    const uint8_t* zp, int64_t n, int64_t k, int group, void* out, cudaStream_t st) {
+    return bf ? launch<false, true, 64, UX>(x, m, nullptr, nullptr, scale, n, k, out, st, packed, zp, group)
+              : launch<false, false, 64, UX>(x, m, nullptr, nullptr, scale, n, k, out, st, packed, zp, group);
 }
 
 wq_status dispatch_g(int group, bool sym, bool bf, const uint16_t* x, int64_t m, const int32_t* qweight,
@@ -546,6 +671,39 @@ wq_status gptq_gemm(const uint16_t* x, int64_t m, const int32_t* qweight, const 
         return WQ_ERR_MISALIGNED;
     const bool bf = out_dtype == WQ_DTYPE_BF16;
     return dispatch_g(group, sym != 0, bf, x, m, qweight, qzeros, scales, n, k, out, st);
+}
+
+wq_status uintx_gemm(const uint16_t* x, int64_t m, const uint8_t* packed, const uint16_t* scale,
+                     const uint8_t* zp, int64_t n, int64_t k, int nbits, int group, int out_dtype, void* out,
+                     void* stream) {
+    if (m < 0 || n < 0 || k < 0) return WQ_ERR_BAD_SHAPE;
+    if (nbits < 2 || nbits > 7) return WQ_ERR_UNSUPPORTED;
+    if (group != 32 && group != 64 && group != 128 && group != 256) return WQ_ERR_UNSUPPORTED;
+    if (k % group != 0) return WQ_ERR_BAD_SHAPE;
+    if (k % 64 != 0) return WQ_ERR_UNSUPPORTED;
+    if (m >= (1ll << 31) || n >= (1ll << 31) || k >= (1ll << 31) ||
+        ((n + BM - 1) / BM) * ((m + BT - 1) / BT) >= (1ll << 31))
+        return WQ_ERR_BAD_SHAPE;
+    if (out_dtype != WQ_DTYPE_F32 && out_dtype != WQ_DTYPE_BF16) return WQ_ERR_BAD_DTYPE;
+    if (m == 0 || n == 0) return WQ_OK;
+    if (!out) return WQ_ERR_NULL_PTR;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (k == 0)  // an empty sum: y = 0
+        return wqh::cuda_status(
+            cudaMemsetAsync(out, 0, (size_t)(m * n) * (out_dtype == WQ_DTYPE_BF16 ? 2 : 4), st));
+    if (!x || !packed || !scale || !zp) return WQ_ERR_NULL_PTR;
+    if (!wqh::aligned16(x) || !wqh::aligned16(packed) || !wqh::aligned_to(scale, 2) ||
+        !wqh::aligned_to(out, 4))
+        return WQ_ERR_MISALIGNED;
+    const bool bf = out_dtype == WQ_DTYPE_BF16;
+    switch (nbits) {
+        case 2: return launch_ux<2>(bf, x, m, packed, scale, zp, n, k, group, out, st);
+        case 3: return launch_ux<3>(bf, x, m, packed, scale, zp, n, k, group, out, st);
+        case 4: return launch_ux<4>(bf, x, m, packed, scale, zp, n, k, group, out, st);
+        case 5: return launch_ux<5>(bf, x, m, packed, scale, zp, n, k, group, out, st);
+        case 6: return launch_ux<6>(bf, x, m, packed, scale, zp, n, k, group, out, st);
+        default: return launch_ux<7>(bf, x, m, packed, scale, zp, n, k, group, out, st);
+    }
 }
 
 }  // extern "C"
