@@ -63,6 +63,7 @@ def _load():
                 "orc_e2m1_code": (I, [ctypes.c_float, I]),
                 "orc_pack_int32": (None, [P, I64, I64, I, P]),
                 "orc_gptq_quantize": (None, [P, I64, I64, I, I, P, P, P, P, P]),
+                "orc_gptq_quantize_f32": (None, [P, I64, I64, I, I, P, P, P, P, P]),
                 "orc_gptq_dequantize": (None, [P, P, P, I64, I64, I, I, I, P]),
                 "orc_mxfp4_quantize_f32": (None, [P, I64, I64, I, P, P]),
                 "orc_mxfp4_quantize": (None, [P, I64, I64, I, P, P]),
@@ -154,6 +155,22 @@ def gptq_quantize(w, group: int = 128, sym: bool = True):
     snr = ctypes.c_double()
     _load().orc_gptq_quantize(_p(w), n, k, group, int(sym), _p(qw), _p(qz), _p(sc), _p(gi),
                               ctypes.byref(snr))
+    return qw, qz, sc, gi, snr.value
+
+
+def gptq_quantize_f32(w: np.ndarray, group: int = 128, sym: bool = True):
+    """The same from a binary32 weight (an fp16 or fp32 input after the page's
+    w.float()).  -> as gptq_quantize."""
+    w = np.ascontiguousarray(w, np.float32)
+    n, k = w.shape
+    g = k // group
+    qw = np.zeros((k // 8, n), np.int32)
+    qz = np.zeros((g, n // 8), np.int32)
+    sc = np.zeros((g, n), np.uint16)
+    gi = np.zeros((k,), np.int32)
+    snr = ctypes.c_double()
+    _load().orc_gptq_quantize_f32(_p(w), n, k, group, int(sym), _p(qw), _p(qz), _p(sc), _p(gi),
+                                  ctypes.byref(snr))
     return qw, qz, sc, gi, snr.value
 
 

@@ -157,9 +157,11 @@ static double snr_from_sums(double sw, double se) {
  * Outputs: qweight int32 [k/8, n], qzeros int32 [k/group, n/8], scales fp16
  * [k/group, n], g_idx int32 [k] = kk // group, snr_db (binary64, from the binary32
  * deq before the fp16 rounding of the scales).  Any output pointer may be NULL. */
-void orc_gptq_quantize(const uint16_t* w, int64_t n, int64_t k, int group, int sym,
-                       int32_t* qweight, int32_t* qzeros, uint16_t* scales,
-                       int32_t* g_idx, double* snr_db) {
+/* quantize_sym / quantize_asym on a binary32 [n, k] weight: the page first
+ * takes w.float(), so every input type reaches this arithmetic as binary32. */
+void orc_gptq_quantize_f32(const float* w, int64_t n, int64_t k, int group, int sym,
+                           int32_t* qweight, int32_t* qzeros, uint16_t* scales,
+                           int32_t* g_idx, double* snr_db) {
     int64_t g = k / group;
     float* wt = (float*)malloc(sizeof(float) * (size_t)(k * n));
     int32_t* codes = (int32_t*)malloc(sizeof(int32_t) * (size_t)(k * n));
@@ -168,7 +170,7 @@ void orc_gptq_quantize(const uint16_t* w, int64_t n, int64_t k, int group, int s
     int32_t* zp = (int32_t*)malloc(sizeof(int32_t) * (size_t)(g * n));
 
     for (int64_t r = 0; r < n; ++r)
-        for (int64_t c = 0; c < k; ++c) wt[c * n + r] = orc_bf16_to_f32(w[r * k + c]);
+        for (int64_t c = 0; c < k; ++c) wt[c * n + r] = w[r * k + c];
 
     for (int64_t gi = 0; gi < g; ++gi) {
         for (int64_t col = 0; col < n; ++col) {
@@ -228,6 +230,16 @@ void orc_gptq_quantize(const uint16_t* w, int64_t n, int64_t k, int group, int s
  * uint4b8: w = (code - 8) * scale; with real zero points w = (code - zp) * scale;
  * the scale is the stored fp16 value).  Output binary32, layout [k, n] when
  * out_kn != 0 (the page's deq layout) else [n, k] (the original weight layout). */
+/* The bf16 weight widened exactly to binary32, then the binary32 path. */
+void orc_gptq_quantize(const uint16_t* w, int64_t n, int64_t k, int group, int sym,
+                       int32_t* qweight, int32_t* qzeros, uint16_t* scales,
+                       int32_t* g_idx, double* snr_db) {
+    float* wf = (float*)malloc(sizeof(float) * (size_t)(k * n));
+    for (int64_t i = 0; i < n * k; ++i) wf[i] = orc_bf16_to_f32(w[i]);
+    orc_gptq_quantize_f32(wf, n, k, group, sym, qweight, qzeros, scales, g_idx, snr_db);
+    free(wf);
+}
+
 void orc_gptq_dequantize(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales,
                          int64_t n, int64_t k, int group, int sym, int out_kn, float* out) {
     for (int64_t kk = 0; kk < k; ++kk) {

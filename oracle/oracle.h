@@ -26,6 +26,9 @@ int orc_floor_log2(float a);
 int orc_e2m1_code(float v, int tie_mode);
 
 void orc_pack_int32(const int32_t* codes, int64_t k, int64_t n, int dim, int32_t* out);
+void orc_gptq_quantize_f32(const float* w, int64_t n, int64_t k, int group, int sym,
+                           int32_t* qweight, int32_t* qzeros, uint16_t* scales,
+                           int32_t* g_idx, double* snr_db);
 void orc_gptq_quantize(const uint16_t* w, int64_t n, int64_t k, int group, int sym,
                        int32_t* qweight, int32_t* qzeros, uint16_t* scales, int32_t* g_idx,
                        double* snr_db);

@@ -729,3 +729,54 @@ def test_mxfp4_linear_one_hot_rows_pick_dequantized_columns():
         mag = np.array([E2M1[c & 7] for c in code]) * np.where(code & 8, -1.0, 1.0)
         want = mag * np.exp2(e[:, j // 32].astype(float) - 127)
         np.testing.assert_array_equal(y[0], want)
+
+
+# ---------------------------------------------------------------- binary32 GPTQ input
+# export_gptq_cpu.py quantizes w.float(): an fp16 or fp32 weight reaches the same
+# binary32 arithmetic with more significant bits than bf16 holds.  Two hand-worked
+# groups (k = group = 8, eight identical columns) use values that only binary32
+# represents, placed so that rounding the input to bf16 first changes a code.
+def _col8(vals):
+    return np.tile(np.asarray(vals, np.float32).reshape(1, 8), (8, 1))
+
+
+def _word(codes):
+    return int(np.int32(np.uint32(sum(int(c) << (4 * i) for i, c in enumerate(codes)))))
+
+
+def test_gptq_f32_sym_hand_group():
+    e = 2.0 ** -26
+    # amax 1.0 -> scale 1/8 exactly; x/scale = 8, -4, 1.5-2^-23, 1.5+2^-23, 2.5, -0.5, 2^-27, -8
+    w = _col8([1.0, -0.5, 0.1875 - e, 0.1875 + e, 0.3125, -0.0625, 2.0 ** -30, -1.0])
+    qw, qz, sc, gi, snr = oracle.gptq_quantize_f32(w, 8, True)
+    codes = [15, 4, 9, 10, 10, 8, 8, 0]  # round half even, +8, clamp (16 -> 15)
+    assert np.all(qw == _word(codes)) and np.all(sc == 0x3000) and np.all(qz == 0x77777777)
+    deq = (np.asarray(codes, np.float64) - 8) * 0.125
+    x = w[0].astype(np.float64)
+    ref = 20 * np.log10(np.sqrt((x * x).sum()) / np.sqrt(((x - deq) ** 2).sum()))
+    assert abs(snr - ref) <= 1e-6 * abs(ref)
+    # the same values rounded to bf16 first give a different code (0.1875 - 2^-26 -> 0.1875 -> 1.5 -> 2)
+    import torch
+
+    wb = oracle.bf16_bits_to_f32(oracle._u16(torch.from_numpy(w).to(torch.bfloat16)))
+    assert not np.array_equal(oracle.gptq_quantize_f32(wb, 8, True)[0], qw)
+
+
+def test_gptq_f32_asym_hand_group():
+    # wmin -0.46875, wmax 0.46875: scale = 0.9375 / 15 = 1/16 exactly; zp = rne(7.5) = 8
+    w = _col8([-0.46875, 0.46875, 0.03125 + 2.0 ** -28, 0.03125, -0.09375, 0.15625 - 2.0 ** -26, 0.0, -0.25])
+    qw, qz, sc, gi, snr = oracle.gptq_quantize_f32(w, 8, False)
+    # x/scale = -7.5, 7.5, 0.5+2^-24, 0.5, -1.5, 2.5-2^-22, 0, -4 -> rne -8, 8, 1, 0, -2, 2, 0, -4; + 8
+    codes = [0, 15, 9, 8, 6, 10, 8, 4]
+    assert np.all(qw == _word(codes)) and np.all(sc == 0x2C00) and np.all(qz == _word([8] * 8))
+    assert np.array_equal(gi, np.zeros(8, np.int32))
+
+
+def test_gptq_f32_path_equals_bf16_path_on_bf16_values():
+    from weight_only_bit_group_gb300 import synth
+
+    w = synth.outlier_columns_bf16(64, 256, 0.02, 0.01, 20.0, 31)
+    for sym in (True, False):
+        a = oracle.gptq_quantize(w, 64, sym)
+        b = oracle.gptq_quantize_f32(oracle.bf16_bits_to_f32(oracle._u16(w)), 64, sym)
+        assert all(np.array_equal(x, y) for x, y in zip(a[:4], b[:4])) and a[4] == b[4]
