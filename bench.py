@@ -724,6 +724,10 @@ def run_single(args):
     dev = torch.device("cuda", 0)
     n, k = (int(x) for x in args.shape.split("x"))
     w = synth.outlier_columns_bf16(n, k, 0.02, 0.005, 20.0, 11, device=dev)
+    esize = 2
+    if args.wdtype != "bf16":  # fp16 / fp32 weights for the quantize kernels
+        w = w.float() if args.wdtype == "f32" else w.half()
+        esize = w.element_size()
     name = args.kernel
     ws = wq.workspace(wq.WQ_OP_GPTQ_QUANTIZE, n, k, GROUP_GPTQ, dev)
     if name.startswith("gptq_quantize"):
@@ -731,7 +735,7 @@ def run_single(args):
         out = fn(w, GROUP_GPTQ, True, ws=ws)
         call = lambda: fn(w, GROUP_GPTQ, True, qweight=out["qweight"], qzeros=out["qzeros"],
                           scales=out["scales"], g_idx=out["g_idx"], snr_db=out["snr_db"], ws=ws)
-        alg = n * k * (2 + 0.5) + (n * k // GROUP_GPTQ) * 2.5 + 4 * k
+        alg = n * k * (esize + 0.5) + (n * k // GROUP_GPTQ) * 2.5 + 4 * k
     elif name.startswith("gptq_dequantize"):
         sym = name.endswith("sym")
         r = (wq.gptq_quantize_sym if sym else wq.gptq_quantize_asym)(w, GROUP_GPTQ, False)
@@ -742,7 +746,7 @@ def run_single(args):
     elif name == "mxfp4_quantize":
         p, e = wq.mxfp4_quantize(w)
         call = lambda: wq.mxfp4_quantize(w, 0, packed=p, e8m0=e)
-        alg = n * k * (2 + 0.5 + 1 / 32)
+        alg = n * k * (esize + 0.5 + 1 / 32)
     elif name == "mxfp4_dequantize":
         p, e = wq.mxfp4_quantize(w)
         out = torch.empty(n, k, dtype=torch.bfloat16, device=dev)
@@ -845,6 +849,8 @@ def main():
     ap.add_argument("--kernel", default=None, help="time one kernel alone (see run_single)")
     ap.add_argument("--shape", default="16384x8192")
     ap.add_argument("--m", type=int, default=512, help="tokens for --kernel gptq_gemm / uintx_gemm")
+    ap.add_argument("--wdtype", choices=["bf16", "f16", "f32"], default="bf16",
+                    help="weight type for --kernel gptq_quantize_* / mxfp4_quantize")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="issue every call eagerly instead of a CUDA graph")

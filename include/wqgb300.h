@@ -57,9 +57,11 @@ typedef int wq_status;
 #define WQ_ERR_CUDA 7
 #define WQ_ERR_DEVICE_TIMEOUT 8 /* a bounded device-side wait ran out (see wq_device_status) */
 
-/* Output element types. */
+/* Element types: outputs take F32 or BF16; weight inputs of gptq_quantize_ex
+ * and mxfp4_quantize_ex also F16. */
 #define WQ_DTYPE_F32 0
 #define WQ_DTYPE_BF16 1
+#define WQ_DTYPE_F16 2
 
 /* Layout of a dequantized matrix. NK = [n, k] (the weight's own layout);
  * KN = [k, n] (the transposed layout the GPTQ page computes its deq in). */
@@ -139,6 +141,17 @@ wq_status gptq_quantize_asym(const uint16_t* w, int64_t n, int64_t k, int group,
                              int32_t* qzeros, uint16_t* scales, int32_t* g_idx, double* snr_db,
                              void* workspace, size_t workspace_bytes, void* stream);
 
+/* gptq_quantize_ex (export_gptq_cpu.py quantize_sym / quantize_asym, which start
+ * from w.float()) -- the same outputs, workspace and rules as gptq_quantize_sym /
+ * _asym (sym selects), for a weight of type w_dtype: WQ_DTYPE_BF16 calls those
+ * entry points; WQ_DTYPE_F16 and WQ_DTYPE_F32 take the binary32 arithmetic on
+ * the exactly widened values (IEEE divisions, round half to even, the SNR from
+ * binary32 squares with compensated sums).  w 16-byte aligned; other inputs
+ * WQ_ERR_BAD_DTYPE. */
+wq_status gptq_quantize_ex(const void* w, int w_dtype, int64_t n, int64_t k, int group, int sym,
+                           int32_t* qweight, int32_t* qzeros, uint16_t* scales, int32_t* g_idx,
+                           double* snr_db, void* workspace, size_t workspace_bytes, void* stream);
+
 /* gptq_dequantize (export_gptq_cpu.py module docstring: uint4b8 w = (code-8)*scale;
  * with real zero points w = (code - zp) * scale).
  * In:  qweight, qzeros (ignored when sym != 0, may be NULL then), scales as
@@ -162,6 +175,14 @@ wq_status gptq_dequantize(const int32_t* qweight, const int32_t* qzeros, const u
  * sign = signbit(v) (so -0.0 codes as 8). */
 wq_status mxfp4_quantize(const uint16_t* w, int64_t n, int64_t k, int tie_mode, uint8_t* packed,
                          uint8_t* e8m0, void* stream);
+
+/* mxfp4_quantize_ex (quantize_dflash_mxfp4.py quantize_mxfp4, which starts from
+ * w.float()) -- as mxfp4_quantize for a weight of type w_dtype (WQ_DTYPE_BF16
+ * calls it; WQ_DTYPE_F16 / WQ_DTYPE_F32: the block exponent from the binary32
+ * amax, the values scaled by the exact power of two and rounded to e2m1 by the
+ * tie mode).  w and packed 16-byte aligned. */
+wq_status mxfp4_quantize_ex(const void* w, int w_dtype, int64_t n, int64_t k, int tie_mode,
+                            uint8_t* packed, uint8_t* e8m0, void* stream);
 
 /* mxfp4_dequantize (quantize_dflash_mxfp4.py, dequantize_mxfp4)
  * out[n][c] = +-E2M1[code & 7] * 2^(e8m0 - 127) as binary32 (WQ_DTYPE_F32) or bf16

@@ -134,6 +134,24 @@ def test_uintx_gemm_argument_errors(L):
     assert L.uintx_gemm(None, 0, None, None, None, 64, 128, 4, 64, 0, None, None) == 0
 
 
+def test_wide_quantize_argument_errors(L):
+    ws = 1 << 20
+    # dtype 7 is no weight type; uint8 outputs etc. are not checked before the dtype
+    assert L.gptq_quantize_ex(BAD, 7, 64, 128, 128, 1, BAD, BAD, BAD, BAD, None, None, 0, None) == 3
+    assert L.gptq_quantize_ex(BAD, 0, 64, 128, 96, 1, BAD, BAD, BAD, BAD, None, None, 0, None) == 5
+    assert L.gptq_quantize_ex(BAD, 2, 60, 128, 128, 1, BAD, BAD, BAD, BAD, None, None, 0, None) == 2
+    assert L.gptq_quantize_ex(BAD, 0, 64, 128, 128, 1, None, BAD, BAD, BAD, None, None, 0, None) == 1
+    assert L.gptq_quantize_ex(BAD, 0, 64, 128, 128, 0, BAD, BAD, BAD, BAD, BAD, BAD, 16, None) == 6
+    assert L.gptq_quantize_ex(MIS, 2, 64, 128, 128, 1, BAD, BAD, BAD, BAD, None, None, 0, None) == 4
+    assert L.gptq_quantize_ex(None, 0, 0, 128, 128, 1, None, None, None, None, None, None, 0, None) == 0
+    assert L.mxfp4_quantize_ex(BAD, 7, 64, 64, 0, BAD, BAD, None) == 3
+    assert L.mxfp4_quantize_ex(BAD, 0, 64, 48, 0, BAD, BAD, None) == 2
+    assert L.mxfp4_quantize_ex(BAD, 2, 64, 64, 5, BAD, BAD, None) == 5
+    assert L.mxfp4_quantize_ex(MIS, 0, 64, 64, 0, BAD, BAD, None) == 4
+    assert L.mxfp4_quantize_ex(None, 2, 0, 64, 0, None, None, None) == 0
+    assert ws  # (the SNR workspace size is the bf16 path's)
+
+
 def test_mxfp4_linear_argument_errors(L):
     assert L.mxfp4_linear(BAD, 1, BAD, BAD, 64, 48, 0, BAD, None) == 2     # k % 32 != 0
     assert L.mxfp4_linear(BAD, 9, BAD, BAD, 64, 64, 0, BAD, None) == 5     # m > 8

@@ -31,6 +31,7 @@ from ._build import LIB as _LIB_PATH
 WQ_OK = 0
 WQ_DTYPE_F32 = 0
 WQ_DTYPE_BF16 = 1
+WQ_DTYPE_F16 = 2
 WQ_LAYOUT_NK = 0
 WQ_LAYOUT_KN = 1
 WQ_TIE_HALF_EVEN = 0
@@ -93,6 +94,8 @@ def lib():
                 "gptq_linear": (I, [P, I64, P, P, P, I64, I64, I, I, I, P, P, SZ, P]),
                 "mxfp4_linear": (I, [P, I64, P, P, I64, I64, I, P, P]),
                 "gptq_gemm": (I, [P, I64, P, P, P, I64, I64, I, I, I, P, P]),
+                "gptq_quantize_ex": (I, [P, I, I64, I64, I, I, P, P, P, P, P, P, SZ, P]),
+                "mxfp4_quantize_ex": (I, [P, I, I64, I64, I, P, P, P]),
                 "uintx_gemm": (I, [P, I64, P, P, P, I64, I64, I, I, I, P, P]),
             }
             for name, (res, args) in sig.items():
@@ -143,8 +146,14 @@ def workspace(op: int, n: int, k: int, arg: int = 0, device="cuda") -> torch.Ten
 
 
 # ------------------------------------------------------------------ GPTQ
+_WIDE = {torch.float32: WQ_DTYPE_F32, torch.float16: WQ_DTYPE_F16}
+
+
 def _gptq_quantize(name, w, group, snr, qweight, qzeros, scales, g_idx, snr_db, ws):
-    _u16(w)
+    wide = w.dtype in _WIDE and w.dtype != torch.bfloat16
+    if not wide:
+        _u16(w)
+    assert w.is_contiguous(), "tensor must be contiguous"
     n, k = w.shape
     g = k // group
     qweight = _empty((k // 8, n), torch.int32, w) if qweight is None else qweight
@@ -156,9 +165,14 @@ def _gptq_quantize(name, w, group, snr, qweight, qzeros, scales, g_idx, snr_db, 
         ws = workspace(WQ_OP_GPTQ_QUANTIZE, n, k, group, w.device) if ws is None else ws
     else:
         snr_db = None
-    st = getattr(lib(), name)(_ptr(w), n, k, group, _ptr(qweight), _ptr(qzeros), _ptr(scales),
-                              _ptr(g_idx), _ptr(snr_db), _ptr(ws), 0 if ws is None else ws.numel(),
-                              _stream(w.device))
+    if wide:  # fp16 / fp32 weights: the binary32 path of gptq_quantize_ex
+        st = lib().gptq_quantize_ex(_ptr(w), _WIDE[w.dtype], n, k, group, int(name == "gptq_quantize_sym"),
+                                    _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(g_idx), _ptr(snr_db),
+                                    _ptr(ws), 0 if ws is None else ws.numel(), _stream(w.device))
+    else:
+        st = getattr(lib(), name)(_ptr(w), n, k, group, _ptr(qweight), _ptr(qzeros), _ptr(scales),
+                                  _ptr(g_idx), _ptr(snr_db), _ptr(ws), 0 if ws is None else ws.numel(),
+                                  _stream(w.device))
     _check(st, name)
     return {"qweight": qweight, "qzeros": qzeros, "scales": scales, "g_idx": g_idx,
             "snr_db": snr_db}
@@ -192,12 +206,20 @@ def gptq_dequantize(qweight, qzeros, scales, n, k, group=128, sym=True,
 
 # ------------------------------------------------------------------ MXFP4
 def mxfp4_quantize(w, tie_mode=WQ_TIE_HALF_EVEN, *, packed=None, e8m0=None):
-    """quantize_dflash_mxfp4.py quantize_mxfp4 on the GPU -> (packed u8 [N,K/2], e8m0 u8 [N,K/32])."""
-    _u16(w)
+    """quantize_dflash_mxfp4.py quantize_mxfp4 on the GPU -> (packed u8 [N,K/2], e8m0 u8 [N,K/32]).
+    w: bf16, fp16 or fp32 [N, K]."""
+    wide = w.dtype in (torch.float32, torch.float16)
+    if not wide:
+        _u16(w)
+    assert w.is_contiguous(), "tensor must be contiguous"
     n, k = w.shape
     packed = _empty((n, k // 2), torch.uint8, w) if packed is None else packed
     e8m0 = _empty((n, k // 32), torch.uint8, w) if e8m0 is None else e8m0
-    st = lib().mxfp4_quantize(_ptr(w), n, k, tie_mode, _ptr(packed), _ptr(e8m0), _stream(w.device))
+    if wide:
+        st = lib().mxfp4_quantize_ex(_ptr(w), _WIDE[w.dtype], n, k, tie_mode, _ptr(packed), _ptr(e8m0),
+                                     _stream(w.device))
+    else:
+        st = lib().mxfp4_quantize(_ptr(w), n, k, tie_mode, _ptr(packed), _ptr(e8m0), _stream(w.device))
     _check(st, "mxfp4_quantize")
     return packed, e8m0
 
