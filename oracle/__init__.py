@@ -76,6 +76,8 @@ def _load():
                 "orc_uintx_pack": (None, [P, I64, I, P]),
                 "orc_uintx_unpack": (None, [P, I64, I, P]),
                 "orc_uintx_quantize": (None, [P, I64, I64, I, I, P, P, P, P]),
+                "orc_uintx_quantize_dt": (None, [P, I, I64, I64, I, I, P, P, P, P]),
+                "orc_uintx_dequantize_dt": (None, [P, P, I, P, I64, I64, I, I, P]),
                 "orc_uintx_dequantize": (None, [P, P, P, I64, I64, I, I, P]),
             }
             for name, (res, args) in sig.items():
@@ -341,4 +343,37 @@ def uintx_dequantize(packed, scale, zp, n: int, k: int, nbits: int, group: int =
     zp = np.ascontiguousarray(zp, np.uint8)
     out = np.zeros((n, k), np.uint16)
     _load().orc_uintx_dequantize(_p(packed), _p(scale), _p(zp), n, k, nbits, group, _p(out))
+    return out
+
+
+# uintx in the weight's own dtype: dt 0 = binary32 (float32 arrays), 1 = bf16,
+# 2 = binary16 (uint16 bit patterns for the 16-bit types)
+def _dt_array(w, dt: int) -> np.ndarray:
+    if _is_torch(w):
+        import torch
+
+        w = w.detach().cpu().contiguous()
+        w = w.numpy() if w.dtype == torch.float32 else w.view(torch.int16).numpy().view(np.uint16)
+    return np.ascontiguousarray(w, np.float32 if dt == 0 else np.uint16)
+
+
+def uintx_quantize_dt(w, dt: int, nbits: int, group: int = 64):
+    """-> (packed u8, scale [N,K/g] in dt (float32 or uint16 bits), zp u8, codes u8)."""
+    w = _dt_array(w, dt)
+    n, k = w.shape
+    packed = np.zeros((uintx_packed_bytes(n * k, nbits),), np.uint8)
+    sc = np.zeros((n, k // group), np.float32 if dt == 0 else np.uint16)
+    zp = np.zeros((n, k // group), np.uint8)
+    codes = np.zeros((n, k), np.uint8)
+    _load().orc_uintx_quantize_dt(_p(w), dt, n, k, nbits, group, _p(packed), _p(sc), _p(zp), _p(codes))
+    return packed, sc, zp, codes
+
+
+def uintx_dequantize_dt(packed, scale, dt: int, zp, n: int, k: int, nbits: int, group: int = 64):
+    """-> [N,K] in dt (float32, or uint16 bit patterns)."""
+    packed = np.ascontiguousarray(packed, np.uint8)
+    scale = _dt_array(scale, dt)
+    zp = np.ascontiguousarray(zp, np.uint8)
+    out = np.zeros((n, k), np.float32 if dt == 0 else np.uint16)
+    _load().orc_uintx_dequantize_dt(_p(packed), _p(scale), dt, _p(zp), n, k, nbits, group, _p(out))
     return out

@@ -549,39 +549,61 @@ void orc_uintx_unpack(const uint8_t* packed, int64_t numel, int nbits, uint8_t* 
  * then pack_uintx of the flattened row-major codes.  scale_out holds the bf16
  * scales [n, k/group], zp_out the uint8 zero points, codes_out (may be NULL) the
  * unpacked codes. */
-void orc_uintx_quantize(const uint16_t* w, int64_t n, int64_t k, int nbits, int group,
-                        uint8_t* packed, uint16_t* scale_out, uint8_t* zp_out,
-                        uint8_t* codes_out) {
+/* uintx in the weight's own dtype (uintx_quant.py works in the weight dtype):
+ * dt = 0 binary32, 1 bf16, 2 binary16.  Every op is the binary32 op on the
+ * operands, rounded once to dt (identity for binary32). */
+static float r_dt(float x, int dt) {
+    if (dt == 1) return bf(x);
+    if (dt == 2) return orc_f16_to_f32(orc_f32_to_f16(x));
+    return x;
+}
+static float load_dt(const void* w, int64_t i, int dt) {
+    if (dt == 1) return orc_bf16_to_f32(((const uint16_t*)w)[i]);
+    if (dt == 2) return orc_f16_to_f32(((const uint16_t*)w)[i]);
+    return ((const float*)w)[i];
+}
+static void store_dt(void* out, int64_t i, int dt, float v) {
+    if (dt == 1) ((uint16_t*)out)[i] = orc_f32_to_bf16(v);
+    else if (dt == 2) ((uint16_t*)out)[i] = orc_f32_to_f16(v);
+    else ((float*)out)[i] = v;
+}
+
+/* UIntXQuantizer._quantize_impl + pack_uintx: per group of `group` values along
+ * k, min/max extended to include 0, scale = (max_pos - min_neg) / qmax clamped
+ * to float32 eps, zero point = clamp(qmin - round(min_neg / scale)), codes =
+ * clamp(round(w * (1 / scale)) + zp); every op in dt. */
+void orc_uintx_quantize_dt(const void* w, int dt, int64_t n, int64_t k, int nbits, int group,
+                           uint8_t* packed, void* scale_out, uint8_t* zp_out, uint8_t* codes_out) {
     const int qmin = 0, qmax = (1 << nbits) - 1;
     const float eps = 0x1p-23f; /* torch.finfo(torch.float32).eps */
     int64_t groups = k / group;
     uint8_t* codes = (uint8_t*)malloc((size_t)(n * k));
     for (int64_t r = 0; r < n; ++r) {
         for (int64_t gi = 0; gi < groups; ++gi) {
-            const uint16_t* wg = w + r * k + gi * group;
+            const int64_t g0 = r * k + gi * group;
             float mn = INFINITY, mx = -INFINITY;
             for (int j = 0; j < group; ++j) {
-                float x = orc_bf16_to_f32(wg[j]);
+                float x = load_dt(w, g0 + j, dt);
                 mn = fminf(mn, x);
                 mx = fmaxf(mx, x);
             }
             float mn_neg = fminf(mn, 0.0f), mx_pos = fmaxf(mx, 0.0f);
-            float sc = bf(mx_pos - mn_neg);
-            sc = bf(sc / (float)(qmax - qmin));
-            sc = fmaxf(sc, eps);
-            float ratio = bf(mn_neg / sc);
-            float zpf = bf((float)qmin - rne(ratio));
+            float sc = r_dt(mx_pos - mn_neg, dt);
+            sc = r_dt(sc / (float)(qmax - qmin), dt);
+            sc = fmaxf(sc, eps); /* eps is exact in bf16, binary16 and binary32 */
+            float ratio = r_dt(mn_neg / sc, dt);
+            float zpf = r_dt((float)qmin - rne(ratio), dt);
             zpf = clampf(zpf, (float)qmin, (float)qmax);
             int zp = (int)zpf;
-            float inv = bf(1.0f / sc);
+            float inv = r_dt(1.0f / sc, dt);
             for (int j = 0; j < group; ++j) {
-                float x = orc_bf16_to_f32(wg[j]);
-                float p = bf(x * inv);
-                float q = bf(rne(p) + (float)zp);
+                float x = load_dt(w, g0 + j, dt);
+                float p = r_dt(x * inv, dt);
+                float q = r_dt(rne(p) + (float)zp, dt);
                 q = clampf(q, (float)qmin, (float)qmax);
-                codes[r * k + gi * group + j] = (uint8_t)q;
+                codes[g0 + j] = (uint8_t)q;
             }
-            scale_out[r * groups + gi] = orc_f32_to_bf16(sc);
+            store_dt(scale_out, r * groups + gi, dt, sc);
             zp_out[r * groups + gi] = (uint8_t)zp;
         }
     }
@@ -590,20 +612,30 @@ void orc_uintx_quantize(const uint16_t* w, int64_t n, int64_t k, int nbits, int 
     free(codes);
 }
 
-/* UIntXQuantizer._dequantize_native: q from the shards, then in bf16
- * (bf16(q) - bf16(zp)) * scale.  out_bf16 is [n, k] bf16. */
-void orc_uintx_dequantize(const uint8_t* packed, const uint16_t* scale, const uint8_t* zp,
-                          int64_t n, int64_t k, int nbits, int group, uint16_t* out_bf16) {
+void orc_uintx_quantize(const uint16_t* w, int64_t n, int64_t k, int nbits, int group,
+                        uint8_t* packed, uint16_t* scale_out, uint8_t* zp_out,
+                        uint8_t* codes_out) {
+    orc_uintx_quantize_dt(w, 1, n, k, nbits, group, packed, scale_out, zp_out, codes_out);
+}
+
+/* _dequantize_native: (q - zp) then times the scale, both in dt. */
+void orc_uintx_dequantize_dt(const uint8_t* packed, const void* scale, int dt, const uint8_t* zp,
+                             int64_t n, int64_t k, int nbits, int group, void* out) {
     int64_t groups = k / group;
     uint8_t* codes = (uint8_t*)malloc((size_t)(n * k));
     orc_uintx_unpack(packed, n * k, nbits, codes);
     for (int64_t r = 0; r < n; ++r)
         for (int64_t c = 0; c < k; ++c) {
             int64_t gi = r * groups + c / group;
-            float sc = orc_bf16_to_f32(scale[gi]);
-            float d = bf((float)codes[r * k + c] - (float)zp[gi]);
-            d = bf(d * sc);
-            out_bf16[r * k + c] = orc_f32_to_bf16(d);
+            float sc = load_dt(scale, gi, dt);
+            float d = r_dt((float)codes[r * k + c] - (float)zp[gi], dt);
+            d = r_dt(d * sc, dt);
+            store_dt(out, r * k + c, dt, d);
         }
     free(codes);
+}
+
+void orc_uintx_dequantize(const uint8_t* packed, const uint16_t* scale, const uint8_t* zp,
+                          int64_t n, int64_t k, int nbits, int group, uint16_t* out_bf16) {
+    orc_uintx_dequantize_dt(packed, scale, 1, zp, n, k, nbits, group, out_bf16);
 }

@@ -54,6 +54,10 @@ void orc_awq_fold(const uint16_t* w, int64_t n, int64_t k, const float* s, int a
 int64_t orc_uintx_packed_bytes(int64_t numel, int nbits);
 void orc_uintx_pack(const uint8_t* codes, int64_t numel, int nbits, uint8_t* out);
 void orc_uintx_unpack(const uint8_t* packed, int64_t numel, int nbits, uint8_t* codes);
+void orc_uintx_quantize_dt(const void* w, int dt, int64_t n, int64_t k, int nbits, int group,
+                           uint8_t* packed, void* scale_out, uint8_t* zp_out, uint8_t* codes_out);
+void orc_uintx_dequantize_dt(const uint8_t* packed, const void* scale, int dt, const uint8_t* zp,
+                             int64_t n, int64_t k, int nbits, int group, void* out);
 void orc_uintx_quantize(const uint16_t* w, int64_t n, int64_t k, int nbits, int group,
                         uint8_t* packed, uint16_t* scale_out, uint8_t* zp_out, uint8_t* codes_out);
 void orc_uintx_dequantize(const uint8_t* packed, const uint16_t* scale, const uint8_t* zp,

@@ -780,3 +780,55 @@ def test_gptq_f32_path_equals_bf16_path_on_bf16_values():
         a = oracle.gptq_quantize(w, 64, sym)
         b = oracle.gptq_quantize_f32(oracle.bf16_bits_to_f32(oracle._u16(w)), 64, sym)
         assert all(np.array_equal(x, y) for x, y in zip(a[:4], b[:4])) and a[4] == b[4]
+
+
+# ---------------------------------------------------------------- uintx in the weight dtype
+# uintx_quant.py works in the weight's own dtype.  Pins for binary16 and binary32:
+# a hand-worked group whose every step is exact in all three types, and a
+# cross-check of the oracle's C rounding against numpy's own float16 / float32
+# arithmetic (each numpy op on those dtypes is the binary32 op rounded once to
+# the dtype, the reading the oracle follows).
+def test_uintx_dt_hand_group():
+    vals = [-1.25, 2.5, 0.5, 0.375, -0.625, 1.0, 0.0, 0.125]
+    # min_neg -1.25, max_pos 2.5: scale 3.75/15 = 0.25, 1/scale = 4, zp = 0 - round(-5) = 5
+    # w * 4 = -5, 10, 2, 1.5, -2.5, 4, 0, 0.5 -> round half even -5, 10, 2, 2, -2, 4, 0, 0 -> + 5
+    codes = [0, 15, 7, 7, 3, 9, 5, 5]
+    for dt, npt in ((0, np.float32), (2, np.float16)):
+        w = np.asarray([vals] * 2, npt)
+        arr = w if dt == 0 else w.view(np.uint16)
+        packed, sc, zp, c = oracle.uintx_quantize_dt(arr, dt, 4, 8)
+        assert c.tolist() == [codes] * 2 and zp.tolist() == [[5], [5]]
+        assert (sc.view(npt) if dt else sc).tolist() == [[0.25], [0.25]]
+        d = oracle.uintx_dequantize_dt(packed, sc, dt, zp, 2, 8, 4, 8)
+        d = d if dt == 0 else d.view(np.float16).astype(np.float32)
+        assert d[0].tolist() == [-1.25, 2.5, 0.5, 0.5, -0.5, 1.0, 0.0, 0.0]
+
+
+def _numpy_uintx(w, nbits, group):
+    T = w.dtype.type
+    n, k = w.shape
+    qmax = (1 << nbits) - 1
+    wg = w.reshape(n, k // group, group)
+    mn = np.minimum(wg.min(axis=2), T(0))
+    mx = np.maximum(wg.max(axis=2), T(0))
+    sc = np.maximum((mx - mn) / T(qmax), T(np.finfo(np.float32).eps))
+    zp = np.clip(T(0) - np.round(mn / sc), 0, qmax)
+    inv = T(1) / sc
+    q = np.clip(np.round(wg * inv[..., None]) + zp[..., None], 0, qmax)
+    deq = (q - zp[..., None]) * sc[..., None]
+    return q.reshape(n, k).astype(np.uint8), sc, zp.astype(np.uint8), deq.reshape(n, k)
+
+
+@pytest.mark.parametrize("nbits", [2, 3, 5, 7])
+def test_uintx_dt_matches_numpy_dtype_arithmetic(nbits):
+    rng = np.random.default_rng(70 + nbits)
+    base = rng.standard_normal((24, 256)) * np.exp(rng.standard_normal((24, 1)))
+    for dt, npt in ((0, np.float32), (2, np.float16)):
+        w = (base * 0.05).astype(npt)
+        arr = w if dt == 0 else w.view(np.uint16)
+        packed, sc, zp, codes = oracle.uintx_quantize_dt(arr, dt, nbits, 64)
+        q_ref, sc_ref, zp_ref, deq_ref = _numpy_uintx(w, nbits, 64)
+        assert np.array_equal(codes, q_ref) and np.array_equal(zp, zp_ref)
+        assert np.array_equal(sc.view(npt) if dt else sc, sc_ref)
+        d = oracle.uintx_dequantize_dt(packed, sc, dt, zp, 24, 256, nbits, 64)
+        assert np.array_equal(d.view(npt) if dt else d, deq_ref.astype(npt))
