@@ -362,6 +362,19 @@ wq_status uintx_dequantize(const uint8_t* packed, const uint16_t* scale, const u
                            int64_t n, int64_t k, int nbits, int group, int out_dtype, void* out,
                            void* stream);
 
+/* uintx_quantize_ex / uintx_dequantize_ex (uintx_quant.py works in the weight's
+ * own dtype) -- uintx_quantize / uintx_dequantize for a weight of type w_dtype:
+ * WQ_DTYPE_BF16 calls those entry points; WQ_DTYPE_F16 and WQ_DTYPE_F32 do every
+ * op in that type (the binary32 op rounded once to fp16; fp32 ops as they are).
+ * scale has the weight's type ([n, k/group]); the dequantized output too.  The
+ * group is any multiple of 8 that divides k.  w, scale and out need their
+ * element alignment only.  Results are unspecified where 1/scale overflows the
+ * type (groups of fp16 values spanning less than about 15 * 2^-16). */
+wq_status uintx_quantize_ex(const void* w, int w_dtype, int64_t n, int64_t k, int nbits, int group,
+                            uint8_t* packed, void* scale, uint8_t* zp, void* stream);
+wq_status uintx_dequantize_ex(const uint8_t* packed, const void* scale, int w_dtype, const uint8_t* zp,
+                              int64_t n, int64_t k, int nbits, int group, void* out, void* stream);
+
 /* ---------------------------------------------------------------- SNR
  * quant_snr (export_gptq_cpu.py quantize_* snr; quantize_dflash_mxfp4.py main()
  * relative error): over the whole tensor, Sw = sum w^2, Se = sum (w - deq)^2 with

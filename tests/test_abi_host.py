@@ -150,6 +150,16 @@ def test_wide_quantize_argument_errors(L):
     assert L.mxfp4_quantize_ex(MIS, 0, 64, 64, 0, BAD, BAD, None) == 4
     assert L.mxfp4_quantize_ex(None, 2, 0, 64, 0, None, None, None) == 0
     assert ws  # (the SNR workspace size is the bf16 path's)
+    assert L.uintx_quantize_ex(BAD, 7, 8, 64, 4, 64, BAD, BAD, BAD, None) == 3
+    assert L.uintx_quantize_ex(BAD, 0, 8, 64, 8, 64, BAD, BAD, BAD, None) == 5     # nbits 8
+    assert L.uintx_quantize_ex(BAD, 2, 8, 64, 4, 12, BAD, BAD, BAD, None) == 2     # group % 8
+    assert L.uintx_quantize_ex(BAD, 0, 8, 64, 4, 48, BAD, BAD, BAD, None) == 2     # k % group
+    assert L.uintx_quantize_ex(BAD, 0, 8, 64, 4, 64, None, BAD, BAD, None) == 1
+    assert L.uintx_quantize_ex(MIS, 0, 8, 64, 4, 64, BAD, BAD, BAD, None) == 4     # fp32 needs 4-byte
+    assert L.uintx_quantize_ex(None, 2, 0, 64, 4, 64, None, None, None, None) == 0
+    assert L.uintx_dequantize_ex(BAD, BAD, 7, BAD, 8, 64, 4, 64, BAD, None) == 3
+    assert L.uintx_dequantize_ex(BAD, BAD, 2, BAD, 8, 64, 1, 64, BAD, None) == 5
+    assert L.uintx_dequantize_ex(BAD, BAD, 0, BAD, 8, 64, 4, 64, None, None) == 1
 
 
 def test_mxfp4_linear_argument_errors(L):

@@ -99,3 +99,23 @@ def test_mxfp4_wide_dequant_round_trip_and_consumer():
     p, e = wq.mxfp4_quantize(w.to(DEV))
     d = wq.mxfp4_dequantize(p, e).cpu().numpy()
     assert np.array_equal(d, oracle.mxfp4_dequantize(*oracle.mxfp4_quantize_f32(w.numpy())))
+
+
+# ------------------------------------------------------------------ uintx in the weight dtype
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16])
+@pytest.mark.parametrize("nbits", [2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("shape,group", [((37, 192), 64), ((37, 192), 24), ((256, 1024), 32)])
+def test_uintx_wide(dtype, nbits, shape, group):
+    n, k = shape
+    w = f32_weight(n, k, 60 + nbits, dtype)
+    packed, sc, zp = wq.uintx_quantize(w.to(DEV), nbits, group)
+    dt = 0 if dtype == torch.float32 else 2
+    rp, rs, rz, _ = oracle.uintx_quantize_dt(w, dt, nbits, group)
+    bits = (lambda t: t.cpu().numpy()) if dt == 0 else (lambda t: t.cpu().view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(packed.cpu().numpy(), rp), "packed"
+    assert np.array_equal(bits(sc), rs), "scale"
+    assert np.array_equal(zp.cpu().numpy(), rz), "zp"
+    d = wq.uintx_dequantize(packed, sc, zp, n, k, nbits, group)
+    assert d.dtype == dtype
+    assert np.array_equal(bits(d), oracle.uintx_dequantize_dt(rp, rs, dt, rz, n, k, nbits, group)), "deq"
+    assert wq.device_status() == 0

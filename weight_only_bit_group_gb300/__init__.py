@@ -96,6 +96,8 @@ def lib():
                 "gptq_gemm": (I, [P, I64, P, P, P, I64, I64, I, I, I, P, P]),
                 "gptq_quantize_ex": (I, [P, I, I64, I64, I, I, P, P, P, P, P, P, SZ, P]),
                 "mxfp4_quantize_ex": (I, [P, I, I64, I64, I, P, P, P]),
+                "uintx_quantize_ex": (I, [P, I, I64, I64, I, I, P, P, P, P]),
+                "uintx_dequantize_ex": (I, [P, P, I, P, I64, I64, I, I, P, P]),
                 "uintx_gemm": (I, [P, I64, P, P, P, I64, I64, I, I, I, P, P]),
             }
             for name, (res, args) in sig.items():
@@ -257,20 +259,35 @@ def uintx_packed_bytes(numel: int, nbits: int) -> int:
 
 
 def uintx_quantize(w, nbits, group=64, *, packed=None, scale=None, zp=None):
-    """uintx_quant.py _quantize_impl + pack_uintx -> (packed u8, scale bf16 [N,K/g], zp u8)."""
-    _u16(w)
+    """uintx_quant.py _quantize_impl + pack_uintx -> (packed u8, scale [N,K/g] in the weight's
+    dtype, zp u8).  w: bf16, fp16 or fp32 [N, K]; the arithmetic runs in that dtype."""
+    wide = w.dtype in (torch.float32, torch.float16)
+    if not wide:
+        _u16(w)
+    assert w.is_contiguous(), "tensor must be contiguous"
     n, k = w.shape
     packed = _empty((uintx_packed_bytes(n * k, nbits),), torch.uint8, w) if packed is None else packed
-    scale = _empty((n, k // group), torch.bfloat16, w) if scale is None else scale
+    scale = _empty((n, k // group), w.dtype if wide else torch.bfloat16, w) if scale is None else scale
     zp = _empty((n, k // group), torch.uint8, w) if zp is None else zp
-    st = lib().uintx_quantize(_ptr(w), n, k, nbits, group, _ptr(packed), _ptr(scale), _ptr(zp),
-                              _stream(w.device))
+    if wide:
+        st = lib().uintx_quantize_ex(_ptr(w), _WIDE[w.dtype], n, k, nbits, group, _ptr(packed), _ptr(scale),
+                                     _ptr(zp), _stream(w.device))
+    else:
+        st = lib().uintx_quantize(_ptr(w), n, k, nbits, group, _ptr(packed), _ptr(scale), _ptr(zp),
+                                  _stream(w.device))
     _check(st, "uintx_quantize")
     return packed, scale, zp
 
 
 def uintx_dequantize(packed, scale, zp, n, k, nbits, group=64, out_dtype=torch.bfloat16, *,
                      out=None):
+    """_dequantize_native.  A bf16 scale gives bf16 (or its exact binary32 widening,
+    out_dtype); an fp16 / fp32 scale computes and returns in that dtype."""
+    if scale.dtype in (torch.float32, torch.float16):
+        out = torch.empty((n, k), dtype=scale.dtype, device=packed.device) if out is None else out
+        _check(lib().uintx_dequantize_ex(_ptr(packed), _ptr(scale), _WIDE[scale.dtype], _ptr(zp), n, k, nbits,
+                                         group, _ptr(out), _stream(packed.device)), "uintx_dequantize_ex")
+        return out
     dt = WQ_DTYPE_BF16 if out_dtype == torch.bfloat16 else WQ_DTYPE_F32
     out = _empty((n, k), out_dtype, packed) if out is None else out
     st = lib().uintx_dequantize(_ptr(packed), _ptr(scale), _ptr(zp), n, k, nbits, group, dt,
