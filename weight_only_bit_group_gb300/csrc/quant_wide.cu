@@ -5,8 +5,10 @@
 // the same binary32 arithmetic as a bf16 one, only with more significant bits,
 // so the shortcuts of the bf16 kernels (exact bf16x2 max/min, exact squares)
 // do not apply and these kernels take each binary32 step as written: IEEE
-// divisions, round half to even, compensated sums of the rounded squares for
-// the SNR.  bf16 weights go to the tuned bf16 kernels.
+// divisions (per element as a correctly rounded reciprocal plus one FMA
+// correction, which gives the same quotient), round half to even, compensated
+// sums of the rounded squares for the SNR.  bf16 weights go to the tuned bf16
+// kernels.
 #include <cuda_fp16.h>
 
 #include "wq_common.cuh"
@@ -74,14 +76,20 @@ gptq_quant_wide_kernel(const void* __restrict__ w, int64_t n, int64_t k, int G, 
             z = fminf(fmaxf(rintf(__fdiv_rn(-wmin, s)), 0.0f), 15.0f);      // (-wmin / s).round().clamp
         }
         if (!valid) s = 1.0f, z = 8.0f;
-        // codes, packed 8 per word along K (low nibble first)
+        // codes, packed 8 per word along K (low nibble first).  x / s as the
+        // correctly rounded reciprocal plus one FMA correction (exact while s,
+        // 1/s and the quotient are normal; a subnormal quotient rounds to code zp
+        // either way); IEEE division for scales above 2^100.
+        const bool fast = s <= 0x1p100f;
+        const float rs = __frcp_rn(s);
         if (valid) {
             for (int j = 0; j < G; j += 8) {
                 load8<DT>(w, row0 + j, v);
                 uint32_t word = 0;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float q = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(v[i], s)), z), 0.0f), 15.0f);
+                    const float qt = fast ? wq::div_by_recip(v[i], s, rs) : __fdiv_rn(v[i], s);
+                    const float q = fminf(fmaxf(__fadd_rn(rintf(qt), z), 0.0f), 15.0f);
                     word |= (uint32_t)q << (4 * i);
                     if (SNR) {
                         const float e = __fsub_rn(v[i], __fmul_rn(__fsub_rn(q, z), s));
