@@ -444,12 +444,13 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             const int s = kb % NS;
             const uint32_t zp = (zw >> (4 * (nrow & 7))) & 15u;
             const uint32_t zb2 = (0x4300u + zp) * 0x10001u;  // bf16x2 of 128 + zp
-            const uint32_t qsrc = (uint32_t)__cvta_generic_to_shared(q_at(s)) + (uint32_t)((4 * h * BM + r) * 4);
+            // plain shared-memory accesses: the compiler may interleave the rows'
+            // loads, arithmetic and stores (the proxy fence below orders them)
+            const uint32_t* qsrc = reinterpret_cast<const uint32_t*>(q_at(s)) + 4 * h * BM + r;
             uint32_t w[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[j]) : "r"(qsrc + j * BM * 4) : "memory");
-            const uint32_t arow = a_at(s) + r * 128;
+            for (int j = 0; j < 4; ++j) w[j] = qsrc[j * BM];
+            uint8_t* arow = smem + (a_at(s) - sbase) + r * 128;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t t0n = w[j] & 0x0F0F0F0Fu, t1n = (w[j] >> 4) & 0x0F0F0F0Fu;
@@ -460,10 +461,7 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 const uint32_t d1 = wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4342), zb2);
                 const uint32_t d2 = wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4140), zb2);
                 const uint32_t d3 = wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4342), zb2);
-                const uint32_t dst = arow + (uint32_t)(((4 * h + j) ^ (r & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(d0), "r"(d1),
-                             "r"(d2), "r"(d3)
-                             : "memory");
+                *reinterpret_cast<uint4*>(arow + (((4 * h + j) ^ (r & 7)) << 4)) = make_uint4(d0, d1, d2, d3);
             }
         };
         uint32_t za = zword(0), zb = zword(1);
