@@ -11,14 +11,18 @@
 // group, in group order.  No bf16-rounded weight is ever formed.
 //
 // One CTA computes 128 output features x 128 tokens over all of K:
-//   warps 0-7   dequant: raw qweight rows (TMA) -> (code - zp) bf16 written into
-//               the 128-byte-swizzled K-major A tile (two threads per feature row)
+//   warps 0-7   dequant: raw qweight rows (TMA) -> (code - zp) bf16, stored by
+//               tcgen05.st straight into TMEM as the MMA's A operand (lane =
+//               feature row, two K values per column; two threads per row)
 //   warps 8-15  epilogue: two warpgroups (token columns 0-63 / 64-127), one
 //               feature row per thread, tcgen05.ld of each group's partial
 //   warp 16     TMA: x tile [128 tokens x 64] (128-byte swizzle) and qweight
 //               rows [8 x 128 features]; owns the TMEM allocation
-//   warp 17     MMA: one thread issues tcgen05.mma (M 128, N 128, K 16) per
-//               16 values of K, commits to the stage and group barriers
+//   warp 17     MMA: one thread issues tcgen05.mma (A from TMEM, x from shared
+//               memory; M 128, N 128, K 16) per 16 values of K, commits to the
+//               stage and group barriers
+// Keeping A out of shared memory matters: an N = 128 MMA reading both operands
+// from shared memory uses all of its bandwidth by itself.
 // Every wait is bounded; on a timeout the CTA records WQ_ERR_DEVICE_TIMEOUT in
 // the device status word, lets its copies and MMAs land, frees TMEM and returns.
 #include <cuda.h>
@@ -34,11 +38,10 @@ namespace {
 constexpr int BM = 128;                    // output features per CTA (MMA M)
 constexpr int BT = 128;                    // tokens per CTA (MMA N)
 constexpr int BK = 64;                     // K per pipeline stage
-constexpr int NS = 6;                      // pipeline stages
+constexpr int NS = 8;                      // pipeline stages
 constexpr int X_BYTES = BT * BK * 2;       // x tile, bf16, 128-byte swizzle
-constexpr int A_BYTES = BM * BK * 2;       // (code - zp) tile, bf16, same layout
 constexpr int Q_BYTES = (BK / 8) * BM * 4; // raw qweight rows
-constexpr int STAGE = X_BYTES + A_BYTES + Q_BYTES;
+constexpr int STAGE = X_BYTES + Q_BYTES;    // the A operand lives in TMEM
 constexpr int BAR_OFF = NS * STAGE;
 // barriers: full[NS] aready[NS] empty[NS] tfull[2] tempty[2] done; then the TMEM
 // address slot and the abort flag
@@ -51,9 +54,14 @@ constexpr int TMA_WARP = EPI_WARP0 + 8;
 constexpr int MMA_WARP = TMA_WARP + 1;
 constexpr int THREADS = (MMA_WARP + 1) * 32;
 constexpr int kBand = 8;                   // token tiles per rasterisation band
-constexpr int TMEM_COLS = 2 * BT;          // two group accumulators
+// TMEM: two group accumulators (columns 0 .. 2 BT - 1), then the dequantized
+// A operand of each stage (BK / 2 columns: two bf16 per 32-bit column, lane =
+// feature row)
+constexpr int A_COL0 = 2 * BT;
+constexpr int TMEM_COLS = 512;
 constexpr uint32_t kSpin = 1u << 22;
-static_assert(STAGE % 1024 == 0 && X_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms");
+static_assert(STAGE % 1024 == 0 && X_BYTES % 1024 == 0, "swizzle atoms");
+static_assert(A_COL0 + NS * (BK / 2) <= TMEM_COLS, "TMEM columns");
 
 __device__ unsigned g_gemm_status;
 
@@ -84,6 +92,27 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T: A's rows in TMEM lanes, two bf16 of K per
+// 32-bit column.
+__device__ __forceinline__ void tc_mma_ta(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// 16 consecutive 32-bit columns of this warp's 32 TMEM lanes from registers.
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // Arrive once on the mbarrier when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -192,8 +221,7 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     uint8_t* smem = smem_raw + pad;
     const uint32_t sbase = raw + pad;
     auto x_at = [&](int s) { return sbase + s * STAGE; };
-    auto a_at = [&](int s) { return sbase + s * STAGE + X_BYTES; };
-    auto q_at = [&](int s) { return smem + s * STAGE + X_BYTES + A_BYTES; };
+    auto q_at = [&](int s) { return smem + s * STAGE + X_BYTES; };
     const uint32_t bar0 = sbase + BAR_OFF;
     auto full = [&](int s) { return bar0 + 8 * s; };
     auto aready = [&](int s) { return bar0 + 8 * (NS + s); };
@@ -268,14 +296,15 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         // compile-time masks of the K-step index and the descriptors advance by
         // constant offsets (no division, no recomputation).
         if (lane == 0) {
-            const uint64_t da0 = sw128_desc(a_at(0)), db0 = sw128_desc(x_at(0));
-            // issue MMAs for K steps [ks0, ks1) of stage descriptors (da, db) into
-            // accumulator b; the first one starts the accumulator when `fresh`
-            auto mmas = [&](uint64_t da, uint64_t db, uint32_t b, int ks0, int ks1, bool fresh) {
+            const uint64_t db0 = sw128_desc(x_at(0));
+            // issue MMAs for K steps [ks0, ks1) of a stage (A columns da in TMEM, x
+            // descriptor db) into accumulator b; the first one starts the
+            // accumulator when `fresh`
+            auto mmas = [&](uint32_t da, uint64_t db, uint32_t b, int ks0, int ks1, bool fresh) {
 #pragma unroll
                 for (int ks = ks0; ks < ks1; ++ks)
-                    tc_mma(tmem + b * BT, da + (uint64_t)(ks * 2), db + (uint64_t)(ks * 2), kIdesc,
-                           (fresh && ks == ks0) ? 0u : 1u);
+                    tc_mma_ta(tmem + b * BT, da + (uint32_t)(ks * 8), db + (uint64_t)(ks * 2), kIdesc,
+                              (fresh && ks == ks0) ? 0u : 1u);
             };
             bool ok = true;
             for (int kb = 0; kb < nkb && ok; ++kb) {
@@ -283,7 +312,8 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 const uint32_t par = (uint32_t)(kb / NS) & 1u;
                 if (!wait_bar(full(s), par, abort_flag) || !wait_bar(aready(s), par, abort_flag)) break;
                 tc_fence_after();
-                const uint64_t da = da0 + (uint64_t)((s * STAGE) >> 4), db = db0 + (uint64_t)((s * STAGE) >> 4);
+                const uint32_t da = tmem + (uint32_t)(A_COL0 + s * (BK / 2));
+                const uint64_t db = db0 + (uint64_t)((s * STAGE) >> 4);
                 if constexpr (UX != 0) {
                     // one accumulator over all of K
                     mmas(da, db, 0u, 0, BK / 16, kb == 0);
@@ -399,7 +429,7 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             if (!warp_wait(full(s), (uint32_t)(kb / NS) & 1u, abort_flag)) break;
             const uint32_t zb2 = (0x4300u + cur.zp) * 0x10001u;  // bf16x2 of 128 + zp
             const uint32_t sc2 = cur.sc * 0x10001u;              // bf16x2 of the scale
-            const uint32_t arow = a_at(s) + r * 128;
+            uint32_t dv[16];  // this thread's 16 TMEM columns of the stage's A
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 uint64_t q = 0;  // eight code bytes
@@ -411,16 +441,15 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 const uint32_t lo = (uint32_t)q, hi = (uint32_t)(q >> 32);
                 // bf16 of 128 + q, minus 128 + zp (exact), times the scale: the
                 // page's bf16 sub and bf16 multiply, each rounded once
-                const uint32_t d0 = wq::bmul2(wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4140), zb2), sc2);
-                const uint32_t d1 = wq::bmul2(wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4342), zb2), sc2);
-                const uint32_t d2 = wq::bmul2(wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4140), zb2), sc2);
-                const uint32_t d3 = wq::bmul2(wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4342), zb2), sc2);
-                const uint32_t dst = arow + (uint32_t)(((4 * h + j) ^ (r & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(d0), "r"(d1),
-                             "r"(d2), "r"(d3)
-                             : "memory");
+                dv[4 * j + 0] = wq::bmul2(wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4140), zb2), sc2);
+                dv[4 * j + 1] = wq::bmul2(wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4342), zb2), sc2);
+                dv[4 * j + 2] = wq::bmul2(wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4140), zb2), sc2);
+                dv[4 * j + 3] = wq::bmul2(wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4342), zb2), sc2);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_st16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(A_COL0 + s * (BK / 2) + 16 * h), dv);
+            // the stores land before the MMA thread is told the stage is ready
+            tc_wait_st();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(aready(s));
         }
@@ -444,25 +473,24 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             const int s = kb % NS;
             const uint32_t zp = (zw >> (4 * (nrow & 7))) & 15u;
             const uint32_t zb2 = (0x4300u + zp) * 0x10001u;  // bf16x2 of 128 + zp
-            // plain shared-memory accesses: the compiler may interleave the rows'
-            // loads, arithmetic and stores (the proxy fence below orders them)
             const uint32_t* qsrc = reinterpret_cast<const uint32_t*>(q_at(s)) + 4 * h * BM + r;
             uint32_t w[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) w[j] = qsrc[j * BM];
-            uint8_t* arow = smem + (a_at(s) - sbase) + r * 128;
+            // column 16h + 4j + i of the stage's A holds K values 2i, 2i+1 of word j
+            uint32_t dv[16];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t t0n = w[j] & 0x0F0F0F0Fu, t1n = (w[j] >> 4) & 0x0F0F0F0Fu;
                 const uint32_t lo = __byte_perm(t0n, t1n, 0x5140);  // codes 0..3 as bytes
                 const uint32_t hi = __byte_perm(t0n, t1n, 0x7362);  // codes 4..7
                 // bytes c | 0x43 << 8 = bf16 of 128 + c; minus 128 + zp is exact
-                const uint32_t d0 = wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4140), zb2);
-                const uint32_t d1 = wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4342), zb2);
-                const uint32_t d2 = wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4140), zb2);
-                const uint32_t d3 = wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4342), zb2);
-                *reinterpret_cast<uint4*>(arow + (((4 * h + j) ^ (r & 7)) << 4)) = make_uint4(d0, d1, d2, d3);
+                dv[4 * j + 0] = wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4140), zb2);
+                dv[4 * j + 1] = wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4342), zb2);
+                dv[4 * j + 2] = wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4140), zb2);
+                dv[4 * j + 3] = wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4342), zb2);
             }
+            tc_st16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(A_COL0 + s * (BK / 2) + 16 * h), dv);
         };
         uint32_t za = zword(0), zb = zword(1);
         for (int kb = 0; kb < nkb; kb += 2) {
@@ -474,8 +502,9 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             zb = zword(kb + 3);
             convert(kb, zcur_a);
             if (two) convert(kb + 1, zcur_b);
-            // generic-proxy writes become visible to the tensor cores' reads
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // the TMEM stores land before the MMA thread is told the stages are ready
+            tc_wait_st();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(aready(kb % NS));
