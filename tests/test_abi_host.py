@@ -175,3 +175,18 @@ def test_empty_inputs_are_ok_without_gpu(L):
     assert L.mxfp4_quantize(None, 0, 64, 0, None, None, None) == 0
     assert L.uintx_dequantize(None, None, None, 3, 0, 4, 64, 1, None, None) == 0
     assert L.gptq_dequantize(None, None, None, 0, 128, 128, 1, 0, 0, None, None) == 0
+
+
+def test_consumers_refuse_non_bf16_operands():
+    import torch
+
+    x16 = torch.zeros(2, 64, dtype=torch.float16)
+    for call in (lambda: wq.gptq_gemm(x16, None, None, None, 64, 64),
+                 lambda: wq.gptq_linear(x16, None, None, None, 64, 64),
+                 lambda: wq.mxfp4_linear(x16, torch.zeros(64, 32, dtype=torch.uint8), None),
+                 lambda: wq.uintx_gemm(x16, None, None, None, 64, 64, 4)):
+        with pytest.raises(TypeError):
+            call()
+    with pytest.raises(TypeError):
+        wq.uintx_gemm(torch.zeros(2, 64, dtype=torch.bfloat16), None,
+                      torch.zeros(64, 1, dtype=torch.float16), None, 64, 64, 4)

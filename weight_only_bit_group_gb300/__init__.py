@@ -127,6 +127,15 @@ def _u16(t: torch.Tensor) -> torch.Tensor:
     return t
 
 
+def _bf16(t: torch.Tensor, what: str) -> torch.Tensor:
+    """A bf16 operand (activations, bf16 scales): other 16-bit types would be read as
+    bf16 bit patterns, so they are refused here."""
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{what} must be bfloat16, got {t.dtype}")
+    assert t.is_contiguous(), f"{what} must be contiguous"
+    return t
+
+
 def _empty(shape, dtype, like):
     return torch.empty(shape, dtype=dtype, device=like.device)
 
@@ -301,7 +310,7 @@ def gptq_linear(x, qweight, qzeros, scales, n, k, group=128, sym=True, out_dtype
                 *, out=None, ws=None):
     """y = x deq(W)^T for a decode batch (x bf16 [m, k], 1 <= m <= 8) straight from
     the GPTQ tensors; y binary32 or bf16 [m, n]."""
-    _u16(x)
+    _bf16(x, "x")
     x2 = x.view(1, -1) if x.dim() == 1 else x
     m = x2.shape[0]
     dt = WQ_DTYPE_BF16 if out_dtype == torch.bfloat16 else WQ_DTYPE_F32
@@ -320,7 +329,7 @@ def gptq_gemm(x, qweight, qzeros, scales, n, k, group=128, sym=True, out_dtype=t
               *, out=None):
     """y = x deq(W)^T on the tensor cores for prefill batches (x bf16 [m, k], any
     m >= 1) straight from the GPTQ tensors; y binary32 or bf16 [m, n]."""
-    _u16(x)
+    _bf16(x, "x")
     x2 = x.view(1, -1) if x.dim() == 1 else x
     m = x2.shape[0]
     dt = WQ_DTYPE_BF16 if out_dtype == torch.bfloat16 else WQ_DTYPE_F32
@@ -334,7 +343,8 @@ def gptq_gemm(x, qweight, qzeros, scales, n, k, group=128, sym=True, out_dtype=t
 def uintx_gemm(x, packed, scale, zp, n, k, nbits, group=64, out_dtype=torch.float32, *, out=None):
     """uintx_quant.py forward on the tensor cores: y = x deq(W)^T with deq the
     page's bf16 values (x bf16 [m, k], any m >= 1); y binary32 or bf16 [m, n]."""
-    _u16(x)
+    _bf16(x, "x")
+    _bf16(scale, "scale (uintx_gemm takes the bf16 weights' scales)")
     x2 = x.view(1, -1) if x.dim() == 1 else x
     m = x2.shape[0]
     dt = WQ_DTYPE_BF16 if out_dtype == torch.bfloat16 else WQ_DTYPE_F32
@@ -348,7 +358,7 @@ def uintx_gemm(x, packed, scale, zp, n, k, nbits, group=64, out_dtype=torch.floa
 def mxfp4_linear(x, packed, e8m0, out_dtype=torch.float32, *, out=None):
     """y = x deq(W)^T for a decode batch (x bf16 [m, k], 1 <= m <= 8) straight from
     the MXFP4 codes [n, k/2] and E8M0 bytes [n, k/32]; y binary32 or bf16 [m, n]."""
-    _u16(x)
+    _bf16(x, "x")
     x2 = x.view(1, -1) if x.dim() == 1 else x
     m, k = x2.shape
     n = packed.shape[0]

@@ -59,7 +59,6 @@ constexpr int kBand = 8;                   // token tiles per rasterisation band
 // feature row)
 constexpr int A_COL0 = 2 * BT;
 constexpr int TMEM_COLS = 512;
-constexpr uint32_t kSpin = 1u << 22;
 static_assert(STAGE % 1024 == 0 && X_BYTES % 1024 == 0, "swizzle atoms");
 static_assert(A_COL0 + NS * (BK / 2) <= TMEM_COLS, "TMEM columns");
 
@@ -81,16 +80,6 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 operands, binary32 accumulator.
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
 }
 // D[tmem] (+)= A[tmem] * B[smem]^T: A's rows in TMEM lanes, two bf16 of K per
 // 32-bit column.
@@ -214,7 +203,6 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                  const int32_t* __restrict__ qzeros, const uint16_t* __restrict__ scales, int m, int n,
                  int k, void* __restrict__ out, const uint8_t* __restrict__ ux_packed,
                  const uint8_t* __restrict__ ux_zp, int ux_group) {
-    constexpr int KPG = G / 16;  // MMA K-steps per group (a power of two)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
