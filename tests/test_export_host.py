@@ -115,3 +115,90 @@ def test_cli_requires_arguments():
         export.main(["gptq"])
     with pytest.raises(SystemExit):
         export.main([])
+
+
+# ------------------------------------------------------------------ exporter logic on the CPU
+# The exporters' host logic (q_k_v split, suffix selection, lm_head untie, report,
+# config, the AWQ fold order) run with the kernel calls replaced by oracle-backed
+# stand-ins: what is written must then equal the oracle composition exactly.
+import oracle  # noqa: E402
+
+
+@pytest.fixture
+def oracle_kernels(monkeypatch):
+    def bits(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(dt)
+
+    def gq(sym):
+        def f(w, group=128, snr=True, **_):
+            qw, qz, sc, gi, s = oracle.gptq_quantize(w, group, sym)
+            return {"qweight": torch.from_numpy(qw), "qzeros": torch.from_numpy(qz),
+                    "scales": bits(sc, torch.float16), "g_idx": torch.from_numpy(gi),
+                    "snr_db": torch.tensor(s, dtype=torch.float64)}
+        return f
+
+    def gdq(qw, qz, sc, n, k, group, sym, out_dtype=torch.float32, **_):
+        return torch.from_numpy(oracle.gptq_dequantize(qw.numpy(), qz.numpy(), sc, n, k, group, sym))
+
+    def qsnr(w, deq, **_):
+        s, r = oracle.quant_snr(w, deq)
+        return torch.tensor(s), torch.tensor(r)
+
+    def aws(w, a, alphas, max_rows=2048, **_):
+        s, i, al, e = oracle.awq_search(w, a.numpy(), alphas, max_rows)
+        return torch.from_numpy(s), torch.tensor(i), torch.tensor(al), torch.from_numpy(e)
+
+    def fold(w, s, axis=0, op=0, *, out=None):
+        r = bits(oracle.awq_fold(w, s.numpy(), axis, op).reshape(w.shape), torch.bfloat16)
+        return out.copy_(r) if out is not None else r
+
+    def mq(w, *a, **_):
+        p, e = oracle.mxfp4_quantize(w)
+        return torch.from_numpy(p), torch.from_numpy(e)
+
+    def mdq(p, e, dt=torch.float32, **_):
+        return torch.from_numpy(oracle.mxfp4_dequantize(p.numpy(), e.numpy()))
+
+    monkeypatch.setattr(export, "gptq_quantize_sym", gq(True))
+    monkeypatch.setattr(export, "gptq_quantize_asym", gq(False))
+    for name, fn in (("gptq_dequantize", gdq), ("quant_snr", qsnr), ("awq_search", aws), ("awq_fold", fold),
+                     ("mxfp4_quantize", mq), ("mxfp4_dequantize", mdq)):
+        monkeypatch.setattr(wq, name, fn)
+
+
+def test_gptq_export_logic(tmp_path, oracle_kernels):
+    state, cfg = synth.tiny_decoder_state(n_layers=1)
+    hd = cfg["head_dim"]
+    state = export.split_fused_qkv(state, cfg["num_attention_heads"] * hd, cfg["num_key_value_heads"] * hd)
+    out, report, summary = export.export_gptq(state, 64, True, quantize_embedding=False,
+                                              quantize_lm_head=True, device="cpu")
+    names = {r["name"] for r in report}
+    assert names == {n for n in state if n.endswith(export.GPTQ_TARGET_SUFFIXES)} | {"lm_head"}
+    assert export.EMBED_NAME in out and "lm_head.qweight" in out  # table kept, head untied
+    qw, qz, sc, gi, snr = oracle.gptq_quantize(state[export.EMBED_NAME], 64, False)
+    assert np.array_equal(out["lm_head.qweight"].numpy(), qw)
+    assert summary["tensors"] == len(report) and summary["bits_per_weight"] == 4 + 20 / 64
+    export.write_gptq_checkpoint(str(tmp_path), out, cfg, report, summary, 64, True, True)
+    c = json.load(open(tmp_path / "config.json"))
+    assert c["quantization_config"]["sym"] is False and c["tie_word_embeddings"] is False
+    back, meta = export.load_safetensors(str(tmp_path / "model.safetensors"))
+    assert set(back) == set(out) and all(torch.equal(back[k], out[k]) for k in out)
+    res = export.verify_gptq_checkpoint(str(tmp_path), state, report, 64, True, device="cpu")
+    assert [r["name"] for r in res] == [r["name"] for r in report]
+
+
+def test_mxfp4_export_logic_fold_order(oracle_kernels):
+    state, act, cfg = synth.tiny_drafter_state(n_layers=1)
+    before = {k: v.clone() for k, v in state.items()}
+    out, alphas, errs = export.export_mxfp4_awq(state, 1, act, device="cpu")
+    assert [a for a, _ in alphas] == ["layers.0.qkv", "layers.0.gate_up", "layers.0.down"]
+    # the norm is divided by the attention scale: redo that one fold by hand
+    w = state["layers.0.self_attn.q_proj.weight"]
+    cat = torch.cat([w, state["layers.0.self_attn.k_proj.weight"], state["layers.0.self_attn.v_proj.weight"]])
+    s, _, _, _ = oracle.awq_search(cat, act["layers.0.self_attn.qkv_proj"].numpy(), synth.ALPHAS, 2048)
+    ln = oracle.awq_fold(state["layers.0.input_layernorm.weight"], s, 0, 1).reshape(-1)
+    assert np.array_equal(out["layers.0.input_layernorm.weight"].view(torch.int16).numpy().view(np.uint16), ln)
+    assert "fc.weight_scale" in out and out["fc.weight"].dtype == torch.uint8
+    assert len(errs) == len(export.mxfp4_targets(1))
+    # the folds run in place on the exporter's own copies, never on the caller's tensors
+    assert all(torch.equal(state[k], before[k]) for k in state)
