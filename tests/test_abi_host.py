@@ -190,3 +190,107 @@ def test_consumers_refuse_non_bf16_operands():
     with pytest.raises(TypeError):
         wq.uintx_gemm(torch.zeros(2, 64, dtype=torch.bfloat16), None,
                       torch.zeros(64, 1, dtype=torch.float16), None, 64, 64, 4)
+
+
+# ------------------------------------------------------------------ binding argument checks
+# The kernels size every read and write from the shape arguments, so the binding
+# checks each tensor before the call.  These run on CPU tensors: every case must
+# raise before the library is reached (a CPU tensor that passed every check would
+# still be refused as not on a CUDA device).
+def _cpu(shape, dtype):
+    import torch
+
+    return torch.zeros(shape, dtype=dtype)
+
+
+def test_binding_refuses_output_dtypes_the_library_does_not_write():
+    import torch
+
+    qw, qz, sc = _cpu((16, 64), torch.int32), _cpu((1, 8), torch.int32), _cpu((1, 64), torch.float16)
+    with pytest.raises(TypeError):  # float16 output would be written as binary32
+        wq.gptq_dequantize(qw, qz, sc, 64, 128, 128, False, out_dtype=torch.float16)
+    with pytest.raises(TypeError):
+        wq.mxfp4_dequantize(_cpu((4, 32), torch.uint8), _cpu((4, 2), torch.uint8), out_dtype=torch.float16)
+    with pytest.raises(TypeError):
+        wq.uintx_dequantize(_cpu((256,), torch.uint8), _cpu((4, 2), torch.bfloat16), _cpu((4, 2), torch.uint8),
+                            4, 128, 4, 64, out_dtype=torch.float64)
+    x = _cpu((1, 128), torch.bfloat16)
+    for call in (lambda: wq.gptq_linear(x, qw, qz, sc, 64, 128, 128, False, out_dtype=torch.float16),
+                 lambda: wq.gptq_gemm(x, qw, qz, sc, 64, 128, 128, False, out_dtype=torch.float16),
+                 lambda: wq.mxfp4_linear(x, _cpu((4, 64), torch.uint8), _cpu((4, 4), torch.uint8),
+                                         out_dtype=torch.float16)):
+        with pytest.raises(TypeError):
+            call()
+    # quant_snr: an fp16 deq would be read as binary32
+    with pytest.raises(TypeError):
+        wq.quant_snr(_cpu((4, 64), torch.bfloat16), _cpu((4, 64), torch.float16))
+
+
+def test_binding_checks_caller_outputs():
+    import torch
+
+    qw, qz, sc = _cpu((16, 64), torch.int32), _cpu((1, 8), torch.int32), _cpu((1, 64), torch.float16)
+    # out whose dtype differs from out_dtype: the kernel would write 4 bytes per 2-byte element
+    with pytest.raises(TypeError, match="out"):
+        wq.gptq_dequantize(qw, qz, sc, 64, 128, 128, False, torch.float32, out=_cpu((64, 128), torch.bfloat16))
+    with pytest.raises(TypeError, match="out"):
+        wq.mxfp4_dequantize(_cpu((4, 32), torch.uint8), _cpu((4, 2), torch.uint8),
+                            out=_cpu((4, 64), torch.bfloat16))
+    # too few elements
+    with pytest.raises(ValueError, match="out"):
+        wq.gptq_dequantize(qw, qz, sc, 64, 128, 128, False, torch.float32, out=_cpu((64, 127), torch.float32))
+    with pytest.raises(ValueError, match="packed"):
+        wq.mxfp4_quantize(_cpu((4, 64), torch.bfloat16), packed=_cpu((4, 31), torch.uint8))
+    with pytest.raises(ValueError, match="scales"):
+        wq.gptq_quantize_asym(_cpu((64, 128), torch.bfloat16), 128, scales=_cpu((1, 63), torch.float16))
+    with pytest.raises(ValueError, match="zp"):
+        wq.uintx_quantize(_cpu((4, 128), torch.bfloat16), 4, 64, zp=_cpu((4, 1), torch.uint8))
+    # not contiguous
+    with pytest.raises(ValueError, match="contiguous"):
+        wq.gptq_dequantize(qw, qz, sc, 64, 128, 128, False, torch.float32,
+                           out=_cpu((128, 64), torch.float32).t())
+    # a workspace that is too small or of the wrong type
+    with pytest.raises(ValueError, match="ws"):
+        wq.quant_snr(_cpu((4, 64), torch.bfloat16), _cpu((4, 64), torch.float32), ws=_cpu((16,), torch.uint8))
+    with pytest.raises(TypeError, match="ws"):
+        wq.gptq_quantize_sym(_cpu((64, 128), torch.bfloat16), 128, ws=_cpu((1 << 20,), torch.float32))
+    # everything consistent: still refused, the tensors are not on a CUDA device
+    with pytest.raises(ValueError, match="CUDA"):
+        wq.gptq_dequantize(qw, qz, sc, 64, 128, 128, False, torch.float32, out=_cpu((64, 128), torch.float32))
+
+
+def test_binding_checks_inputs():
+    import torch
+
+    # the stored GPTQ tensors must match n, k, group
+    with pytest.raises(ValueError, match="qweight"):
+        wq.gptq_dequantize(_cpu((15, 64), torch.int32), None, _cpu((1, 64), torch.float16), 64, 128, 128, True)
+    with pytest.raises(ValueError, match="qzeros"):  # asym needs its zero points
+        wq.gptq_dequantize(_cpu((16, 64), torch.int32), None, _cpu((1, 64), torch.float16), 64, 128, 128, False)
+    with pytest.raises(ValueError, match="e8m0"):
+        wq.mxfp4_dequantize(_cpu((4, 32), torch.uint8), _cpu((4, 1), torch.uint8))
+    with pytest.raises(ValueError, match="packed"):
+        wq.uintx_dequantize(_cpu((255,), torch.uint8), _cpu((4, 2), torch.bfloat16), _cpu((4, 2), torch.uint8),
+                            4, 128, 4, 64)
+    # 16-bit weights other than bf16 would be read as bf16 bit patterns
+    a = _cpu((64,), torch.float32)
+    for call in (lambda: wq.awq_search(_cpu((4, 64), torch.float16), a, [0.0, 1.0]),
+                 lambda: wq.awq_fold(_cpu((4, 64), torch.float16), a),
+                 lambda: wq.quant_snr(_cpu((4, 64), torch.float16), _cpu((4, 64), torch.float32)),
+                 lambda: wq.gptq_quantize_sym(_cpu((64, 128), torch.int16), 128)):
+        with pytest.raises(TypeError):
+            call()
+    # the activation statistics: binary32, one per column
+    with pytest.raises(TypeError, match="a"):
+        wq.awq_search(_cpu((4, 64), torch.bfloat16), _cpu((64,), torch.float64), [0.0, 1.0])
+    with pytest.raises(ValueError, match="a"):
+        wq.awq_search(_cpu((4, 64), torch.bfloat16), _cpu((32,), torch.float32), [0.0, 1.0])
+    # fold scales: k entries per column fold, n per row fold
+    with pytest.raises(ValueError, match="s"):
+        wq.awq_fold(_cpu((4, 64), torch.bfloat16), _cpu((4,), torch.float32), axis=0)
+    with pytest.raises(ValueError, match="layout"):
+        wq.quant_snr(_cpu((4, 64), torch.bfloat16), _cpu((4, 64), torch.float32), layout="mk")
+    # consumers: x must have the weight's k columns
+    with pytest.raises(ValueError, match="columns"):
+        wq.gptq_gemm(_cpu((2, 96), torch.bfloat16), _cpu((16, 64), torch.int32), None,
+                     _cpu((1, 64), torch.float16), 64, 128)

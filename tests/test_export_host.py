@@ -131,7 +131,10 @@ def oracle_kernels(monkeypatch):
 
     def gq(sym):
         def f(w, group=128, snr=True, **_):
-            qw, qz, sc, gi, s = oracle.gptq_quantize(w, group, sym)
+            if w.dtype == torch.bfloat16:
+                qw, qz, sc, gi, s = oracle.gptq_quantize(w, group, sym)
+            else:  # fp16 / fp32 weights: the binary32 entry (the page's w.float())
+                qw, qz, sc, gi, s = oracle.gptq_quantize_f32(w.float().numpy(), group, sym)
             return {"qweight": torch.from_numpy(qw), "qzeros": torch.from_numpy(qz),
                     "scales": bits(sc, torch.float16), "g_idx": torch.from_numpy(gi),
                     "snr_db": torch.tensor(s, dtype=torch.float64)}
@@ -202,3 +205,23 @@ def test_mxfp4_export_logic_fold_order(oracle_kernels):
     assert len(errs) == len(export.mxfp4_targets(1))
     # the folds run in place on the exporter's own copies, never on the caller's tensors
     assert all(torch.equal(state[k], before[k]) for k in state)
+
+
+def test_gptq_export_keeps_fp16_weights(oracle_kernels):
+    """An fp16 checkpoint is quantized from its own values (export_gptq_cpu.py
+    quantize_* start from w.float()), not from a bf16 rounding of them."""
+    state, cfg = synth.tiny_decoder_state(n_layers=1)
+    hd = cfg["head_dim"]
+    state = export.split_fused_qkv(state, cfg["num_attention_heads"] * hd, cfg["num_key_value_heads"] * hd)
+    g = torch.Generator().manual_seed(5)
+    state = {k: (v.float() + torch.randn(v.shape, generator=g) * 1e-4).half() for k, v in state.items()}
+    out, report, _ = export.export_gptq(state, 64, True, device="cpu")
+    name = "model.layers.0.mlp.down_proj.weight"
+    w = state[name]
+    qw, qz, sc, gi, snr = oracle.gptq_quantize_f32(w.float().numpy(), 64, False)
+    base = name[: -len(".weight")]
+    assert np.array_equal(out[f"{base}.qweight"].numpy(), qw)
+    assert np.array_equal(out[f"{base}.scales"].view(torch.int16).numpy().view(np.uint16), sc)
+    # and differs from what a bf16 rounding of the weights would give
+    qw_bf, *_ = oracle.gptq_quantize(w.to(torch.bfloat16), 64, False)
+    assert not np.array_equal(qw_bf, qw)

@@ -114,7 +114,12 @@ def export_gptq(state: dict, group: int = 128, asym: bool = False, quantize_embe
     out, report = {}, []
 
     def q(name, t, base):
-        r = quantize(t.to(device=device, dtype=torch.bfloat16).contiguous(), group, True)
+        # bf16, fp16 and fp32 weights are quantized as they are (the page starts
+        # from w.float(); fp16 / fp32 take the library's binary32 path); any other
+        # floating type is widened to binary32 first
+        if t.dtype not in (torch.bfloat16, torch.float16, torch.float32):
+            t = t.float()
+        r = quantize(t.to(device=device).contiguous(), group, True)
         for key in ("qweight", "qzeros", "scales", "g_idx"):
             out[f"{base}.{key}"] = r[key].cpu()
         report.append({"name": name, "snr_db": round(float(r["snr_db"]), 2)})
@@ -309,8 +314,8 @@ def _mxfp4_main(a) -> None:
     with open(os.path.join(a.src, "config.json")) as fh:
         cfg = json.load(fh)
     nl = cfg["num_hidden_layers"]
-    c0 = torch.load(f"{a.calib_prefix}.tp0.pt", map_location="cpu")
-    c1 = torch.load(f"{a.calib_prefix}.tp1.pt", map_location="cpu")
+    c0 = torch.load(f"{a.calib_prefix}.tp0.pt", map_location="cpu", weights_only=True)
+    c1 = torch.load(f"{a.calib_prefix}.tp1.pt", map_location="cpu", weights_only=True)
     act = {}
     for l in range(nl):
         P = f"layers.{l}"
