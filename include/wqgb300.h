@@ -81,6 +81,8 @@ typedef int wq_status;
 #define WQ_OP_GPTQ_QUANTIZE 0 /* arg = group; only needed when snr_db != NULL */
 #define WQ_OP_QUANT_SNR 1     /* arg ignored */
 #define WQ_OP_AWQ_SEARCH 2    /* arg = n_alpha */
+#define WQ_OP_MXFP4_ERR 3     /* mxfp4_quantize_err; arg ignored */
+#define WQ_OP_UINTX_ERR 4     /* uintx_quantize_err; arg = nbits (ignored) */
 
 /* Human-readable name of a status code (static string). */
 const char* wq_status_string(wq_status status);
@@ -103,6 +105,23 @@ const char* wq_version(void);
  * is synchronous (a device-to-host copy on the legacy default stream): call it
  * after the streams that ran the kernels have been synchronised. */
 wq_status wq_device_status(void);
+
+/* Diagnostic: the budget of a class of bounded device-side waits, for launches
+ * made after this call, process-wide; returns the previous budget (0xFFFFFFFF
+ * and no change for an unknown site).  Pure host state: needs no GPU.
+ *   WQ_WAIT_GPTQ_STAGE  polls of each wait of gptq_quantize_sym / _asym (bf16
+ *                       weights) on the mbarrier of a TMA load; default 2^22.
+ *   WQ_WAIT_GEMM_MMA    slices of 64 polls of each wait of the MMA-issuing
+ *                       thread of gptq_gemm / uintx_gemm; default 512.
+ * The defaults are far beyond any latency.  A budget of 0 makes every such wait
+ * give up at once, which runs the kernel's timeout path without any fault: it
+ * stops its work, lets the copies and MMAs it already issued complete (those
+ * drains keep their own budgets), frees what it holds and records
+ * WQ_ERR_DEVICE_TIMEOUT for wq_device_status; the outputs of that call are then
+ * incomplete.  Meant for testing that path; restore the returned value after. */
+#define WQ_WAIT_GPTQ_STAGE 0
+#define WQ_WAIT_GEMM_MMA 1
+unsigned wq_set_wait_budget(int site, unsigned budget);
 
 /* Bytes of workspace `op` needs for an [n, k] weight (0 if none).  Pure host
  * arithmetic: needs no GPU. */
@@ -176,6 +195,25 @@ wq_status gptq_dequantize(const int32_t* qweight, const int32_t* qzeros, const u
 wq_status mxfp4_quantize(const uint16_t* w, int64_t n, int64_t k, int tie_mode, uint8_t* packed,
                          uint8_t* e8m0, void* stream);
 
+/* mxfp4_quantize_err (quantize_dflash_mxfp4.py: quantize_mxfp4, then main()'s
+ * relative-error report of the quantized target, rel = ||deq - w|| / ||w|| with
+ * deq as dequantize_mxfp4 returns it) -- mxfp4_quantize plus the reconstruction
+ * error of the same pass: the kernel decodes its own codes on-chip, so w is read
+ * once and no dequantized tensor is written.
+ * In/Out: as mxfp4_quantize (bf16 w), and
+ *      snr_db, rel_err  one double each on the device (either may be NULL; both
+ *               NULL is plain mxfp4_quantize): over the whole tensor, Sw = sum w^2,
+ *               Se = sum (w - deq)^2 with binary32 terms, snr_db = 20*log10(
+ *               sqrt(Sw) / max(sqrt(Se), 1e-12)), rel_err = sqrt(Se) / sqrt(Sw);
+ *               the same definitions as quant_snr, within 1e-4 relative of
+ *               binary64 sums of the same terms.
+ *      workspace  >= wq_workspace_bytes(WQ_OP_MXFP4_ERR, n, k, 0), 16-byte
+ *               aligned; calls that overlap on the GPU need separate workspaces.
+ * n == 0 or k == 0 launches nothing and leaves snr_db / rel_err unwritten. */
+wq_status mxfp4_quantize_err(const uint16_t* w, int64_t n, int64_t k, int tie_mode, uint8_t* packed,
+                             uint8_t* e8m0, double* snr_db, double* rel_err, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
 /* mxfp4_quantize_ex (quantize_dflash_mxfp4.py quantize_mxfp4, which starts from
  * w.float()) -- as mxfp4_quantize for a weight of type w_dtype (WQ_DTYPE_BF16
  * calls it; WQ_DTYPE_F16 / WQ_DTYPE_F32: the block exponent from the binary32
@@ -218,11 +256,14 @@ wq_status awq_search(const uint16_t* w, int64_t n, int64_t k, const float* a,
  * Same arguments and results as awq_search, minus workspace/workspace_bytes.
  * Scratch: a fixed 2,883,840-byte array inside the library (held by every GPU
  * that loads the library until the process exits), enough for k <= 16384 and
- * n_alpha <= 16; larger k returns WQ_ERR_BAD_SHAPE before any launch.  The
- * first call on a device (with that device current) looks the array's device
- * address up once; make that first call before any stream capture.  Every call
- * shares the array: calls that overlap on the GPU race and must be serialised by
- * the caller.  Calls no allocation routine. */
+ * n_alpha <= 16.  Larger k returns WQ_ERR_BAD_SHAPE and n_alpha outside 1..16
+ * WQ_ERR_UNSUPPORTED (as awq_search), before any launch.  The first call in a
+ * device's CUDA context (with that device current) looks the array's device
+ * address up once; make that first call before any stream capture.  The address
+ * is cached per context, so a call after a context reset (cudaDeviceReset) looks
+ * it up again.  `stream` must belong to the current device (WQ_ERR_UNSUPPORTED
+ * otherwise).  Every call shares the array: calls that overlap on the GPU race
+ * and must be serialised by the caller.  Calls no allocation routine. */
 wq_status awq_search_static_scratch(const uint16_t* w, int64_t n, int64_t k, const float* a,
                                     const float* alphas_host, int n_alpha, int max_rows,
                                     int tie_mode, float* best_s, int32_t* best_idx,
@@ -353,6 +394,19 @@ int64_t uintx_packed_bytes(int64_t numel, int nbits);
  *   / scale), 0, qmax), q = clamp(round(w * (1/scale)) + zp, 0, qmax). */
 wq_status uintx_quantize(const uint16_t* w, int64_t n, int64_t k, int nbits, int group,
                          uint8_t* packed, uint16_t* scale, uint8_t* zp, void* stream);
+
+/* uintx_quantize_err (uintx_quant.py: _quantize_impl + pack_uintx, and the
+ * reconstruction error of the weight that _dequantize_native rebuilds; the same
+ * SNR / relative-error definitions as export_gptq_cpu.py quantize_* and
+ * quantize_dflash_mxfp4.py main()) -- uintx_quantize plus the error of the same
+ * pass, deq = bf16(bf16(q - zp) * scale) formed on-chip from the codes.
+ * In/Out: as uintx_quantize (bf16 w), and snr_db, rel_err (device doubles,
+ * either may be NULL; both NULL is plain uintx_quantize) as mxfp4_quantize_err;
+ * workspace >= wq_workspace_bytes(WQ_OP_UINTX_ERR, n, k, nbits), 16-byte aligned.
+ * n == 0 or k == 0 launches nothing and leaves snr_db / rel_err unwritten. */
+wq_status uintx_quantize_err(const uint16_t* w, int64_t n, int64_t k, int nbits, int group,
+                             uint8_t* packed, uint16_t* scale, uint8_t* zp, double* snr_db,
+                             double* rel_err, void* workspace, size_t workspace_bytes, void* stream);
 
 /* uintx_dequantize (uintx_quant.py, unpack_uintx + _dequantize_native)
  * out = bf16(bf16(q - zp) * scale), as bf16 (WQ_DTYPE_BF16) or its exact binary32

@@ -53,6 +53,7 @@ def step_outputs():
             o[tag]["qweight"].fill_(0x5A5A5A5A)
             o[tag]["snr_db"].fill_(float("nan"))
         o["mx"]["packed"].fill_(0xA5)
+        o["snr"]["rel_err"].fill_(float("nan"))
         o["ux"]["packed"].fill_(0xA5)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
@@ -93,6 +94,6 @@ def test_step_awq_alpha_matches_oracle(step_outputs):
     got = wl.awq_out
     np.testing.assert_allclose(got["errs"].cpu().numpy(), errs, rtol=REL)
     order = np.argsort(errs)
-    if errs[order[1]] - errs[order[0]] > 1e-6 * errs[order[0]]:
+    if errs[order[1]] - errs[order[0]] > 1e-9 * errs[order[0]]:  # not a near-tie
         assert int(got["best_idx"]) == bi
         np.testing.assert_allclose(got["best_s"].cpu().numpy(), best_s, rtol=2e-7)

@@ -188,6 +188,42 @@ def test_gptq_other_groups_large_sampled(group):
         _sampled_gptq(w, group, sym, 74 + group)
 
 
+def check_gptq_dequant(n, k, group, seed):
+    """gptq_dequantize element by element against the oracle on seeded stored
+    tensors (every code and zero point), both rules, both layouts, both output
+    dtypes (export_gptq_cpu.py module docstring: w = (code - 8) * scale; with real
+    zero points w = (code - zp) * scale)."""
+    qw, qz, sc = synth.gptq_packed(n, k, group, seed)
+    qw_d, qz_d, sc_d = qw.to(DEV), qz.to(DEV), sc.to(DEV)
+    for sym in (True, False):
+        for layout in ("nk", "kn"):
+            want = oracle.gptq_dequantize(npy(qw), npy(qz), sc, n, k, group, sym, out_kn=(layout == "kn"))
+            got = wq.gptq_dequantize(qw_d, None if sym else qz_d, sc_d, n, k, group, sym, torch.float32, layout)
+            assert np.array_equal(npy(got).view(np.uint32), want.view(np.uint32)), (n, k, group, sym, layout)
+            got16 = wq.gptq_dequantize(qw_d, None if sym else qz_d, sc_d, n, k, group, sym, torch.bfloat16,
+                                       layout)
+            assert np.array_equal(u16(got16), bf16_of_f32(want)), (n, k, group, sym, layout, "bf16")
+            del got, got16, want
+
+
+@pytest.mark.parametrize("name,n,k", [("gate_proj", 14336, 4096), ("down_proj", 4096, 14336)])
+def test_gptq_dequantize_full_size(name, n, k):
+    """The layer's largest projections at full size, group 128: every warp (nk) and
+    CTA (kn) walks several tiles, so the incremental tile walk is compared too."""
+    check_gptq_dequant(n, k, 128, 80 + n % 7)
+
+
+@pytest.mark.parametrize("group", [32, 64, 128, 256])
+@pytest.mark.parametrize("shape", [(200, 768), (8, 256), (72, 1280), (1032, 4352)])
+def test_gptq_dequantize_ragged(group, shape):
+    """Row counts that are not multiples of a warp's 32 rows or a CTA's 1024
+    columns, k not a multiple of the 128-wide tile, every group size."""
+    n, k = shape
+    if k % group:
+        pytest.skip("k not a multiple of group")
+    check_gptq_dequant(n, k, group, n + 3 * k + group)
+
+
 # ------------------------------------------------------------------ MXFP4
 def check_mxfp4(w: torch.Tensor, tie_mode: int, ref=None):
     packed, e8 = wq.mxfp4_quantize(w.to(DEV), tie_mode)
@@ -220,14 +256,20 @@ def test_mxfp4_edge_blocks(tie_mode):
     check_mxfp4(w, tie_mode)
 
 
-def test_mxfp4_full_size_and_dequant():
-    """gate_up [34816, 5120] with 1% of blocks x50, full tensor, both dequant dtypes."""
+@pytest.fixture(scope="module")
+def gate_up_ref():
+    """The C3 tensor (gate_up [34816, 5120], 1% of blocks x50) and the oracle's
+    codes and E8M0 bytes for it (half-even ties), computed once per module."""
     w = synth.mxfp4_gate_up(device="cpu")
-    n, k = w.shape
+    n = w.shape[0]
     chunks = [(i, min(i + 4352, n)) for i in range(0, n, 4352)]
     refs = pool_map(lambda c: oracle.mxfp4_quantize(w[c[0]:c[1]]), chunks)
-    p_ref = np.concatenate([r[0] for r in refs])
-    e_ref = np.concatenate([r[1] for r in refs])
+    return w, chunks, np.concatenate([r[0] for r in refs]), np.concatenate([r[1] for r in refs])
+
+
+def test_mxfp4_full_size_and_dequant(gate_up_ref):
+    """gate_up [34816, 5120] with 1% of blocks x50, full tensor, both dequant dtypes."""
+    w, chunks, p_ref, e_ref = gate_up_ref
     packed, e8, _, _ = check_mxfp4(w, 0, (p_ref, e_ref))
     out32 = npy(wq.mxfp4_dequantize(packed, e8, torch.float32))
     out16 = u16(wq.mxfp4_dequantize(packed, e8, torch.bfloat16))
@@ -235,6 +277,43 @@ def test_mxfp4_full_size_and_dequant():
         want = oracle.mxfp4_dequantize(p_ref[lo:hi], e_ref[lo:hi])
         assert np.array_equal(out32[lo:hi], want)
         assert np.array_equal(out16[lo:hi], bf16_of_f32(want))
+
+
+def check_mxfp4_err(w, tie_mode, ref=None):
+    """mxfp4_quantize_err: the codes and E8M0 bytes of mxfp4_quantize, and the
+    relative error / SNR of the page's dequantized weight against w
+    (quantize_dflash_mxfp4.py main(): relative error of each quantized target),
+    within 1e-4 of the oracle's binary64 sums of the same binary32 terms."""
+    p, e, snr, rel = wq.mxfp4_quantize(w.to(DEV), tie_mode, err=True)
+    p_ref, e_ref = ref if ref is not None else oracle.mxfp4_quantize(w, tie_mode)
+    assert np.array_equal(npy(e), e_ref) and np.array_equal(npy(p), p_ref)
+    s_ref, r_ref = oracle.quant_snr(w, oracle.mxfp4_dequantize(p_ref, e_ref))
+    assert abs(float(rel) - r_ref) <= REL * abs(r_ref), (float(rel), r_ref)
+    assert abs(float(snr) - s_ref) <= REL * abs(s_ref), (float(snr), s_ref)
+
+
+def test_mxfp4_quantize_err_full_size(gate_up_ref):
+    """The fused error on the full C3 tensor (one pass; no dequantized tensor)."""
+    w, _, p_ref, e_ref = gate_up_ref
+    check_mxfp4_err(w, 0, (p_ref, e_ref))
+
+
+@pytest.mark.parametrize("tie_mode", [0, 1])
+def test_mxfp4_quantize_err_small(tie_mode):
+    """Exact-tie blocks (both tie rules), a ragged row count, mixed magnitudes and
+    a row of zeros among normal rows.  Magnitudes stay where w^2 is a finite
+    binary32 value (beyond it both sides give inf / NaN, as the page's float32
+    norms would)."""
+    g = torch.Generator().manual_seed(11)
+    nb = 8 * 1024 // 32
+    e = torch.randint(-20, 21, (nb, 1), generator=g).double()
+    vals = torch.randint(0, 25, (nb, 32), generator=g).double() * 0.25
+    vals *= torch.where(torch.rand((nb, 32), generator=g) < 0.5, -1.0, 1.0).double()
+    vals[torch.arange(nb), torch.randint(0, 32, (nb,), generator=g)] = 6.0  # fixes the block exponent at e
+    check_mxfp4_err((vals * torch.exp2(e)).view(8, 1024).to(torch.bfloat16), tie_mode)
+    w = torch.randn(37, 4096, generator=g) * torch.exp(torch.randn(37, 1, generator=g) * 3)
+    w[5] = 0.0
+    check_mxfp4_err(w.to(torch.bfloat16), tie_mode)
 
 
 def test_mxfp4_dequant_all_bytes():
@@ -307,6 +386,33 @@ def test_uintx_degenerate_groups():
         check_uintx(fused, nbits)
 
 
+def check_uintx_err(w, nbits, group=64, ref=None):
+    """uintx_quantize_err: the outputs of uintx_quantize and the SNR / relative
+    error of the page's bf16 dequantized weight (_dequantize_native) against w,
+    within 1e-4 of the oracle's binary64 sums."""
+    n, k = w.shape
+    packed, scale, zp, snr, rel = wq.uintx_quantize(w.to(DEV), nbits, group, err=True)
+    p_ref, s_ref, z_ref, _ = ref if ref is not None else oracle.uintx_quantize(w, nbits, group)
+    assert np.array_equal(u16(scale), s_ref) and np.array_equal(npy(zp), z_ref)
+    assert np.array_equal(npy(packed), p_ref)
+    deq = oracle.bf16_bits_to_f32(oracle.uintx_dequantize(p_ref, s_ref, z_ref, n, k, nbits, group))
+    sn_ref, r_ref = oracle.quant_snr(w, deq)
+    assert abs(float(rel) - r_ref) <= REL * abs(r_ref), (float(rel), r_ref)
+    assert abs(float(snr) - sn_ref) <= REL * abs(sn_ref), (float(snr), sn_ref)
+
+
+@pytest.mark.parametrize("nbits", [2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("shape,group", [((64, 512), 64), ((9, 192), 64), ((40, 96), 32), ((5, 24), 8),
+                                         ((333, 4096), 64)])
+def test_uintx_quantize_err_shapes(nbits, shape, group):
+    """The fused error on the single-pass path (numel % 512 == 0, group 64) and on
+    the general path (ragged numel, other groups)."""
+    n, k = shape
+    g = torch.Generator().manual_seed(nbits * 77 + n + k)
+    w = (torch.randn(n, k, generator=g) * 0.02 * torch.exp(torch.randn(n, 1, generator=g))).to(torch.bfloat16)
+    check_uintx_err(w, nbits, group)
+
+
 @pytest.mark.parametrize("nbits", [2, 3, 4, 5, 6, 7])
 def test_uintx_layer_full_size(nbits):
     """One full layer of the 8-layer uintx workload per nbits (218 M weights)."""
@@ -319,6 +425,7 @@ def test_uintx_layer_full_size(nbits):
             want = oracle.uintx_dequantize(p_ref, s_ref, z_ref, n, k, nbits)
             got = wq.uintx_dequantize(packed, scale, zp, n, k, nbits)
             assert np.array_equal(u16(got), want), name
+            check_uintx_err(w, nbits, 64, ref)  # the fused error at full size
 
 
 # ------------------------------------------------------------------ SNR
@@ -359,7 +466,11 @@ def check_awq(w, a, alphas, max_rows, tie_mode=0):
     np.testing.assert_allclose(e, e_ref, rtol=REL, atol=0)
     order = np.sort(e_ref)
     margin = (order[1] - order[0]) / order[0] if len(order) > 1 and order[0] > 0 else 1.0
-    if margin > 1e-6:  # a near-tie between the two best alphas is reported, not failed
+    # the reading of search_scale's argmin: a relative margin below 1e-9 between
+    # the two best alphas is a near-tie, reported and not failed; above it the
+    # chosen alpha and its scales must be the oracle's (the cases here have
+    # margins of 1e-3 and more, printed by test_awq_full_size)
+    if margin > 1e-9:
         assert int(bi) == bi_ref and float(ba) == ba_ref
         np.testing.assert_allclose(npy(best_s), s_ref, rtol=2e-7, atol=0)
     return int(bi), margin

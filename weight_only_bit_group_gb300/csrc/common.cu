@@ -109,7 +109,8 @@ extern "C" int64_t uintx_packed_bytes(int64_t numel, int nbits) {
 }
 
 // Workspace layouts (all offsets 256-byte aligned):
-//   GPTQ quantize with SNR, quant_snr: control block (arrival counter) |
+//   GPTQ quantize with SNR, quant_snr, mxfp4_quantize_err, uintx_quantize_err:
+//               control block (arrival counter) |
 //               kMaxPartials x 16-byte per-CTA float-float pairs.
 //   awq_search: control block | s table [n_alpha][k] f32 | a_c/s table
 //               [n_alpha][k] f32 | a_c [k] f32 | ln(an) [k] f64 + an [k] f32 |
@@ -120,6 +121,8 @@ extern "C" size_t wq_workspace_bytes(int op, int64_t n, int64_t k, int arg) {
     switch (op) {
         case WQ_OP_GPTQ_QUANTIZE:
         case WQ_OP_QUANT_SNR:
+        case WQ_OP_MXFP4_ERR:
+        case WQ_OP_UINTX_ERR:
             return wqh::kCtrlBytes + up((size_t)wqh::kMaxPartials * 2 * sizeof(double));
         case WQ_OP_AWQ_SEARCH: {
             if (arg < 1 || k < 0) return 0;
@@ -130,5 +133,18 @@ extern "C" size_t wq_workspace_bytes(int op, int64_t n, int64_t k, int arg) {
         }
         default:
             return 0;
+    }
+}
+
+namespace wqh {
+unsigned gptq_stage_polls_exchange(unsigned polls);  // gptq.cu
+unsigned gemm_mma_slices_exchange(unsigned slices);  // gemm.cu
+}  // namespace wqh
+
+extern "C" unsigned wq_set_wait_budget(int site, unsigned budget) {
+    switch (site) {
+        case WQ_WAIT_GPTQ_STAGE: return wqh::gptq_stage_polls_exchange(budget);
+        case WQ_WAIT_GEMM_MMA: return wqh::gemm_mma_slices_exchange(budget);
+        default: return 0xFFFFFFFFu;
     }
 }

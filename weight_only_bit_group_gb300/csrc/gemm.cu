@@ -29,6 +29,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "wq_common.cuh"
@@ -171,8 +172,14 @@ __device__ __forceinline__ bool poll_bar(uint32_t bar, uint32_t parity, uint32_t
 // Wait with the abort protocol: polls in slices, gives up early once another
 // role aborted, and records a timeout.  Same outcome on every lane that calls it
 // (callers that need a warp-wide decision combine it with __all_sync).
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    for (uint32_t i = 0; i < 512; ++i) {
+constexpr uint32_t kWaitSlices = 512;  // default budget of a wait: 512 slices of 64 polls
+// Budget (slices) of the MMA-issuing thread's waits for the next launches (kernel
+// argument; a diagnostic lowers it to make the abort path run, see
+// wq_set_wait_budget).  The other roles and every drain keep their own budgets.
+std::atomic<unsigned> g_mma_slices{kWaitSlices};
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         uint32_t slices = kWaitSlices) {
+    for (uint32_t i = 0; i < slices; ++i) {
         if (poll_bar(bar, parity, 64)) return true;
         if (*abort_flag) return false;
     }
@@ -202,7 +209,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap qmap,
                  const int32_t* __restrict__ qzeros, const uint16_t* __restrict__ scales, int m, int n,
                  int k, void* __restrict__ out, const uint8_t* __restrict__ ux_packed,
-                 const uint8_t* __restrict__ ux_zp, int ux_group) {
+                 const uint8_t* __restrict__ ux_zp, int ux_group, uint32_t mma_slices) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -298,7 +305,9 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             for (int kb = 0; kb < nkb && ok; ++kb) {
                 const int s = kb % NS;
                 const uint32_t par = (uint32_t)(kb / NS) & 1u;
-                if (!wait_bar(full(s), par, abort_flag) || !wait_bar(aready(s), par, abort_flag)) break;
+                if (!wait_bar(full(s), par, abort_flag, mma_slices) ||
+                    !wait_bar(aready(s), par, abort_flag, mma_slices))
+                    break;
                 tc_fence_after();
                 const uint32_t da = tmem + (uint32_t)(A_COL0 + s * (BK / 2));
                 const uint64_t db = db0 + (uint64_t)((s * STAGE) >> 4);
@@ -313,7 +322,7 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                     const uint32_t b = (uint32_t)g & 1u;
                     const bool gstart = (kb & (BPG - 1)) == 0;
                     if (gstart) {
-                        if (!wait_bar(tempty(b), ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag)) break;
+                        if (!wait_bar(tempty(b), ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag, mma_slices)) break;
                         tc_fence_after();
                     }
                     mmas(da, db, b, 0, BK / 16, gstart);
@@ -324,7 +333,8 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                     const int halves = (k - kb * BK) >= BK ? 2 : 1;
                     for (int hh = 0; hh < halves && ok; ++hh) {
                         const int g = 2 * kb + hh;
-                        if (!wait_bar(tempty((uint32_t)hh), ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag)) {
+                        if (!wait_bar(tempty((uint32_t)hh), ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag,
+                                      mma_slices)) {
                             ok = false;
                             break;
                         }
@@ -611,7 +621,8 @@ wq_status launch(const uint16_t* x, int64_t m, const int32_t* qweight, const int
     }
     const dim3 grid((unsigned)(((n + BM - 1) / BM) * ((m + BT - 1) / BT)));
     gptq_gemm_kernel<SYM, BF16OUT, G, UX><<<grid, THREADS, SMEM, st>>>(
-        xmap, qmap, qzeros, scales, (int)m, (int)n, (int)k, out, ux_packed, ux_zp, ux_group);
+        xmap, qmap, qzeros, scales, (int)m, (int)n, (int)k, out, ux_packed, ux_zp, ux_group,
+        g_mma_slices.load());
     return wqh::check_launch();
 }
 
@@ -647,6 +658,8 @@ wq_status dispatch_g(int group, bool sym, bool bf, const uint16_t* x, int64_t m,
 }  // namespace
 
 namespace wqh {
+unsigned gemm_mma_slices_exchange(unsigned slices) { return g_mma_slices.exchange(slices); }
+
 // Read and clear this file's device status word (0 when no wait ran out).
 unsigned gemm_status_take() {
     unsigned v = 0;

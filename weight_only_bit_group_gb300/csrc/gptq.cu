@@ -24,6 +24,7 @@
 // out records WQ_ERR_DEVICE_TIMEOUT in a device status word (read by
 // wq_device_status) and the kernel finishes without touching the stage again.
 #include <cudaTypedefs.h>
+#include <atomic>
 #include <mutex>
 
 #include "wq_common.cuh"
@@ -112,19 +113,25 @@ __device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst&
 __device__ unsigned g_device_status;  // WQ_ERR_DEVICE_TIMEOUT once a bounded wait ran out
 
 // Wait for phase `parity` of the mbarrier at shared address `bar`, giving up
-// after kMaxPolls polls (each poll may itself suspend for a while).
+// after `polls` polls (each poll may itself suspend for a while).
 constexpr unsigned kMaxPolls = 1u << 22;
-__device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity) {
-    for (unsigned i = 0; i < kMaxPolls; ++i)
+__device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity, unsigned polls) {
+    for (unsigned i = 0; i < polls; ++i)
         if (wq::mbar_try_wait(bar, parity)) return true;
     return false;
 }
+
+// Poll budget of the stage waits for the next launches (kernel argument; a
+// diagnostic lowers it to make the timeout path run, see wq_set_wait_budget).
+// The drain of loads still in flight after a timeout always uses kMaxPolls.
+std::atomic<unsigned> g_stage_polls{kMaxPolls};
 
 template <bool SYM, int G, bool SNR>
 __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_quant_kernel(
     const __grid_constant__ CUtensorMap wmap, int64_t n, int64_t k, int32_t* __restrict__ qweight,
     int32_t* __restrict__ qzeros, uint16_t* __restrict__ scales, int32_t* __restrict__ g_idx,
-    float4* __restrict__ slots, unsigned* __restrict__ counter, double* __restrict__ snr_db) {
+    float4* __restrict__ slots, unsigned* __restrict__ counter, double* __restrict__ snr_db,
+    unsigned max_polls) {
     using T = QTile<G>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // the 128-byte swizzle needs 1 KB aligned boxes
@@ -153,13 +160,17 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
     for (int c = 0; c < 8; ++c) roff8[c] = (uint32_t)(half * (T::NB / 2) * T::BOXB + row * 128 + 16 * (c ^ (row & 7)));
 #define WQ_CHUNK(c) (*reinterpret_cast<const uint4*>(stage + roff8[(c) & 7] + ((c) >> 3) * T::BOXB))
 
+    unsigned inflight = 0;  // bit i: a load into stage i has been issued and not yet waited for
     auto issue = [&](int nb, int kb, int st) {
-        if (lane == 0 && nb < tn) {
-            const uint32_t bar = bar_s + 8 * st, dst = wsm_s + st * T::STAGE;
-            wq::mbar_expect_tx(bar, T::STAGE);
+        if (nb < tn) {  // warp-uniform
+            if (lane == 0) {
+                const uint32_t bar = bar_s + 8 * st, dst = wsm_s + st * T::STAGE;
+                wq::mbar_expect_tx(bar, T::STAGE);
 #pragma unroll
-            for (int b = 0; b < T::NB; ++b)
-                wq::tma_load_2d(dst + b * T::BOXB, &wmap, kb * T::KT + 64 * b, nb * T::R, bar);
+                for (int b = 0; b < T::NB; ++b)
+                    wq::tma_load_2d(dst + b * T::BOXB, &wmap, kb * T::KT + 64 * b, nb * T::R, bar);
+            }
+            inflight |= 1u << st;
         }
     };
 
@@ -184,11 +195,12 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
         issue(na, ka, ahead);
         step(na, ka);
         ahead = ahead + 1 == T::NS ? 0 : ahead + 1;
-        if (!wait_stage(bar_s + 8 * st, parity)) {
+        if (!wait_stage(bar_s + 8 * st, parity, max_polls)) {
             atomicExch(&g_device_status, (unsigned)WQ_ERR_DEVICE_TIMEOUT);
             ok = false;
             break;
         }
+        inflight &= ~(1u << st);
         const int64_t n0 = (int64_t)nb * T::R, k0 = (int64_t)kb * T::KT;
         const int64_t col = n0 + row;
         const bool rowv = col < n;
@@ -313,9 +325,13 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
         if (++st == T::NS) { st = 0; parity ^= 1u; }
     }
     if (!ok && lane == 0) {
-        // loads may still be in flight into any stage: wait (bounded) for them
-        // before the CTA's shared memory can be handed to another CTA
-        for (int i = 0; i < T::NS; ++i) wait_stage(bar_s + 8 * i, 0), wait_stage(bar_s + 8 * i, 1);
+        // loads still in flight (the stage that timed out, the one ahead of it):
+        // wait for them with the full budget before the CTA's shared memory can be
+        // handed to another CTA.  Stages are used round-robin, so a stage at or
+        // after the current one completes with the current parity, one before it
+        // (already refilled for the next round) with the other.
+        for (int i = 0; i < T::NS; ++i)
+            if ((inflight >> i) & 1u) wait_stage(bar_s + 8 * i, i >= st ? parity : parity ^ 1u, kMaxPolls);
     }
     __syncwarp();
     if (SNR) wq::finish_snr(wq::ff_of(ksw), wq::ff_of(kse), slots, counter, snr_db, nullptr);
@@ -374,7 +390,7 @@ wq_status launch_quant(const uint16_t* w, int64_t n, int64_t k, int32_t* qweight
     const int grid = wqh::grid_for(fn, T::THREADS, T::SMEM, (warp_tiles + T::WARPS - 1) / T::WARPS,
                                    wqh::kMaxPartials);
     gptq_quant_kernel<SYM, G, SNR><<<grid, T::THREADS, T::SMEM, st>>>(
-        map, n, k, qweight, qzeros, scales, g_idx, slots, counter, snr_db);
+        map, n, k, qweight, qzeros, scales, g_idx, slots, counter, snr_db, g_stage_polls.load());
     return wqh::check_launch();
 }
 
@@ -648,3 +664,7 @@ extern "C" wq_status wq_device_status(void) {
     s = wqh::cuda_status(cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero)));
     return s != WQ_OK ? s : (wq_status)v;
 }
+
+namespace wqh {
+unsigned gptq_stage_polls_exchange(unsigned polls) { return g_stage_polls.exchange(polls); }
+}  // namespace wqh

@@ -12,6 +12,13 @@
 //   store  one uint32 of 8 nibbles per lane (128 B per warp), one e8m0 byte per
 //          block.
 // HBM bound: 2 B read + 0.53 B written per weight.
+//
+// mxfp4_quantize_err runs the same kernel with ERR = 1: each lane also decodes
+// its codes back (hardware e2m1 -> f16x2, times 2^exp: the values
+// dequantize_mxfp4 returns), forms the binary32 terms w^2 and (w - deq)^2 that
+// quantize_dflash_mxfp4.py main() reduces into its relative error, and the grid
+// finishes both sums with the last-CTA float-float reduction: no second read of
+// w and no dequantized tensor in memory.
 #include "wq_common.cuh"
 
 namespace {
@@ -40,6 +47,21 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
     return r;
 }
 
+// Two e2m1 nibbles of one byte -> two binary32 magnitudes with sign (exact).
+__device__ __forceinline__ void e2m1x2_to_f(uint32_t byte, float& lo, float& hi) {
+    uint32_t h2;
+    uint16_t in = (uint16_t)byte;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "h"(in));
+    lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+    hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+}
+
+// 2^(e - 127) in binary32: e = 0 is the subnormal 2^-127, e = 255 is inf
+// (as exp2(128.0) is in binary32).
+__device__ __forceinline__ float e8m0_scale(uint32_t e) {
+    return __uint_as_float(e == 0 ? 0x00400000u : (e << 23));
+}
+
 // Page-literal tie rewrite: exact midpoints 0.75, 1.75 and 3.5 go two grid steps
 // down from the half-even choice ((argmin // 2) * 2 with argmin the lower
 // neighbour); the other midpoints already agree with half-even.
@@ -56,17 +78,36 @@ __device__ __forceinline__ uint32_t code_pair(float x0, float x1, float inv) {
     return b;
 }
 
-template <int TIE>
+// Error terms of one packed pair: sw += x*x, se += (x - deq)^2 with deq = e2m1
+// value * 2^exp.  x - deq is formed by one FMA of the exact product q * 2^exp
+// (a power-of-two scaling, never rounded for these magnitudes), so it is the
+// binary32 difference the page's (deq - w) computes.
+__device__ __forceinline__ void err_pair(uint32_t xbits, uint32_t byte, wq::f2_t ns2, wq::f2_t& sw,
+                                         wq::f2_t& se) {
+    float q0, q1;
+    e2m1x2_to_f(byte, q0, q1);
+    const wq::f2_t x = wq::bf2_to_f2(xbits);
+    const wq::f2_t d = wq::fma2(wq::f2(q0, q1), ns2, x);
+    se = wq::fma2(d, d, se);
+    sw = wq::fma2(x, x, sw);
+}
+
+template <int TIE, int ERR>
 __global__ void __launch_bounds__(kThreads) mxfp4_quant_kernel(const uint4* __restrict__ w,
                                                                int64_t nchunks,
                                                                uint32_t* __restrict__ packed,
-                                                               uint8_t* __restrict__ e8m0) {
+                                                               uint8_t* __restrict__ e8m0,
+                                                               float4* __restrict__ slots,
+                                                               unsigned* __restrict__ counter,
+                                                               double* __restrict__ snr_db,
+                                                               double* __restrict__ rel_err) {
     // two pipeline stages of kUnroll 16-byte chunks, private to each thread
     __shared__ __align__(16) uint4 stage_buf[2][kUnroll][kThreads];
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
     const int64_t step = nwarps * 32 * kUnroll;
+    wq::KSum dw, de;
 
     auto issue = [&](int64_t wb, int st) {
 #pragma unroll
@@ -92,6 +133,7 @@ __global__ void __launch_bounds__(kThreads) mxfp4_quant_kernel(const uint4* __re
             ch[u] = wb + (int64_t)u * nwarps * 32 + lane;
             v[u] = ch[u] < nchunks ? stage_buf[j & 1][u][threadIdx.x] : make_uint4(0, 0, 0, 0);
         }
+        wq::f2_t sw = wq::f2(0.f, 0.f), se = wq::f2(0.f, 0.f);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const uint32_t M = 0x7fff7fffu;
@@ -105,28 +147,27 @@ __global__ void __launch_bounds__(kThreads) mxfp4_quant_kernel(const uint4* __re
             word |= code_pair<TIE>(wq::bf_lo(v[u].y), wq::bf_hi(v[u].y), inv) << 8;
             word |= code_pair<TIE>(wq::bf_lo(v[u].z), wq::bf_hi(v[u].z), inv) << 16;
             word |= code_pair<TIE>(wq::bf_lo(v[u].w), wq::bf_hi(v[u].w), inv) << 24;
+            if (ERR) {
+                // lanes past the end hold zeros: zero codes, zero terms
+                const float ns = -e8m0_scale((uint32_t)(ex + 127));
+                const wq::f2_t ns2 = wq::f2(ns, ns);
+                err_pair(v[u].x, word & 0xffu, ns2, sw, se);
+                err_pair(v[u].y, (word >> 8) & 0xffu, ns2, sw, se);
+                err_pair(v[u].z, (word >> 16) & 0xffu, ns2, sw, se);
+                err_pair(v[u].w, word >> 24, ns2, sw, se);
+            }
             if (ch[u] < nchunks) {
                 packed[ch[u]] = word;
                 if ((lane & 3) == 0) e8m0[ch[u] >> 2] = (uint8_t)(ex + 127);
             }
         }
+        if (ERR) {
+            dw.add(__fadd_rn(sw.x, sw.y));
+            de.add(__fadd_rn(se.x, se.y));
+        }
     }
     wq::cp_async_wait<0>();
-}
-
-// Two e2m1 nibbles of one byte -> two binary32 magnitudes with sign (exact).
-__device__ __forceinline__ void e2m1x2_to_f(uint32_t byte, float& lo, float& hi) {
-    uint32_t h2;
-    uint16_t in = (uint16_t)byte;
-    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "h"(in));
-    lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
-    hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
-}
-
-// 2^(e - 127) in binary32: e = 0 is the subnormal 2^-127, e = 255 is inf
-// (as exp2(128.0) is in binary32).
-__device__ __forceinline__ float e8m0_scale(uint32_t e) {
-    return __uint_as_float(e == 0 ? 0x00400000u : (e << 23));
+    if (ERR) wq::finish_snr(wq::ff_of(dw), wq::ff_of(de), slots, counter, snr_db, rel_err);
 }
 
 template <int OUT_BF16>
@@ -174,6 +215,26 @@ __global__ void __launch_bounds__(kThreads) mxfp4_dequant_kernel(const uint32_t*
     }
 }
 
+template <int TIE, int ERR>
+wq_status launch_quant(const uint16_t* w, int64_t nchunks, uint8_t* packed, uint8_t* e8m0,
+                       void* workspace, double* snr_db, double* rel_err, cudaStream_t st) {
+    const void* fn = (const void*)mxfp4_quant_kernel<TIE, ERR>;
+    // with the error sums every CTA owns one partial-sum slot
+    const int grid = wqh::grid_for(fn, kThreads, 0, (nchunks + kThreads - 1) / kThreads,
+                                   ERR ? wqh::kMaxPartials : 1 << 30);
+    unsigned* counter = nullptr;
+    float4* slots = nullptr;
+    if (ERR) {
+        counter = (unsigned*)workspace;
+        slots = (float4*)((char*)workspace + wqh::kCtrlBytes);
+        wq_status s = wqh::cuda_status(cudaMemsetAsync(counter, 0, sizeof(unsigned), st));
+        if (s != WQ_OK) return s;
+    }
+    mxfp4_quant_kernel<TIE, ERR><<<grid, kThreads, 0, st>>>((const uint4*)w, nchunks, (uint32_t*)packed,
+                                                            e8m0, slots, counter, snr_db, rel_err);
+    return wqh::check_launch();
+}
+
 }  // namespace
 
 extern "C" wq_status mxfp4_quantize(const uint16_t* w, int64_t n, int64_t k, int tie_mode,
@@ -185,18 +246,29 @@ extern "C" wq_status mxfp4_quantize(const uint16_t* w, int64_t n, int64_t k, int
     if (!wqh::aligned16(w) || !wqh::aligned16(packed)) return WQ_ERR_MISALIGNED;
     const int64_t nchunks = n * k / 8;
     cudaStream_t st = (cudaStream_t)stream;
-    if (tie_mode == WQ_TIE_HALF_EVEN) {
-        int grid = wqh::grid_for((const void*)mxfp4_quant_kernel<WQ_TIE_HALF_EVEN>, kThreads, 0,
-                                 (nchunks + kThreads - 1) / kThreads, 1 << 30);
-        mxfp4_quant_kernel<WQ_TIE_HALF_EVEN><<<grid, kThreads, 0, st>>>(
-            (const uint4*)w, nchunks, (uint32_t*)packed, e8m0);
-    } else {
-        int grid = wqh::grid_for((const void*)mxfp4_quant_kernel<WQ_TIE_PAGE_LITERAL>, kThreads, 0,
-                                 (nchunks + kThreads - 1) / kThreads, 1 << 30);
-        mxfp4_quant_kernel<WQ_TIE_PAGE_LITERAL><<<grid, kThreads, 0, st>>>(
-            (const uint4*)w, nchunks, (uint32_t*)packed, e8m0);
-    }
-    return wqh::check_launch();
+    if (tie_mode == WQ_TIE_HALF_EVEN)
+        return launch_quant<WQ_TIE_HALF_EVEN, 0>(w, nchunks, packed, e8m0, nullptr, nullptr, nullptr, st);
+    return launch_quant<WQ_TIE_PAGE_LITERAL, 0>(w, nchunks, packed, e8m0, nullptr, nullptr, nullptr, st);
+}
+
+extern "C" wq_status mxfp4_quantize_err(const uint16_t* w, int64_t n, int64_t k, int tie_mode,
+                                        uint8_t* packed, uint8_t* e8m0, double* snr_db,
+                                        double* rel_err, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+    if (!snr_db && !rel_err) return mxfp4_quantize(w, n, k, tie_mode, packed, e8m0, stream);
+    if (n < 0 || k < 0 || k % 32 != 0) return WQ_ERR_BAD_SHAPE;
+    if (tie_mode != WQ_TIE_HALF_EVEN && tie_mode != WQ_TIE_PAGE_LITERAL) return WQ_ERR_UNSUPPORTED;
+    if (n == 0 || k == 0) return WQ_OK;
+    if (!w || !packed || !e8m0 || !workspace) return WQ_ERR_NULL_PTR;
+    if (workspace_bytes < wq_workspace_bytes(WQ_OP_MXFP4_ERR, n, k, 0)) return WQ_ERR_WORKSPACE_TOO_SMALL;
+    if (!wqh::aligned16(w) || !wqh::aligned16(packed) || !wqh::aligned_to(workspace, 16) ||
+        (snr_db && !wqh::aligned_to(snr_db, 8)) || (rel_err && !wqh::aligned_to(rel_err, 8)))
+        return WQ_ERR_MISALIGNED;
+    const int64_t nchunks = n * k / 8;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (tie_mode == WQ_TIE_HALF_EVEN)
+        return launch_quant<WQ_TIE_HALF_EVEN, 1>(w, nchunks, packed, e8m0, workspace, snr_db, rel_err, st);
+    return launch_quant<WQ_TIE_PAGE_LITERAL, 1>(w, nchunks, packed, e8m0, workspace, snr_db, rel_err, st);
 }
 
 extern "C" wq_status mxfp4_dequantize(const uint8_t* packed, const uint8_t* e8m0, int64_t n,

@@ -22,6 +22,12 @@
 // bf16 arithmetic: every page step is the binary32 operation on bf16 operands
 // rounded once to bf16 (cvt.rn).  w * (1/scale) is an exact binary32 product of
 // two bf16 values, so rounding it with cvt.rn.bf16 reproduces the bf16 multiply.
+//
+// uintx_quantize_err runs the same kernels with ERR = 1: from the code bytes in
+// registers each lane rebuilds the page's bf16 dequantized value
+// (_dequantize_native: bf16(bf16(q - zp) * scale)) and accumulates the binary32
+// terms w^2 and (w - deq)^2; the grid finishes both sums with the last-CTA
+// float-float reduction, so the reconstruction error costs no second pass.
 #include "wq_common.cuh"
 
 namespace {
@@ -104,11 +110,26 @@ __device__ __forceinline__ void store_shards(const uint32_t (&blo)[8], const uin
     }
 }
 
-template <int NBITS>
+// Error terms of one packed pair: x the two bf16 weights, r the two bf16 values
+// q - zp (exact integers), s2 the group's bf16 scale in both halves.
+__device__ __forceinline__ void err_pair(uint32_t x, uint32_t r, uint32_t s2, wq::f2_t& sw,
+                                         wq::f2_t& se) {
+    const wq::f2_t xf = wq::bf2_to_f2(x);
+    const wq::f2_t df = wq::bf2_to_f2(wq::bmul2(r, s2));  // the page's bf16 deq
+    const wq::f2_t d = wq::fma2(df, wq::f2(-1.0f, -1.0f), xf);  // RN(x - deq)
+    se = wq::fma2(d, d, se);
+    sw = wq::fma2(xf, xf, sw);
+}
+
+template <int NBITS, int ERR>
 __global__ void __launch_bounds__(kThreads, 2) uintx_quant_fused(const uint16_t* __restrict__ w,
                                                                  int64_t numel, uint8_t* __restrict__ packed,
                                                                  uint16_t* __restrict__ scale,
-                                                                 uint8_t* __restrict__ zp) {
+                                                                 uint8_t* __restrict__ zp,
+                                                                 float4* __restrict__ slots,
+                                                                 unsigned* __restrict__ counter,
+                                                                 double* __restrict__ snr_db,
+                                                                 double* __restrict__ rel_err) {
     constexpr int QMAX = (1 << NBITS) - 1;
     // two pipeline stages x 8 segments x 16 bytes, private to each thread
     extern __shared__ __align__(16) uint4 dyn_smem[];
@@ -118,6 +139,7 @@ __global__ void __launch_bounds__(kThreads, 2) uintx_quant_fused(const uint16_t*
     const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
     const int64_t items = (L1 + 255) / 256;
+    wq::KSum dw, de;
 
     auto issue = [&](int64_t it, int st) {
         const int64_t d = it * 256 + 8 * lane;
@@ -172,9 +194,12 @@ __global__ void __launch_bounds__(kThreads, 2) uintx_quant_fused(const uint16_t*
         const uint32_t mine = qp.inv_bits | (qp.zp << 16);
 
         uint32_t blo[8], bhi[8];
+        wq::f2_t sw = wq::f2(0.f, 0.f), se = wq::f2(0.f, 0.f);
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             const uint32_t P = __shfl_sync(0xffffffffu, mine, (lane & ~7) | m);
+            // the group's scale (bf16) in both halves, for the error terms only
+            const uint32_t s2 = ERR ? __shfl_sync(0xffffffffu, qp.scale_bits, (lane & ~7) | m) * 0x10001u : 0u;
             const uint32_t z = P >> 16;
             // bf16(w * inv) clamped to [-zp, qmax - zp] (bf16x2, exact bounds)
             const uint32_t inv2 = (P & 0xffffu) * 0x10001u;
@@ -193,6 +218,11 @@ __global__ void __launch_bounds__(kThreads, 2) uintx_quant_fused(const uint16_t*
                 for (int i = 0; i < 4; ++i) q[i] = wq::badd2(q[i], kB192x2);
                 blo[m] = __byte_perm(q[0], q[1], 0x6420) + zadd;
                 bhi[m] = __byte_perm(q[2], q[3], 0x6420) + zadd;
+                if (ERR) {
+                    // (192 + round(.)) - 192 = the exact integer q - zp, in bf16
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) err_pair(u[i], wq::bsub2(q[i], kB192x2), s2, sw, se);
+                }
             } else {
                 // + (1.5 * 2^23 + 128) in binary32: the adder rounds half to even (the
                 // offset is even) and the low byte of the sum is 128 + round(.)
@@ -201,17 +231,26 @@ __global__ void __launch_bounds__(kThreads, 2) uintx_quant_fused(const uint16_t*
                 uint32_t b[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    float t0, t1;
-                    wq::f2u(wq::add2(wq::bf2_to_f2(q[i]), M2), t0, t1);
-                    b[i] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x0040);
+                    const wq::f2_t t = wq::add2(wq::bf2_to_f2(q[i]), M2);
+                    b[i] = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x0040);
+                    if (ERR) {
+                        // t - (1.5 * 2^23 + 128) = the exact integer q - zp
+                        const wq::f2_t r = wq::add2(t, wq::f2(-(kMagic + 128.0f), -(kMagic + 128.0f)));
+                        err_pair(u[i], wq::f2_to_bf2(r.x, r.y), s2, sw, se);
+                    }
                 }
                 blo[m] = __byte_perm(b[0], b[1], 0x5410) + zadd;
                 bhi[m] = __byte_perm(b[2], b[3], 0x5410) + zadd;
             }
         }
         if (valid) store_shards<NBITS>(blo, bhi, packed, numel, L1, d);
+        if (ERR) {  // lanes past the end hold zeros: zero terms
+            dw.add(__fadd_rn(sw.x, sw.y));
+            de.add(__fadd_rn(se.x, se.y));
+        }
     }
     wq::cp_async_wait<0>();
+    if (ERR) wq::finish_snr(wq::ff_of(dw), wq::ff_of(de), slots, counter, snr_db, rel_err);
 }
 
 // ----------------------------------------------------------- general path
@@ -241,29 +280,48 @@ __global__ void __launch_bounds__(kThreads) uintx_qparams_kernel(const uint16_t*
     }
 }
 
-template <int NBITS>
+template <int NBITS, int ERR>
 __global__ void __launch_bounds__(kThreads) uintx_pack_general(const uint16_t* __restrict__ w,
                                                                int64_t numel, int group,
                                                                const uint16_t* __restrict__ scale,
                                                                const uint8_t* __restrict__ zp,
-                                                               uint8_t* __restrict__ packed) {
+                                                               uint8_t* __restrict__ packed,
+                                                               float4* __restrict__ slots,
+                                                               unsigned* __restrict__ counter,
+                                                               double* __restrict__ snr_db,
+                                                               double* __restrict__ rel_err) {
     using S = Shards<NBITS>;
     constexpr int QMAX = (1 << NBITS) - 1;
     const int64_t L1 = numel / 8;
     const int64_t base2 = S::has4 ? numel / 2 : 0;
     const int64_t base1 = base2 + (S::has2 ? numel / 4 : 0);
     const int64_t stride = (int64_t)gridDim.x * kThreads;
+    wq::KSum dw, de;
     for (int64_t d = (int64_t)blockIdx.x * kThreads + threadIdx.x; d < L1; d += stride) {
         uint32_t c[8];
+        float sw = 0.f, se = 0.f;
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             const int64_t e = m * L1 + d, g = e / group;
             const float sc = wq::bf_to_f(__ldg(scale + g));
             const uint32_t z = __ldg(zp + g);
             const float inv = wq::bfr(__fdiv_rn(1.0f, sc));
-            const float p = wq::bfr(__fmul_rn(wq::bf_to_f(__ldg(w + e)), inv));
+            const float x = wq::bf_to_f(__ldg(w + e));
+            const float p = wq::bfr(__fmul_rn(x, inv));
             const float pc = fminf(fmaxf(p, -(float)z), (float)(QMAX - (int)z));
-            c[m] = (uint32_t)(__float_as_int(__fadd_rn(pc, kMagic)) - 0x4B400000) + z;
+            const int r = __float_as_int(__fadd_rn(pc, kMagic)) - 0x4B400000;  // q - zp
+            c[m] = (uint32_t)r + z;
+            if (ERR) {
+                // _dequantize_native: bf16(q - zp) is exact, times the bf16 scale, one rounding
+                const float dq = wq::bfr(__fmul_rn((float)r, sc));
+                const float df = __fsub_rn(x, dq);
+                se = __fmaf_rn(df, df, se);
+                sw = __fmaf_rn(x, x, sw);
+            }
+        }
+        if (ERR) {
+            dw.add(sw);
+            de.add(se);
         }
         if (S::has4) {
 #pragma unroll
@@ -285,6 +343,7 @@ __global__ void __launch_bounds__(kThreads) uintx_pack_general(const uint16_t* _
             packed[base1 + d] = (uint8_t)b;
         }
     }
+    if (ERR) wq::finish_snr(wq::ff_of(dw), wq::ff_of(de), slots, counter, snr_db, rel_err);
 }
 
 // ----------------------------------------------------------- dequant
@@ -421,13 +480,30 @@ __global__ void __launch_bounds__(kThreads) uintx_dequant_general(const uint8_t*
     }
 }
 
-template <int NBITS>
+// Error outputs of uintx_quantize_err (all null for uintx_quantize).
+struct ErrOut {
+    void* workspace = nullptr;
+    double* snr_db = nullptr;
+    double* rel_err = nullptr;
+};
+
+template <int NBITS, int ERR>
 wq_status quant_nbits(const uint16_t* w, int64_t numel, int group, uint8_t* packed, uint16_t* scale,
-                      uint8_t* zp, cudaStream_t st) {
+                      uint8_t* zp, const ErrOut& eo, cudaStream_t st) {
     constexpr int QMAX = (1 << NBITS) - 1;
+    unsigned* counter = nullptr;
+    float4* slots = nullptr;
+    if (ERR) {
+        counter = (unsigned*)eo.workspace;
+        slots = (float4*)((char*)eo.workspace + wqh::kCtrlBytes);
+        wq_status s = wqh::cuda_status(cudaMemsetAsync(counter, 0, sizeof(unsigned), st));
+        if (s != WQ_OK) return s;
+    }
+    // with the error sums every CTA owns one partial-sum slot
+    const int cap = ERR ? wqh::kMaxPartials : 1 << 30;
     if (group == 64 && numel % 512 == 0) {
         const int64_t items = (numel / 8 + 255) / 256;  // one per warp
-        const void* fn = (const void*)uintx_quant_fused<NBITS>;
+        const void* fn = (const void*)uintx_quant_fused<NBITS, ERR>;
         constexpr int smem = 2 * 8 * kThreads * 16;
         static bool attr_set = false;
         if (!attr_set) {
@@ -436,8 +512,9 @@ wq_status quant_nbits(const uint16_t* w, int64_t numel, int group, uint8_t* pack
             if (s != WQ_OK) return s;
             attr_set = true;
         }
-        const int grid = wqh::grid_for(fn, kThreads, smem, (items + 7) / 8, 1 << 30);
-        uintx_quant_fused<NBITS><<<grid, kThreads, smem, st>>>(w, numel, packed, scale, zp);
+        const int grid = wqh::grid_for(fn, kThreads, smem, (items + 7) / 8, cap);
+        uintx_quant_fused<NBITS, ERR><<<grid, kThreads, smem, st>>>(w, numel, packed, scale, zp, slots,
+                                                                    counter, eo.snr_db, eo.rel_err);
         return wqh::check_launch();
     }
     const int64_t ngroups = numel / group;
@@ -447,10 +524,25 @@ wq_status quant_nbits(const uint16_t* w, int64_t numel, int group, uint8_t* pack
     wq_status s = wqh::check_launch();
     if (s != WQ_OK) return s;
     const int64_t L1 = numel / 8;
-    grid = wqh::grid_for((const void*)uintx_pack_general<NBITS>, kThreads, 0,
-                         (L1 + kThreads - 1) / kThreads, 1 << 30);
-    uintx_pack_general<NBITS><<<grid, kThreads, 0, st>>>(w, numel, group, scale, zp, packed);
+    grid = wqh::grid_for((const void*)uintx_pack_general<NBITS, ERR>, kThreads, 0,
+                         (L1 + kThreads - 1) / kThreads, cap);
+    uintx_pack_general<NBITS, ERR><<<grid, kThreads, 0, st>>>(w, numel, group, scale, zp, packed, slots,
+                                                              counter, eo.snr_db, eo.rel_err);
     return wqh::check_launch();
+}
+
+template <int ERR>
+wq_status quant_dispatch(const uint16_t* w, int64_t numel, int nbits, int group, uint8_t* packed,
+                         uint16_t* scale, uint8_t* zp, const ErrOut& eo, cudaStream_t st) {
+    switch (nbits) {
+        case 2: return quant_nbits<2, ERR>(w, numel, group, packed, scale, zp, eo, st);
+        case 3: return quant_nbits<3, ERR>(w, numel, group, packed, scale, zp, eo, st);
+        case 4: return quant_nbits<4, ERR>(w, numel, group, packed, scale, zp, eo, st);
+        case 5: return quant_nbits<5, ERR>(w, numel, group, packed, scale, zp, eo, st);
+        case 6: return quant_nbits<6, ERR>(w, numel, group, packed, scale, zp, eo, st);
+        case 7: return quant_nbits<7, ERR>(w, numel, group, packed, scale, zp, eo, st);
+        default: return WQ_ERR_UNSUPPORTED;
+    }
 }
 
 template <int NBITS, bool BF16>
@@ -489,17 +581,28 @@ extern "C" wq_status uintx_quantize(const uint16_t* w, int64_t n, int64_t k, int
     if (!w || !packed || !scale || !zp) return WQ_ERR_NULL_PTR;
     if (!wqh::aligned16(w) || !wqh::aligned16(packed) || !wqh::aligned_to(scale, 2))
         return WQ_ERR_MISALIGNED;
-    const int64_t numel = n * k;
-    cudaStream_t st = (cudaStream_t)stream;
-    switch (nbits) {
-        case 2: return quant_nbits<2>(w, numel, group, packed, scale, zp, st);
-        case 3: return quant_nbits<3>(w, numel, group, packed, scale, zp, st);
-        case 4: return quant_nbits<4>(w, numel, group, packed, scale, zp, st);
-        case 5: return quant_nbits<5>(w, numel, group, packed, scale, zp, st);
-        case 6: return quant_nbits<6>(w, numel, group, packed, scale, zp, st);
-        case 7: return quant_nbits<7>(w, numel, group, packed, scale, zp, st);
-        default: return WQ_ERR_UNSUPPORTED;
-    }
+    return quant_dispatch<0>(w, n * k, nbits, group, packed, scale, zp, ErrOut{}, (cudaStream_t)stream);
+}
+
+extern "C" wq_status uintx_quantize_err(const uint16_t* w, int64_t n, int64_t k, int nbits, int group,
+                                        uint8_t* packed, uint16_t* scale, uint8_t* zp, double* snr_db,
+                                        double* rel_err, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+    if (!snr_db && !rel_err) return uintx_quantize(w, n, k, nbits, group, packed, scale, zp, stream);
+    wq_status s = check_common(n, k, nbits, group);
+    if (s != WQ_OK) return s;
+    if (n == 0 || k == 0) return WQ_OK;
+    if (!w || !packed || !scale || !zp || !workspace) return WQ_ERR_NULL_PTR;
+    if (workspace_bytes < wq_workspace_bytes(WQ_OP_UINTX_ERR, n, k, nbits)) return WQ_ERR_WORKSPACE_TOO_SMALL;
+    if (!wqh::aligned16(w) || !wqh::aligned16(packed) || !wqh::aligned_to(scale, 2) ||
+        !wqh::aligned_to(workspace, 16) || (snr_db && !wqh::aligned_to(snr_db, 8)) ||
+        (rel_err && !wqh::aligned_to(rel_err, 8)))
+        return WQ_ERR_MISALIGNED;
+    ErrOut eo;
+    eo.workspace = workspace;
+    eo.snr_db = snr_db;
+    eo.rel_err = rel_err;
+    return quant_dispatch<1>(w, n * k, nbits, group, packed, scale, zp, eo, (cudaStream_t)stream);
 }
 
 extern "C" wq_status uintx_dequantize(const uint8_t* packed, const uint16_t* scale, const uint8_t* zp,

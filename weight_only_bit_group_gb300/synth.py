@@ -80,6 +80,19 @@ def small_gptq(seed: int = 1, device="cpu") -> torch.Tensor:
     return normal_bf16((256, 512), 0.02, seed, device)
 
 
+def gptq_packed(n: int, k: int, group: int, seed: int, device="cpu"):
+    """Random stored GPTQ tensors of an [n, k] weight, as a checkpoint would hold
+    them: qweight int32 [k/8, n] and qzeros int32 [k/group, n/8] with uniformly
+    random nibbles (every code and zero point), scales fp16 [k/group, n] drawn
+    LogNormal around 0.0025 (the scale of N(0, 0.02) weights at 4 bits).
+    -> (qweight, qzeros, scales)."""
+    g = _gen(seed, "cpu")
+    qw = torch.randint(-2 ** 31, 2 ** 31, (k // 8, n), generator=g, dtype=torch.int64).to(torch.int32)
+    qz = torch.randint(-2 ** 31, 2 ** 31, (k // group, n // 8), generator=g, dtype=torch.int64).to(torch.int32)
+    sc = (torch.randn((k // group, n), generator=g) + math.log(0.0025)).exp_().to(torch.float16)
+    return qw.to(device), qz.to(device), sc.to(device)
+
+
 def mxfp4_gate_up(seed: int = 3, device="cpu", shape=GATE_UP_SHAPE) -> torch.Tensor:
     n, k = shape
     return outlier_blocks_bf16(n, k, 0.015, 0.01, 50.0, seed, 32, device)
