@@ -9,9 +9,9 @@ weights, N(0, 0.02) with 0.5% outlier input columns), all inputs resident in HBM
   GPTQ asym dequantize -> bf16 [N,K]           gptq_dequantize      x7
   GPTQ sym  int4 quantize+pack (+ fused SNR)   gptq_quantize_sym    x7
   GPTQ sym  dequantize -> bf16 [N,K]           gptq_dequantize      x7
-  MXFP4 quantize (half-even ties)              mxfp4_quantize       x7
+  MXFP4 quantize (half-even ties) + fused      mxfp4_quantize_err   x7
+    reconstruction SNR / rel. error
   MXFP4 dequantize -> bf16                     mxfp4_dequantize     x7
-  MXFP4 reconstruction SNR / rel. error        quant_snr            x7
   uintx4 quantize + shard pack (group 64)      uintx_quantize       x7
   uintx4 unpack + dequantize -> bf16           uintx_dequantize     x7
   AWQ alpha search (gate||up, 2048 rows, 11 a) awq_search           x1
@@ -31,6 +31,12 @@ followed by a 256 MB read (outside the events, leaving no dirty lines; the
 inputs, 436 MB, exceed L2 anyway); a barrier and torch.cuda.synchronize() on
 both sides of the K timed steps; max over ranks.  Per-phase events (on the
 joining stream) give each phase's duration for the roofline.
+
+The same JSON line also carries the other large configurations, each kernel
+timed alone (graph replay between L2 flushes, CUDA events; `configs` key):
+MXFP4 quantize (+ fused error) and dequantize of gate_up [34816, 5120], the AWQ
+search on that tensor (2048-row stride-17 subsample, 11 alphas; ALU roofline)
+and uintx quantize / dequantize of 8 layers (1.745 G weights) at nbits 2..7.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -191,7 +197,7 @@ class Workload:
             for tag in ("asym", "sym"):
                 o[tag]["g_idx"] = torch.empty(k, dtype=torch.int32, device=device)
                 o[tag]["ws"] = wq.workspace(wq.WQ_OP_GPTQ_QUANTIZE, n, k, GROUP_GPTQ, device)
-            o["snr"]["ws"] = wq.workspace(wq.WQ_OP_QUANT_SNR, n, k, 0, device)
+            o["snr"]["ws"] = wq.workspace(wq.WQ_OP_MXFP4_ERR, n, k, 0, device)
             self.out.append(o)
         n, k = self.gate_up.shape
         self.awq_out = dict(best_s=torch.empty(k, dtype=torch.float32, device=device),
@@ -268,19 +274,19 @@ class Workload:
             P.append((f"gptq_dequantize_{tag}", *each(d)[:1], dbytes, 2 * self.numel, len(layer), each(d)[1]))
 
         def mq(i, w):
-            o = self.out[i]["mx"]
-            wq.mxfp4_quantize(w, 0, packed=o["packed"], e8m0=o["e8m0"])
+            # quantize_mxfp4 plus main()'s relative error of the same pass
+            o, s = self.out[i]["mx"], self.out[i]["snr"]
+            wq.mxfp4_quantize(w, 0, packed=o["packed"], e8m0=o["e8m0"], err=True, snr_db=s["snr_db"],
+                              rel_err=s["rel_err"], ws=s["ws"])
 
         def md(i, w):
             o = self.out[i]["mx"]
             wq.mxfp4_dequantize(o["packed"], o["e8m0"], torch.bfloat16, out=self.deq[i])
-            s = self.out[i]["snr"]
-            wq.quant_snr(w, self.deq[i], "nk", snr_db=s["snr_db"], rel_err=s["rel_err"], ws=s["ws"])
 
         mx_q = sum(2 * w.numel() + w.numel() // 2 + w.numel() // 32 for _, w in layer)
-        mx_d = sum(w.numel() // 2 + w.numel() // 32 + 2 * w.numel() + 4 * w.numel() for _, w in layer)
-        P.append(("mxfp4_quantize", *each(mq)[:1], mx_q, 2 * self.numel, len(layer), each(mq)[1]))
-        P.append(("mxfp4_dequantize+quant_snr", *each(md)[:1], mx_d, 2 * self.numel, 2 * len(layer), each(md)[1]))
+        mx_d = sum(w.numel() // 2 + w.numel() // 32 + 2 * w.numel() for _, w in layer)
+        P.append(("mxfp4_quantize+err", *each(mq)[:1], mx_q, 2 * self.numel, len(layer), each(mq)[1]))
+        P.append(("mxfp4_dequantize", *each(md)[:1], mx_d, 2 * self.numel, len(layer), each(md)[1]))
 
         def uq(i, w):
             o = self.out[i]["ux"]
@@ -332,7 +338,7 @@ def source_sha(kernel_files) -> str:
 
 PHASE_SOURCE = {"gptq_quantize_asym": ["gptq.cu"], "gptq_quantize_sym": ["gptq.cu"],
                 "gptq_dequantize_asym": ["gptq.cu"], "gptq_dequantize_sym": ["gptq.cu"],
-                "mxfp4_quantize": ["mxfp4.cu"], "mxfp4_dequantize+quant_snr": ["mxfp4.cu", "snr.cu"],
+                "mxfp4_quantize+err": ["mxfp4.cu"], "mxfp4_dequantize": ["mxfp4.cu"],
                 "uintx_quantize": ["uintx.cu"], "uintx_dequantize": ["uintx.cu"], "awq_search": ["awq.cu"]}
 
 
@@ -375,6 +381,154 @@ def l2_flusher(dev):
         torch.sum(clean, 0, out=sink)
 
     return flush
+
+
+# ---------------------------------------------------------------- other configs
+def time_captured(call, flush, reps=10, warm=3):
+    """Mean CUDA-event time (ms) of one replay of `call` captured as a CUDA graph,
+    with L2 flushed before every replay (the events sit on the launching stream)."""
+    call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    times = []
+    for i in range(warm + reps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        if i >= warm:
+            times.append(a.elapsed_time(b))
+    del graph
+    return statistics.mean(times)
+
+
+def fork_join(calls, streams):
+    """Issue calls[j] on streams[j % len(streams)], forked from and joined back to
+    the current stream (graph branches when captured)."""
+    main = torch.cuda.current_stream()
+    fork = torch.cuda.Event()
+    fork.record(main)
+    for st in streams:
+        st.wait_event(fork)
+    for j, c in enumerate(calls):
+        with torch.cuda.stream(streams[j % len(streams)]):
+            c()
+    for st in streams:
+        e = torch.cuda.Event()
+        e.record(st)
+        main.wait_event(e)
+
+
+def hbm_entry(alg_bytes, ms, peak, kind):
+    gbs = alg_bytes / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 4), "alg_bytes": int(alg_bytes), "alg_GBps": round(gbs, 1),
+            "frac_of_" + kind: round(gbs / peak, 4)}
+
+
+# FP32 operations per (subsampled weight, alpha) of the AWQ search, as the scope
+# table of the search counts them: W*s, |.| max, the scaling by 2^-exp, the
+# nearest-e2m1 choice, the dequant multiply, the division by s, the subtraction,
+# the activation weight, the square and the sum.
+AWQ_OPS_PER_WEIGHT_ALPHA = 12
+FP32_LANES_PER_SM = 128
+
+
+def fp32_peak_tops(dev):
+    """FP32 lane-operation peak (T op/s): SMs x 128 FP32 lanes x the maximum SM
+    clock (an FMA counts as one operation)."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    mhz = 2070.0
+    if os.path.exists(path):
+        with open(path) as fh:
+            mhz = float(json.load(fh).get("sm_max_mhz", mhz))
+    return sms * FP32_LANES_PER_SM * mhz * 1e6 / 1e12, sms, mhz
+
+
+def time_configs(dev, flush, reps=10):
+    """The large configurations other than the step's layer, each kernel alone:
+    MXFP4 quantize (+ fused error) / dequantize of gate_up [34816, 5120] with 1% of
+    blocks x50; the AWQ search on that tensor; uintx quantize / dequantize of 8
+    layers at every nbits 2..7.  -> dict for the JSON line's `configs` key."""
+    import weight_only_bit_group_gb300 as wq
+    from weight_only_bit_group_gb300 import synth
+
+    peak, kind = peaks()
+    out = {}
+    # ---- MXFP4 on gate_up
+    w = synth.mxfp4_gate_up(device=dev)
+    n, k = w.shape
+    e = n * k
+    packed = torch.empty(n, k // 2, dtype=torch.uint8, device=dev)
+    e8 = torch.empty(n, k // 32, dtype=torch.uint8, device=dev)
+    snr = torch.empty((), dtype=torch.float64, device=dev)
+    rel = torch.empty((), dtype=torch.float64, device=dev)
+    ws = wq.workspace(wq.WQ_OP_MXFP4_ERR, n, k, 0, dev)
+    deq = torch.empty(n, k, dtype=torch.bfloat16, device=dev)
+    tq = time_captured(lambda: wq.mxfp4_quantize(w, 0, packed=packed, e8m0=e8, err=True, snr_db=snr,
+                                                 rel_err=rel, ws=ws), flush, reps)
+    tq0 = time_captured(lambda: wq.mxfp4_quantize(w, 0, packed=packed, e8m0=e8), flush, reps)
+    td = time_captured(lambda: wq.mxfp4_dequantize(packed, e8, torch.bfloat16, out=deq), flush, reps)
+    out["mxfp4_gate_up_34816x5120"] = {
+        "weights": e,
+        "mxfp4_quantize+err": hbm_entry(e * (2 + 0.5 + 1 / 32), tq, peak, kind),
+        "mxfp4_quantize": hbm_entry(e * (2 + 0.5 + 1 / 32), tq0, peak, kind),
+        "mxfp4_dequantize_bf16": hbm_entry(e * (0.5 + 1 / 32 + 2), td, peak, kind),
+        "rel_err": round(float(rel), 6)}
+    del deq, packed, e8
+    # ---- AWQ search on the same tensor (stride-17 subsample of 2048 rows)
+    a = synth.awq_activation(k, 4, dev)
+    o = dict(best_s=torch.empty(k, dtype=torch.float32, device=dev),
+             best_idx=torch.empty((), dtype=torch.int32, device=dev),
+             best_alpha=torch.empty((), dtype=torch.float32, device=dev),
+             errs=torch.empty(len(synth.ALPHAS), dtype=torch.float64, device=dev),
+             ws=wq.workspace(wq.WQ_OP_AWQ_SEARCH, n, k, len(synth.ALPHAS), dev))
+    ta = time_captured(lambda: wq.awq_search(w, a, synth.ALPHAS, 2048, 0, **o), flush, reps)
+    units = 2048 * k * len(synth.ALPHAS)
+    tops = AWQ_OPS_PER_WEIGHT_ALPHA * units / (ta * 1e-3) / 1e12
+    fpk, sms, mhz = fp32_peak_tops(dev)
+    out["awq_gate_up_34816x5120_2048rows_11alpha"] = {
+        "ms": round(ta, 4), "alg_bytes": 2048 * k * 2,
+        "alg_GBps": round(2048 * k * 2 / (ta * 1e-3) / 1e9, 1), "best_alpha": float(o["best_alpha"]),
+        "roofline": {"bound": "alu", "achieved": round(tops, 2), "peak": round(fpk, 2), "unit": "T FP32 op/s",
+                     "frac": round(tops / fpk, 4),
+                     "ops_per_unit": AWQ_OPS_PER_WEIGHT_ALPHA, "units": units,
+                     "peak_from": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x {mhz:.0f} MHz"}}
+    del w, o
+    # ---- uintx over 8 layers, every nbits
+    layers = [t for _, t in synth.uintx_layers(8, 5, dev)]
+    layers.sort(key=lambda t: -t.numel())
+    numel = sum(t.numel() for t in layers)
+    streams = [torch.cuda.Stream(dev) for _ in range(7)]
+    deqs = [torch.empty_like(t) for t in layers]
+    ux = {"weights": numel, "layers": 8, "group": 64}
+    for nbits in range(2, 8):
+        bufs = []
+        for t in layers:
+            nn, kk = t.shape
+            bufs.append((torch.empty(wq.uintx_packed_bytes(t.numel(), nbits), dtype=torch.uint8, device=dev),
+                         torch.empty(nn, kk // 64, dtype=torch.bfloat16, device=dev),
+                         torch.empty(nn, kk // 64, dtype=torch.uint8, device=dev)))
+        qcalls = [lambda t=t, b=b: wq.uintx_quantize(t, nbits, 64, packed=b[0], scale=b[1], zp=b[2])
+                  for t, b in zip(layers, bufs)]
+        dcalls = [lambda t=t, b=b, d=d: wq.uintx_dequantize(b[0], b[1], b[2], t.shape[0], t.shape[1], nbits, 64,
+                                                              torch.bfloat16, out=d)
+                  for t, b, d in zip(layers, bufs, deqs)]
+        tq = time_captured(lambda: fork_join(qcalls, streams), flush, reps)
+        td = time_captured(lambda: fork_join(dcalls, streams), flush, reps)
+        side = nbits / 8 + 3 / 64
+        ux[f"nbits{nbits}"] = {"uintx_quantize": hbm_entry(numel * (2 + side), tq, peak, kind),
+                               "uintx_dequantize_bf16": hbm_entry(numel * (side + 2), td, peak, kind)}
+        del bufs
+    out["uintx_8layers_h4096_i14336_kv1024"] = ux
+    del layers, deqs
+    torch.cuda.synchronize()
+    return out
 
 
 # ---------------------------------------------------------------- our arm
@@ -503,6 +657,10 @@ def run_ours(args, rank, world, dist):
                 "alg_bytes_per_launch": round(dom[2] / n_launch)}
     launches = sum(p[4] for p in phases) * args.steps
 
+    configs = None
+    if not args.no_configs:
+        configs = time_configs(dev, flush_l2)
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, wl, dev, dist, world)
@@ -515,6 +673,8 @@ def run_ours(args, rank, world, dist):
                 "LogNormal(0,1) activation means)",
         "config": {"workload": "gptq_layer_7proj_h4096_i14336_kv1024 (218,103,808 weights) "
                                "through every hot-path row",
+                   "other_configs_timed": "configs key: mxfp4 gate_up [34816,5120] (1% blocks x50), AWQ on it "
+                                          "(2048 rows stride 17, 11 alphas), uintx 8 layers nbits 2..7",
                    "weights_per_step": wl.numel, "weight_bytes_per_step": weight_bytes,
                    "gptq_group": GROUP_GPTQ, "uintx_nbits": NBITS_UINTX, "uintx_group": GROUP_UINTX,
                    "mxfp4_ties": "half_even", "awq": "gate||up [28672,4096] -> 2048 rows, 11 alphas",
@@ -528,6 +688,8 @@ def run_ours(args, rank, world, dist):
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 3),
     }
+    if configs is not None:
+        line["configs"] = configs
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -853,6 +1015,8 @@ def main():
                     help="weight type for --kernel gptq_quantize_* / mxfp4_quantize")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the MXFP4 / AWQ / 8-layer uintx timings of the other configurations")
     ap.add_argument("--no-graph", action="store_true", help="issue every call eagerly instead of a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
