@@ -909,6 +909,17 @@ def run_single(args):
         p, e = wq.mxfp4_quantize(w)
         call = lambda: wq.mxfp4_quantize(w, 0, packed=p, e8m0=e)
         alg = n * k * (esize + 0.5 + 1 / 32)
+    elif name == "mxfp4_quantize_err":
+        p, e, sn, re = wq.mxfp4_quantize(w, err=True)
+        ews = wq.workspace(wq.WQ_OP_MXFP4_ERR, n, k, 0, dev)
+        call = lambda: wq.mxfp4_quantize(w, 0, packed=p, e8m0=e, err=True, snr_db=sn, rel_err=re, ws=ews)
+        alg = n * k * (esize + 0.5 + 1 / 32)
+    elif name == "uintx_quantize_err":
+        p, sc, z, sn, re = wq.uintx_quantize(w, NBITS_UINTX, err=True)
+        ews = wq.workspace(wq.WQ_OP_UINTX_ERR, n, k, NBITS_UINTX, dev)
+        call = lambda: wq.uintx_quantize(w, NBITS_UINTX, packed=p, scale=sc, zp=z, err=True, snr_db=sn,
+                                         rel_err=re, ws=ews)
+        alg = n * k * (2 + NBITS_UINTX / 8 + 3 / 64)
     elif name == "mxfp4_dequantize":
         p, e = wq.mxfp4_quantize(w)
         out = torch.empty(n, k, dtype=torch.bfloat16, device=dev)

@@ -76,11 +76,25 @@ __device__ __forceinline__ uint32_t bound2(float v) {
     return b | (b << 16);
 }
 
+// bf16 pair -> two binary32 values through mixed-precision FMAs (w * 1 - 0, exact)
+// that read the bf16 halves in place: the unpacking runs on the FMA pipe, not on
+// the integer pipe that the clamps and the nibble pack already keep busy.
+__device__ __forceinline__ wq::f2_t bf2_to_f2_fma(uint32_t u) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h, one;\n\tmov.b32 {l, h}, %2;\n\tmov.b16 one, 0x3F80;\n\t"
+        "fma.rn.f32.bf16 %0, l, one, %3;\n\tfma.rn.f32.bf16 %1, h, one, %3;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(u), "f"(-0.0f));
+    return wq::f2(lo, hi);
+}
+
 // Codes of one 8-value chunk (one qweight word) and the SNR terms, on packed
 // binary32 pairs.  Per value: clamp (bf16x2, on w), q = RN(w/s) by reciprocal +
 // correction, t = rint(q) + 1.5*2^23 from the binary32 adder; the low bits of
 // t hold rint(q), and the word is sum over i of bits(t_i) << 4i plus the
 // per-group constant cg = (zp - bits(1.5*2^23)) * 0x11111111 (mod 2^32).
+// SNR terms as the page forms them: deq = RN((code - zp) * s), e = RN(w - deq)
+// (one mixed FMA reading w's bf16 half), e^2 and w^2 (mixed FMA) summed.
 template <bool SYM, bool SNR>
 __device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst& gc, const wq::f2_t R2,
                                                 const wq::f2_t NS2, uint32_t cg, wq::f2_t& sw2,
@@ -92,7 +106,7 @@ __device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst&
     for (int p = 0; p < 4; ++p) {
         uint32_t uc = wq::bmin2(u[p], gc.hi2);
         if (!SYM) uc = wq::bmax2(uc, gc.lo2);  // sym: w/s >= -8 always
-        const wq::f2_t x = wq::bf2_to_f2(uc);
+        const wq::f2_t x = bf2_to_f2_fma(uc);
         const wq::f2_t qa = wq::mul2(x, R2);
         const wq::f2_t rem = wq::fma2(qa, NS2, x);                          // x - qa*s, exact
         const wq::f2_t tq = wq::add2(wq::fma2(rem, R2, qa), M2);            // rint(RN(x/s)) + 1.5*2^23
@@ -101,10 +115,16 @@ __device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst&
         word += (uint32_t)__float_as_int(t0) << (8 * p);
         word += (uint32_t)__float_as_int(t1) << (8 * p + 4);
         if (SNR) {
-            const wq::f2_t xo = wq::bf2_to_f2(u[p]);
-            const wq::f2_t e = wq::fma2(wq::add2(tq, NM2), NS2, xo);       // w - (code - zp) * s
+            const wq::f2_t nd = wq::mul2(wq::add2(tq, NM2), NS2);  // -deq = -RN((code - zp) * s)
+            float e0, e1, w0, w1;
+            asm("{\n\t.reg .b16 l, h, one;\n\tmov.b32 {l, h}, %4;\n\tmov.b16 one, 0x3F80;\n\t"
+                "fma.rn.f32.bf16 %0, l, one, %5;\n\tfma.rn.f32.bf16 %1, h, one, %6;\n\t"
+                "fma.rn.f32.bf16 %2, l, l, %7;\n\tfma.rn.f32.bf16 %3, h, h, %8;\n\t}"
+                : "=f"(e0), "=f"(e1), "=f"(w0), "=f"(w1)
+                : "r"(u[p]), "f"(nd.x), "f"(nd.y), "f"(sw2.x), "f"(sw2.y));
+            const wq::f2_t e = wq::f2(e0, e1);  // RN(w - deq)
             se2 = wq::fma2(e, e, se2);
-            sw2 = wq::fma2(xo, xo, sw2);
+            sw2 = wq::f2(w0, w1);
         }
     }
     return word;
@@ -538,19 +558,27 @@ __global__ void __launch_bounds__(128) gptq_dequant_nk(const int32_t* __restrict
         const bool rowv = col < n;
         const int nw = (int)min((int64_t)KT, k - k0) / 8;  // qweight rows in this tile
         const int32_t* qp = qweight + (k0 / 8) * n + col;
-        uint32_t wd[16];
+        // every load of the tile is issued before the first use: the 16 qweight
+        // words and, per group, the fp16 scale and the qzeros word
+        uint32_t wd[16], sh[16], zw[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) wd[c] = (rowv && c < nw) ? wq::ld_stream1(qp + (int64_t)c * n) : 0u;
+        for (int c = 0; c < 16; ++c) {
+            const bool cv = rowv && c < nw;
+            wd[c] = cv ? wq::ld_stream1(qp + (int64_t)c * n) : 0u;
+            sh[c] = 0u;
+            zw[c] = 0u;
+            if ((c & cpg_mask) == 0 && cv) {  // first word of a group (uniform over the warp)
+                const int64_t g = (k0 + 8 * c) >> lg_group;
+                sh[c] = __ldg(scales + g * n + col);
+                if (!SYM) zw[c] = (uint32_t)__ldg(qzeros + g * (n / 8) + col / 8);
+            }
+        }
         wq::f2_t S2 = wq::f2(0.f, 0.f), Z2 = wq::f2(-kMagic - 8.f, -kMagic - 8.f);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
             if ((c & cpg_mask) == 0) {  // first word of a group (uniform)
-                const int64_t g = (k0 + 8 * c) >> lg_group;
-                float sv = 0.f, z = 8.f;
-                if (rowv && c < nw) {
-                    sv = __half2float(__ushort_as_half(__ldg(scales + g * n + col)));
-                    if (!SYM) z = (float)((__ldg(qzeros + g * (n / 8) + col / 8) >> (4 * (col & 7))) & 15);
-                }
+                const float sv = __half2float(__ushort_as_half((unsigned short)sh[c]));
+                const float z = SYM ? 8.f : (float)((zw[c] >> (4 * (col & 7))) & 15u);
                 S2 = wq::f2(sv, sv);
                 Z2 = wq::f2(-(kMagic + z), -(kMagic + z));
             }

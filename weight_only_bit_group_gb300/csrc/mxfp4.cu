@@ -3,22 +3,22 @@
 //
 // Layout: k % 32 == 0, so the 32-value blocks of a row-major [n, k] matrix are
 // consecutive in memory and the whole matrix is a flat stream of blocks.  One
-// thread takes one 16-byte chunk (8 bf16 values), four lanes make one block:
-//   load   uint4 (8 bf16) by cp.async into a two-stage per-thread shared-memory
-//          pipeline (the next chunks stream in while these are coded)
-//   amax   16-bit SIMD max of |bf16| bit patterns, 2 shuffles over 4 lanes
-//   code   v = w * 2^-exp (exact), hardware cvt to e2m1x2 (round half even,
-//          saturate at 6) -- the e2m1 encoding IS the page's magnitude index
-//   store  one uint32 of 8 nibbles per lane (128 B per warp), one e8m0 byte per
-//          block.
+// lane codes one block (64 bytes of bf16) per step:
+//   load   four 16-byte loads, the next block's issued before this one is coded
+//   amax   bf16x2 max tree of |w| inside the lane
+//   code   v = w * 2^-exp (exact: one mixed bf16 x bf16 -> binary32 FMA per value,
+//          read straight from the packed bf16 pair), hardware cvt to e2m1x2
+//          (round half even, saturate at 6) -- the e2m1 encoding IS the page's
+//          magnitude index
+//   store  one 16-byte word of 32 codes and one E8M0 byte per lane.
 // HBM bound: 2 B read + 0.53 B written per weight.
 //
 // mxfp4_quantize_err runs the same kernel with ERR = 1: each lane also decodes
-// its codes back (hardware e2m1 -> f16x2, times 2^exp: the values
-// dequantize_mxfp4 returns), forms the binary32 terms w^2 and (w - deq)^2 that
-// quantize_dflash_mxfp4.py main() reduces into its relative error, and the grid
-// finishes both sums with the last-CTA float-float reduction: no second read of
-// w and no dequantized tensor in memory.
+// its codes back (hardware e2m1 -> f16x2: the values dequantize_mxfp4 returns,
+// before the block scale), forms the terms w^2 and (w - deq)^2 that
+// quantize_dflash_mxfp4.py main() reduces into its relative error (see
+// code_pair_err), and the grid finishes both sums with the last-CTA float-float
+// reduction: no second read of w and no dequantized tensor in memory.
 #include "wq_common.cuh"
 
 namespace {
@@ -70,103 +70,100 @@ __device__ __forceinline__ uint32_t page_tie(uint32_t nib, float v) {
     return (m == 0.75f || m == 1.75f || m == 3.5f) ? nib - 2u : nib;
 }
 
-template <int TIE>
-__device__ __forceinline__ uint32_t code_pair(float x0, float x1, float inv) {
-    float a0 = __fmul_rn(x0, inv), a1 = __fmul_rn(x1, inv);
+// Codes of one packed pair of weights (the two bf16 values of `u`; inv_h =
+// 2^-exp as bf16 bits) and, with ERR, the pair's error terms in the block's
+// scaled domain.  Both halves go straight into mixed-precision FMAs (bf16 x bf16
+// + binary32): a = w * 2^-exp is exact (a product of two bf16 values), so no
+// bf16 -> binary32 unpacking runs on the integer pipe.  With ERR: sa += a^2 and
+// se += (q - a)^2, q the e2m1 value of the chosen code (back from the code byte
+// through the hardware e2m1 -> f16x2 conversion; q - a is one mixed f16 /
+// binary32 subtraction, exact).  a * 2^exp = w and (q - a) * 2^exp = deq - w
+// exactly, so a block's two sums, scaled by 2^exp twice, are the sums of the
+// page's binary32 terms w^2 and (deq - w)^2 up to the rounding of each square
+// (relative 2^-24).
+template <int TIE, int ERR>
+__device__ __forceinline__ uint32_t code_pair_err(uint32_t u, uint16_t inv_h, wq::f2_t& sa, wq::f2_t& se) {
+    float a0, a1;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, lo, %3, %4;\n\tfma.rn.f32.bf16 %1, hi, %3, %4;\n\t}"
+        : "=f"(a0), "=f"(a1)
+        : "r"(u), "h"(inv_h), "f"(-0.0f));
     uint32_t b = e2m1x2(a0, a1);
     if (TIE == WQ_TIE_PAGE_LITERAL) b = page_tie(b & 15u, a0) | (page_tie(b >> 4, a1) << 4);
+    if (ERR) {
+        uint32_t h2;
+        const uint16_t in = (uint16_t)b;
+        asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "h"(in));
+        float r0, r1;
+        asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "sub.rn.f32.f16 %0, lo, %3;\n\tsub.rn.f32.f16 %1, hi, %4;\n\t}"
+            : "=f"(r0), "=f"(r1)
+            : "r"(h2), "f"(a0), "f"(a1));
+        const wq::f2_t a = wq::f2(a0, a1), r = wq::f2(r0, r1);  // r = q - a, exact
+        se = wq::fma2(r, r, se);
+        sa = wq::fma2(a, a, sa);
+    }
     return b;
 }
 
-// Error terms of one packed pair: sw += x*x, se += (x - deq)^2 with deq = e2m1
-// value * 2^exp.  x - deq is formed by one FMA of the exact product q * 2^exp
-// (a power-of-two scaling, never rounded for these magnitudes), so it is the
-// binary32 difference the page's (deq - w) computes.
-__device__ __forceinline__ void err_pair(uint32_t xbits, uint32_t byte, wq::f2_t ns2, wq::f2_t& sw,
-                                         wq::f2_t& se) {
-    float q0, q1;
-    e2m1x2_to_f(byte, q0, q1);
-    const wq::f2_t x = wq::bf2_to_f2(xbits);
-    const wq::f2_t d = wq::fma2(wq::f2(q0, q1), ns2, x);
-    se = wq::fma2(d, d, se);
-    sw = wq::fma2(x, x, sw);
-}
-
+// One lane codes one whole 32-value block per step: four 16-byte loads (the
+// next block's are issued before this one is coded), the block |amax| by a
+// bf16x2 max tree inside the lane (no shuffles), 16 code pairs, one 16-byte
+// store of the 32 codes and one E8M0 byte.  Consecutive lanes take consecutive
+// blocks, so a warp reads 2 KB and writes 512 + 32 bytes contiguously per
+// step; the four loads of a lane hit the same L1 lines.
 template <int TIE, int ERR>
 __global__ void __launch_bounds__(kThreads) mxfp4_quant_kernel(const uint4* __restrict__ w,
-                                                               int64_t nchunks,
-                                                               uint32_t* __restrict__ packed,
+                                                               int64_t nblocks,
+                                                               uint4* __restrict__ packed,
                                                                uint8_t* __restrict__ e8m0,
                                                                float4* __restrict__ slots,
                                                                unsigned* __restrict__ counter,
                                                                double* __restrict__ snr_db,
                                                                double* __restrict__ rel_err) {
-    // two pipeline stages of kUnroll 16-byte chunks, private to each thread
-    __shared__ __align__(16) uint4 stage_buf[2][kUnroll][kThreads];
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
-    const int64_t step = nwarps * 32 * kUnroll;
+    const int64_t nth = (int64_t)gridDim.x * kThreads;
+    int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     wq::KSum dw, de;
-
-    auto issue = [&](int64_t wb, int st) {
+    uint4 nx[4];
+    if (b < nblocks) {
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t c = wb + (int64_t)u * nwarps * 32 + lane;
-            if (c < nchunks) wq::cp_async16(&stage_buf[st][u][threadIdx.x], w + c);
-        }
-        wq::cp_async_commit();
-    };
-
-    // Every lane of a warp runs the same trip count (shuffles below); lanes past
-    // the end compute on zeros and store nothing.  nchunks % 4 == 0 and chunk
-    // indices are 4-aligned per lane quad, so a quad is all-valid or all-invalid.
-    issue(warp * 32, 0);
-    int j = 0;
-    for (int64_t wb = warp * 32; wb < nchunks; wb += step, ++j) {
-        issue(wb + step, (j + 1) & 1);
-        wq::cp_async_wait<1>();
-        uint4 v[kUnroll];
-        int64_t ch[kUnroll];
+        for (int q = 0; q < 4; ++q) nx[q] = __ldg(w + 4 * b + q);
+    }
+    for (; b < nblocks; b += nth) {
+        uint4 v[4];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            ch[u] = wb + (int64_t)u * nwarps * 32 + lane;
-            v[u] = ch[u] < nchunks ? stage_buf[j & 1][u][threadIdx.x] : make_uint4(0, 0, 0, 0);
-        }
-        wq::f2_t sw = wq::f2(0.f, 0.f), se = wq::f2(0.f, 0.f);
+        for (int q = 0; q < 4; ++q) v[q] = nx[q];
+        if (b + nth < nblocks) {
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const uint32_t M = 0x7fff7fffu;
-            uint32_t m2 = __vmaxu2(__vmaxu2(v[u].x & M, v[u].y & M), __vmaxu2(v[u].z & M, v[u].w & M));
-            uint32_t a = max(m2 & 0xffffu, m2 >> 16);
-            a = max(a, wq::shfl_xor(a, 1));
-            a = max(a, wq::shfl_xor(a, 2));
-            const int ex = exp_from_bf16_mag(a);
-            const float inv = __uint_as_float((uint32_t)(127 - ex) << 23);  // 2^-exp, normal
-            uint32_t word = code_pair<TIE>(wq::bf_lo(v[u].x), wq::bf_hi(v[u].x), inv);
-            word |= code_pair<TIE>(wq::bf_lo(v[u].y), wq::bf_hi(v[u].y), inv) << 8;
-            word |= code_pair<TIE>(wq::bf_lo(v[u].z), wq::bf_hi(v[u].z), inv) << 16;
-            word |= code_pair<TIE>(wq::bf_lo(v[u].w), wq::bf_hi(v[u].w), inv) << 24;
-            if (ERR) {
-                // lanes past the end hold zeros: zero codes, zero terms
-                const float ns = -e8m0_scale((uint32_t)(ex + 127));
-                const wq::f2_t ns2 = wq::f2(ns, ns);
-                err_pair(v[u].x, word & 0xffu, ns2, sw, se);
-                err_pair(v[u].y, (word >> 8) & 0xffu, ns2, sw, se);
-                err_pair(v[u].z, (word >> 16) & 0xffu, ns2, sw, se);
-                err_pair(v[u].w, word >> 24, ns2, sw, se);
-            }
-            if (ch[u] < nchunks) {
-                packed[ch[u]] = word;
-                if ((lane & 3) == 0) e8m0[ch[u] >> 2] = (uint8_t)(ex + 127);
-            }
+            for (int q = 0; q < 4; ++q) nx[q] = __ldg(w + 4 * (b + nth) + q);
         }
+        // block |amax| as bf16 magnitudes (max.xorsign.abs leaves garbage sign bits)
+        uint32_t m2[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            m2[q] = wq::babsmax2(wq::babsmax2(v[q].x, v[q].y), wq::babsmax2(v[q].z, v[q].w));
+        uint32_t m = wq::babsmax2(wq::babsmax2(m2[0], m2[1]), wq::babsmax2(m2[2], m2[3])) & 0x7fff7fffu;
+        const int ex = exp_from_bf16_mag(max(m & 0xffffu, m >> 16));
+        const uint16_t inv_h = (uint16_t)((127 - ex) << 7);  // 2^-exp as bf16 (normal)
+        wq::f2_t sa = wq::f2(0.f, 0.f), se = wq::f2(0.f, 0.f);
+        uint32_t word[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            word[q] = code_pair_err<TIE, ERR>(v[q].x, inv_h, sa, se);
+            word[q] |= code_pair_err<TIE, ERR>(v[q].y, inv_h, sa, se) << 8;
+            word[q] |= code_pair_err<TIE, ERR>(v[q].z, inv_h, sa, se) << 16;
+            word[q] |= code_pair_err<TIE, ERR>(v[q].w, inv_h, sa, se) << 24;
+        }
+        packed[b] = make_uint4(word[0], word[1], word[2], word[3]);
+        e8m0[b] = (uint8_t)(ex + 127);
         if (ERR) {
-            dw.add(__fadd_rn(sw.x, sw.y));
-            de.add(__fadd_rn(se.x, se.y));
+            // back to the weights' scale: times 2^exp twice (2^(2 exp) itself may
+            // leave the binary32 range)
+            const float sc = e8m0_scale((uint32_t)(ex + 127));
+            dw.add(__fmul_rn(__fmul_rn(__fadd_rn(sa.x, sa.y), sc), sc));
+            de.add(__fmul_rn(__fmul_rn(__fadd_rn(se.x, se.y), sc), sc));
         }
     }
-    wq::cp_async_wait<0>();
     if (ERR) wq::finish_snr(wq::ff_of(dw), wq::ff_of(de), slots, counter, snr_db, rel_err);
 }
 
@@ -219,8 +216,9 @@ template <int TIE, int ERR>
 wq_status launch_quant(const uint16_t* w, int64_t nchunks, uint8_t* packed, uint8_t* e8m0,
                        void* workspace, double* snr_db, double* rel_err, cudaStream_t st) {
     const void* fn = (const void*)mxfp4_quant_kernel<TIE, ERR>;
+    const int64_t nblocks = nchunks / 4;
     // with the error sums every CTA owns one partial-sum slot
-    const int grid = wqh::grid_for(fn, kThreads, 0, (nchunks + kThreads - 1) / kThreads,
+    const int grid = wqh::grid_for(fn, kThreads, 0, (nblocks + kThreads - 1) / kThreads,
                                    ERR ? wqh::kMaxPartials : 1 << 30);
     unsigned* counter = nullptr;
     float4* slots = nullptr;
@@ -230,8 +228,8 @@ wq_status launch_quant(const uint16_t* w, int64_t nchunks, uint8_t* packed, uint
         wq_status s = wqh::cuda_status(cudaMemsetAsync(counter, 0, sizeof(unsigned), st));
         if (s != WQ_OK) return s;
     }
-    mxfp4_quant_kernel<TIE, ERR><<<grid, kThreads, 0, st>>>((const uint4*)w, nchunks, (uint32_t*)packed,
-                                                            e8m0, slots, counter, snr_db, rel_err);
+    mxfp4_quant_kernel<TIE, ERR><<<grid, kThreads, 0, st>>>((const uint4*)w, nblocks, (uint4*)packed, e8m0,
+                                                            slots, counter, snr_db, rel_err);
     return wqh::check_launch();
 }
 

@@ -111,12 +111,24 @@ __device__ __forceinline__ void store_shards(const uint32_t (&blo)[8], const uin
 }
 
 // Error terms of one packed pair: x the two bf16 weights, r the two bf16 values
-// q - zp (exact integers), s2 the group's bf16 scale in both halves.
+// q - zp (exact integers), s2 the group's bf16 scale in both halves.  deq =
+// bf16(r * s) is the page's bf16 multiply (mul.rn.bf16x2); the binary32 values
+// of w and the difference w - deq come from mixed-precision FMAs that read the
+// bf16 halves in place (w * 1 and deq * -1 + w, each exact or rounded once as
+// the binary32 subtraction is), so the integer pipe, which the code
+// computation keeps busy, does no unpacking.
 __device__ __forceinline__ void err_pair(uint32_t x, uint32_t r, uint32_t s2, wq::f2_t& sw,
                                          wq::f2_t& se) {
-    const wq::f2_t xf = wq::bf2_to_f2(x);
-    const wq::f2_t df = wq::bf2_to_f2(wq::bmul2(r, s2));  // the page's bf16 deq
-    const wq::f2_t d = wq::fma2(df, wq::f2(-1.0f, -1.0f), xf);  // RN(x - deq)
+    const uint32_t dq = wq::bmul2(r, s2);  // the page's bf16 deq
+    float x0, x1, d0, d1;
+    asm("{\n\t.reg .b16 xl, xh, ql, qh, one, m1;\n\t"
+        "mov.b32 {xl, xh}, %4;\n\tmov.b32 {ql, qh}, %5;\n\t"
+        "mov.b16 one, 0x3F80;\n\tmov.b16 m1, 0xBF80;\n\t"
+        "fma.rn.f32.bf16 %0, xl, one, %6;\n\tfma.rn.f32.bf16 %1, xh, one, %6;\n\t"
+        "fma.rn.f32.bf16 %2, ql, m1, %0;\n\tfma.rn.f32.bf16 %3, qh, m1, %1;\n\t}"
+        : "=f"(x0), "=f"(x1), "=f"(d0), "=f"(d1)
+        : "r"(x), "r"(dq), "f"(-0.0f));
+    const wq::f2_t xf = wq::f2(x0, x1), d = wq::f2(d0, d1);  // w and RN(w - deq)
     se = wq::fma2(d, d, se);
     sw = wq::fma2(xf, xf, sw);
 }
