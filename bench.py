@@ -558,28 +558,43 @@ def run_ours(args, rank, world, dist):
 
     side = torch.cuda.Stream(dev)
 
+    side_phases = [p for p in phases if p[-1] is None]
+    main_phases = [p for p in phases if p[-1] is not None]
+    if args.awq_after != "start" and args.awq_after not in [p[0] for p in main_phases]:
+        raise SystemExit(f"--awq-after: no phase {args.awq_after!r}")
+
     def step_body(evs):
         # the AWQ search (one latency-bound call that barely uses HBM) runs on a
-        # side stream next to the bandwidth-bound phases; the step is timed by its
-        # own event pair on the launching stream, after joining the side stream
+        # side stream next to the bandwidth-bound phases, forked from the launching
+        # stream at the start of the step or after the phase --awq-after names; the
+        # step is timed by its own event pair on the launching stream, after
+        # joining the side stream
         main = torch.cuda.current_stream(dev)
         s0, s1 = timing_event(), timing_event()
         s0.record()
-        fork = torch.cuda.Event()
-        fork.record(main)
-        side.wait_event(fork)
-        for name, fn, *rest in phases:
-            a, b = timing_event(), timing_event()
-            if rest[-1] is None:  # single call: side stream
+
+        def fork_side():
+            fork = torch.cuda.Event()
+            fork.record(main)
+            side.wait_event(fork)
+            for name, fn, *rest in side_phases:
+                a, b = timing_event(), timing_event()
                 with torch.cuda.stream(side):
                     a.record()
                     fn()
                     b.record()
-            else:
-                a.record()
-                fn()
-                b.record()
+                evs.append((name, a, b))
+
+        if args.awq_after == "start":
+            fork_side()
+        for name, fn, *rest in main_phases:
+            a, b = timing_event(), timing_event()
+            a.record()
+            fn()
+            b.record()
             evs.append((name, a, b))
+            if name == args.awq_after:
+                fork_side()
         join = torch.cuda.Event()
         join.record(side)
         main.wait_event(join)
@@ -680,7 +695,8 @@ def run_ours(args, rank, world, dist):
                    "mxfp4_ties": "half_even", "awq": "gate||up [28672,4096] -> 2048 rows, 11 alphas",
                    "l2": "flushed before every step (256 MB write, then 256 MB read so no dirty lines remain); inputs 436 MB > L2",
                    "launch": ("eager" if args.no_graph else "one CUDA graph per step (captured ABI calls)")
-                             + "; the 7 projections of a phase run on 7 concurrent streams; AWQ on a side stream",
+                             + "; the 7 projections of a phase run on 7 concurrent streams; AWQ on a side stream"
+                             + (" from the step's start" if args.awq_after == "start" else f" after {args.awq_after}"),
                    "parallelism": f"replicas x{world} (one layer per GPU, no collective)"},
         "roofline": roofline,
         "kernels": kernels,
@@ -1025,6 +1041,8 @@ def main():
     ap.add_argument("--wdtype", choices=["bf16", "f16", "f32"], default="bf16",
                     help="weight type for --kernel gptq_quantize_* / mxfp4_quantize")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--awq-after", default="start",
+                    help="fork the AWQ search's side stream at the step's start or after this phase")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the MXFP4 / AWQ / 8-layer uintx timings of the other configurations")

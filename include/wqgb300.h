@@ -287,7 +287,8 @@ wq_status awq_search_static_scratch(const uint16_t* w, int64_t n, int64_t k, con
  * decode batches: y = x deq(W)^T without materialising deq.
  * In:  x        bf16 [m, k], 16-byte aligned, 1 <= m <= 8 (WQ_ERR_UNSUPPORTED above).
  *      qweight, qzeros, scales as produced by gptq_quantize_*; group 32, 64,
- *               128 or 256; sym selects the rule (qzeros may be NULL for sym).
+ *               128 or 256; sym selects the rule (qzeros may be NULL for sym);
+ *               qweight 16-byte aligned.
  * Out: out      [m, n], binary32 (WQ_DTYPE_F32) or bf16 (WQ_DTYPE_BF16: the
  *               binary32 result rounded to nearest even).
  *      workspace >= gptq_linear_workspace_bytes(m, n), 256-byte aligned,
@@ -295,11 +296,13 @@ wq_status awq_search_static_scratch(const uint16_t* w, int64_t n, int64_t k, con
  *               call leaves its arrival counters at zero again, so no reset is
  *               needed between calls (zero it again after a call that failed).
  *               Calls that overlap on the GPU need separate workspaces.
- * Math: deq = (code - zp) * fp16 scale (exact in binary32); per group the
- * products x * (code - zp) (exact) are summed in binary32 and the group sum is
- * multiplied by the scale and added in binary32; K-slices are added in a fixed
- * order.  The result is within (k + 2) * 2^-24 * sum_k |x * deq| of the exact
- * value and is the same from run to run.  k == 0 writes zeros. */
+ * Math: deq = (code - zp) * fp16 scale (exact in binary32); the products
+ * x * (code - zp) (exact) are summed in binary32 over runs of at most 64 input
+ * channels of one group, each run sum is multiplied by the group's scale and
+ * added in binary32; K-slices are added in a fixed order.  Every product passes
+ * through at most k + 1 roundings, so the result is within (k + 2) * 2^-24 *
+ * sum_k |x * deq| of the exact value, and it is the same from run to run.
+ * k == 0 writes zeros. */
 size_t gptq_linear_workspace_bytes(int64_t m, int64_t n);
 wq_status gptq_linear(const uint16_t* x, int64_t m, const int32_t* qweight, const int32_t* qzeros,
                       const uint16_t* scales, int64_t n, int64_t k, int group, int sym,

@@ -6,105 +6,195 @@
 // Only the codes (0.5 B per weight) and the group scale / zero point are read,
 // a quarter of the bytes of a bf16 weight, so for m = 1 the kernel is HBM bound.
 //
-// Grid: ceil(N/256) column blocks x S slices of whole groups along K.  Thread =
-// one output column.  The CTA stages its slice of x (all m rows) in shared
-// memory as binary32, read by broadcast.  Per qweight word the 8 codes become
-// binary32 1.5*2^23 + c by byte permutes; subtracting 1.5*2^23 + zp gives the
-// exact c - zp, and f32x2 FMAs accumulate x (c - zp) over the group; the group
-// sum times the fp16 scale is added to the column's sum.  Partials go to a
-// workspace slot per (slice, row, column); the last CTA of a column block to
-// finish adds the S slices in order (deterministic, no waiting), writes y and
-// sets the block's arrival counter back to zero, so that a call needs no
-// separate reset of the workspace.
+// Grid: ceil(N/128) column blocks x S slices along K.  A CTA is 4 warps over the
+// same 128 output columns; lane = 4 adjacent columns, so one 16-byte piece of a
+// qweight row holds the 8 codes of each of its 4 columns.  Each warp walks
+// `batches` batches of 8 qweight rows (64 input channels) through a 4-stage
+// cp.async pipeline of its own: the codes (16 bytes per lane and row) and the
+// batch's x rows land in shared memory three batches ahead of their use, so
+// the loads stream while earlier batches are computed.  The group scales and
+// zero points of the next batch are read into registers one batch ahead.
+// Per qweight word the 8 codes become bf16 128 + c by byte permutes (two codes
+// per permute); subtracting 128 + zp in bf16x2 gives the exact c - zp; mixed
+// bf16 x bf16 -> binary32 FMAs multiply by x (read in place from its bf16
+// pairs) and add into two binary32 sums per column and token (even and odd
+// input channels): every product is exact and every addition rounds once.  The
+// group sum times the fp16 scale is added to the column's sum.  The 4 warps'
+// sums meet in shared memory and are added in warp order; each CTA writes its
+// slice's partial to a workspace slot per (slice, row, column); the last CTA of
+// a column block to finish adds the S slices in order (deterministic, no
+// waiting), writes y and sets the block's arrival counter back to zero, so that
+// a call needs no separate reset of the workspace.
 #include "wq_common.cuh"
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr int kThreads = 128;   // 4 warps
+constexpr int kCols = 128;      // output columns per CTA (4 per lane)
+constexpr int kRPW = 8;         // qweight rows per warp batch
+constexpr int kNST = 4;         // pipeline stages per warp
 constexpr int kMaxSlices = 64;
 constexpr int kMaxM = 8;
-constexpr int kXSmemBytes = 40 * 1024;  // staged x: under the default 48 KB dynamic limit
 
-__device__ __forceinline__ float code_f(uint32_t bytes, int j) {
-    return __uint_as_float(__byte_perm(bytes, 0x4B400000u, 0x7640u + (unsigned)j));
+template <int M>
+struct LinSmem {
+    static constexpr int W = kRPW * 32 * 16;  // codes of one stage: [row][lane] 16 bytes
+    static constexpr int X = kRPW * M * 16;   // x of one stage: [token][row] 8 bf16
+    static constexpr int STAGE = W + X;
+    static constexpr int WARP = kNST * STAGE;
+    static constexpr int CTA = 4 * WARP;
+};
+
+// acc_e += sum of c_{2i} x_{2i}, acc_o += sum of c_{2i+1} x_{2i+1} over the 8
+// input channels of one word: d0 = (c0, c2), d1 = (c4, c6), d2 = (c1, c3),
+// d3 = (c5, c7) as bf16x2 (c - zp, exact), xv the 8 bf16 x values in order.
+__device__ __forceinline__ void dot8(uint32_t d0, uint32_t d1, uint32_t d2, uint32_t d3, uint4 xv,
+                                     float& e, float& o) {
+    asm("{\n\t.reg .b16 a0, a1, b0, b1, c0, c1, f0, f1, x0, x1, x2, x3, x4, x5, x6, x7;\n\t"
+        "mov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\tmov.b32 {c0, c1}, %4;\n\tmov.b32 {f0, f1}, %5;\n\t"
+        "mov.b32 {x0, x1}, %6;\n\tmov.b32 {x2, x3}, %7;\n\tmov.b32 {x4, x5}, %8;\n\tmov.b32 {x6, x7}, %9;\n\t"
+        "fma.rn.f32.bf16 %0, a0, x0, %0;\n\tfma.rn.f32.bf16 %0, a1, x2, %0;\n\t"
+        "fma.rn.f32.bf16 %0, b0, x4, %0;\n\tfma.rn.f32.bf16 %0, b1, x6, %0;\n\t"
+        "fma.rn.f32.bf16 %1, c0, x1, %1;\n\tfma.rn.f32.bf16 %1, c1, x3, %1;\n\t"
+        "fma.rn.f32.bf16 %1, f0, x5, %1;\n\tfma.rn.f32.bf16 %1, f1, x7, %1;\n\t}"
+        : "+f"(e), "+f"(o)
+        : "r"(d0), "r"(d1), "r"(d2), "r"(d3), "r"(xv.x), "r"(xv.y), "r"(xv.z), "r"(xv.w));
 }
 
 template <bool SYM, int M, int G>
 __global__ void __launch_bounds__(kThreads) gptq_linear_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ qweight,
     const int32_t* __restrict__ qzeros, const uint16_t* __restrict__ scales, int64_t n, int64_t k,
-    int gps, float* __restrict__ part, unsigned* __restrict__ counters, int out_bf16,
+    int batches, float* __restrict__ part, unsigned* __restrict__ counters, int out_bf16,
     void* __restrict__ out) {
-    extern __shared__ __align__(16) float xs[];  // [M][gps * G]
-    const int64_t groups = k / G;
-    const int64_t g0 = (int64_t)blockIdx.y * gps;
-    const int64_t g1 = min(g0 + gps, groups);
-    const int len = (int)((g1 - g0) * G);  // this slice's input channels
+    using L = LinSmem<M>;
+    constexpr int RPG = (G / 8) < kRPW ? (G / 8) : kRPW;  // rows of one group inside a batch
+    constexpr int GPB = kRPW / RPG;                       // groups (or one group's part) per batch
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned char* wsm = smem + warp * L::WARP;
+    const int64_t c0 = (int64_t)blockIdx.x * kCols + 4 * lane;
+    const bool cv = c0 < n;  // n % 8 == 0: a lane's 4 columns are all valid or all not
+    const int64_t rows = k / 8;
     const int S = gridDim.y;
+    // first qweight row of batch bt of this warp (the CTA's 4 warps take
+    // consecutive 8-row pieces of each 32-row step of the slice)
+    auto rowof = [&](int bt) -> int64_t { return (((int64_t)blockIdx.y * batches + bt) * 4 + warp) * kRPW; };
 
-    const int64_t col = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const bool colv = col < n;
-    constexpr int WPG = G / 8;  // qweight words per group
-    // the first group's words are requested before x is staged (independent
-    // loads in flight together); each later group's while the previous is summed
-    uint32_t nx[WPG];
-    if (colv) {
+    auto issue = [&](int bt) {
+        if (bt < batches) {
+            const int64_t r0 = rowof(bt);
+            unsigned char* sw = wsm + (bt % kNST) * L::STAGE;
 #pragma unroll
-        for (int r = 0; r < WPG; ++r) nx[r] = (uint32_t)__ldg(qweight + (g0 * WPG + r) * n + col);
-    }
-
-    // x[m][g0*G .. g1*G) -> binary32 in shared memory (8 values per thread step)
-    for (int i = threadIdx.x; i < M * len / 8; i += kThreads) {
-        const int m = i / (len / 8), c = i % (len / 8);
-        const uint4 u = *reinterpret_cast<const uint4*>(x + m * k + g0 * G + 8 * c);
-        float4* d = reinterpret_cast<float4*>(xs + m * (gps * G) + 8 * c);
-        d[0] = make_float4(wq::bf_lo(u.x), wq::bf_hi(u.x), wq::bf_lo(u.y), wq::bf_hi(u.y));
-        d[1] = make_float4(wq::bf_lo(u.z), wq::bf_hi(u.z), wq::bf_lo(u.w), wq::bf_hi(u.w));
-    }
-    __syncthreads();
-
-    float acc[M];
-#pragma unroll
-    for (int m = 0; m < M; ++m) acc[m] = 0.0f;
-    if (colv) {
-        for (int64_t g = g0; g < g1; ++g) {
-            uint32_t wd[WPG];
-#pragma unroll
-            for (int r = 0; r < WPG; ++r) wd[r] = nx[r];
-            if (g + 1 < g1) {
-#pragma unroll
-                for (int r = 0; r < WPG; ++r) nx[r] = (uint32_t)__ldg(qweight + ((g + 1) * WPG + r) * n + col);
+            for (int r = 0; r < kRPW; ++r)
+                if (cv && r0 + r < rows) wq::cp_async16(sw + (r * 32 + lane) * 16, qweight + (r0 + r) * n + c0);
+            for (int p = lane; p < kRPW * M; p += 32) {  // piece p: token p / 8, row p % 8
+                const int m = p / kRPW, r = p % kRPW;
+                if (r0 + r < rows) wq::cp_async16(sw + L::W + p * 16, x + m * k + (r0 + r) * 8);
             }
-            const float s = __half2float(__ushort_as_half(__ldg(scales + g * n + col)));
-            float zp = 8.0f;
-            if (!SYM) zp = (float)((__ldg(qzeros + g * (n / 8) + col / 8) >> (4 * (col & 7))) & 15);
-            const wq::f2_t Z2 = wq::f2(-(kMagic + zp), -(kMagic + zp));
-            wq::f2_t ag[M];
+        }
+        wq::cp_async_commit();  // every lane commits a group per batch, empty or not
+    };
+    // the group constants of a batch: 4 scales and the qzeros word of each group
+    auto consts = [&](int bt, uint32_t (&sh)[GPB][4], uint32_t (&zw)[GPB]) {
+        const int64_t r0 = rowof(bt);
 #pragma unroll
-            for (int m = 0; m < M; ++m) ag[m] = wq::f2(0.0f, 0.0f);
-            const float* xg = xs + (g - g0) * G;
+        for (int gi = 0; gi < GPB; ++gi) {
+            const bool gv = bt < batches && cv && r0 + gi * RPG < rows;
+            const int64_t g = ((r0 + gi * RPG) * 8) / G;
 #pragma unroll
-            for (int r = 0; r < WPG; ++r) {
-                const uint32_t lo = wd[r] & 0x0F0F0F0Fu, hi = (wd[r] >> 4) & 0x0F0F0F0Fu;
+            for (int j = 0; j < 4; ++j) sh[gi][j] = gv ? (uint32_t)__ldg(scales + g * n + c0 + j) : 0u;
+            zw[gi] = (!SYM && gv) ? (uint32_t)__ldg(qzeros + g * (n / 8) + c0 / 8) : 0u;
+        }
+    };
+
+    float acc[M][4];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    // c - zp of input channels 8r + 4h .. 8r + 4h + 3 (exact)
-                    const wq::f2_t d0 = wq::add2(wq::f2(code_f(lo, 2 * h), code_f(hi, 2 * h)), Z2);
-                    const wq::f2_t d1 = wq::add2(wq::f2(code_f(lo, 2 * h + 1), code_f(hi, 2 * h + 1)), Z2);
+    for (int m = 0; m < M; ++m)
 #pragma unroll
-                    for (int m = 0; m < M; ++m) {
-                        const float4 xv = *reinterpret_cast<const float4*>(xg + m * (gps * G) + 8 * r + 4 * h);
-                        ag[m] = wq::fma2(d0, wq::f2(xv.x, xv.y), ag[m]);
-                        ag[m] = wq::fma2(d1, wq::f2(xv.z, xv.w), ag[m]);
-                    }
+        for (int j = 0; j < 4; ++j) acc[m][j] = 0.0f;
+
+#pragma unroll
+    for (int i = 0; i < kNST - 1; ++i) issue(i);
+    uint32_t shn[GPB][4], zwn[GPB];
+    consts(0, shn, zwn);
+    for (int bt = 0; bt < batches; ++bt) {
+        issue(bt + kNST - 1);
+        uint32_t sh[GPB][4], zw[GPB];
+#pragma unroll
+        for (int gi = 0; gi < GPB; ++gi) {
+            zw[gi] = zwn[gi];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sh[gi][j] = shn[gi][j];
+        }
+        consts(bt + 1, shn, zwn);
+        wq::cp_async_wait<kNST - 1>();  // this lane's copies of batch bt have landed
+        __syncwarp();                    // ... and every other lane's (the x pieces)
+        const int64_t r0 = rowof(bt);
+        const unsigned char* sw = wsm + (bt % kNST) * L::STAGE;
+#pragma unroll
+        for (int gi = 0; gi < GPB; ++gi) {
+            uint32_t zb2[4];  // bf16x2 of 128 + zp, per column
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t zp = SYM ? 8u : (zw[gi] >> (4 * ((c0 + j) & 7))) & 15u;
+                zb2[j] = (0x4300u + zp) * 0x10001u;
+            }
+            float ge[M][4], go[M][4];
+#pragma unroll
+            for (int m = 0; m < M; ++m)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ge[m][j] = go[m][j] = 0.0f;
+#pragma unroll
+            for (int rr = 0; rr < RPG; ++rr) {
+                const int r = gi * RPG + rr;
+                if (r0 + r >= rows) break;  // uniform over the warp
+                const uint4 wv = *reinterpret_cast<const uint4*>(sw + (r * 32 + lane) * 16);
+                uint4 xv[M];
+#pragma unroll
+                for (int m = 0; m < M; ++m) xv[m] = *reinterpret_cast<const uint4*>(sw + L::W + (m * kRPW + r) * 16);
+                const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    // byte q of lo / hi: the codes of input channels 2q / 2q + 1
+                    const uint32_t lo = wd[j] & 0x0F0F0F0Fu, hi = (wd[j] >> 4) & 0x0F0F0F0Fu;
+                    // bytes c | 0x43 << 8 = bf16 of 128 + c; minus 128 + zp is exact
+                    const uint32_t d0 = wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4140), zb2[j]);
+                    const uint32_t d1 = wq::bsub2(__byte_perm(lo, 0x43434343u, 0x4342), zb2[j]);
+                    const uint32_t d2 = wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4140), zb2[j]);
+                    const uint32_t d3 = wq::bsub2(__byte_perm(hi, 0x43434343u, 0x4342), zb2[j]);
+#pragma unroll
+                    for (int m = 0; m < M; ++m) dot8(d0, d1, d2, d3, xv[m], ge[m][j], go[m][j]);
                 }
             }
 #pragma unroll
-            for (int m = 0; m < M; ++m) acc[m] = __fmaf_rn(__fadd_rn(ag[m].x, ag[m].y), s, acc[m]);
-        }
+            for (int j = 0; j < 4; ++j) {
+                const float sc = __half2float(__ushort_as_half((unsigned short)sh[gi][j]));
 #pragma unroll
-        for (int m = 0; m < M; ++m) part[((int64_t)blockIdx.y * M + m) * n + col] = acc[m];
+                for (int m = 0; m < M; ++m) acc[m][j] = __fmaf_rn(__fadd_rn(ge[m][j], go[m][j]), sc, acc[m][j]);
+            }
+        }
+        __syncwarp();  // every lane is done with this stage before it is refilled
+    }
+    wq::cp_async_wait<0>();
+
+    // the 4 warps' sums of each column, added in warp order
+    __shared__ float red[4][M][kCols];
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) red[warp][m][4 * lane + j] = acc[m][j];
+    __syncthreads();
+    const int64_t col = (int64_t)blockIdx.x * kCols + threadIdx.x;
+    const bool colv = col < n;
+    if (colv) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            float v = red[0][m][threadIdx.x];
+#pragma unroll
+            for (int w2 = 1; w2 < 4; ++w2) v = __fadd_rn(v, red[w2][m][threadIdx.x]);
+            part[((int64_t)blockIdx.y * M + m) * n + col] = v;
+        }
     }
     // the last CTA of this column block adds the slices in order
     // (the barrier orders every thread's partial before thread 0's fence, which
@@ -144,25 +234,34 @@ template <bool SYM, int M, int G>
 wq_status launch_linear(const uint16_t* x, const int32_t* qweight, const int32_t* qzeros,
                         const uint16_t* scales, int64_t n, int64_t k, int out_bf16, void* out,
                         char* ws, cudaStream_t st) {
+    using L = LinSmem<M>;
     const void* fn = (const void*)gptq_linear_kernel<SYM, M, G>;
-    const int64_t col_blocks = (n + kThreads - 1) / kThreads;
-    const int64_t groups = k / G;
-    const int64_t target = wqh::grid_for(fn, kThreads, 0, (int64_t)1 << 30, 1 << 30);
-    int64_t S = target / col_blocks;
-    if (S < 1) S = 1;
-    if (S > kMaxSlices) S = kMaxSlices;
-    if (S > groups) S = groups;
-    int64_t gps = (groups + S - 1) / S;
-    const int64_t max_gps = kXSmemBytes / (M * G * 4);
-    if (gps > max_gps) return WQ_ERR_BAD_SHAPE;  // k beyond kMaxSlices * max_gps groups
-    S = (groups + gps - 1) / gps;
+    static bool attr_set = false;  // per process; the attribute is per function
+    if (!attr_set) {
+        const wq_status s =
+            wqh::cuda_status(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::CTA));
+        if (s != WQ_OK) return s;
+        attr_set = true;
+    }
+    const int64_t col_blocks = (n + kCols - 1) / kCols;
+    const int64_t rows = k / 8;
+    const int64_t nbw = (rows + kRPW - 1) / kRPW;  // 8-row warp batches per column block
+    // one wave: about as many CTAs as fit on the GPU at once, each warp walking
+    // several batches through its pipeline (and never more slices than the
+    // kMaxSlices the workspace holds)
+    const int64_t resident = wqh::grid_for(fn, kThreads, L::CTA, (int64_t)1 << 30, 1 << 30);
+    int64_t want = resident / col_blocks;
+    if (want < 1) want = 1;
+    if (want > kMaxSlices) want = kMaxSlices;
+    const int64_t batches = (nbw + 4 * want - 1) / (4 * want);
+    const int64_t S = (nbw + 4 * batches - 1) / (4 * batches);
+    if (S < 1 || batches >= (1ll << 31) || col_blocks >= (1ll << 31)) return WQ_ERR_BAD_SHAPE;
     // arrival counters: zero before the first call (the caller zeroes the
     // workspace once), reset to zero by the last CTA of every column block
     unsigned* counters = reinterpret_cast<unsigned*>(ws);
     float* part = reinterpret_cast<float*>(ws + ((col_blocks * 4 + 255) & ~(int64_t)255));
-    const size_t smem = (size_t)M * gps * G * sizeof(float);
-    gptq_linear_kernel<SYM, M, G><<<dim3((unsigned)col_blocks, (unsigned)S), kThreads, smem, st>>>(
-        x, qweight, qzeros, scales, n, k, (int)gps, part, counters, out_bf16, out);
+    gptq_linear_kernel<SYM, M, G><<<dim3((unsigned)col_blocks, (unsigned)S), kThreads, L::CTA, st>>>(
+        x, qweight, qzeros, scales, n, k, (int)batches, part, counters, out_bf16, out);
     return wqh::check_launch();
 }
 
@@ -372,7 +471,7 @@ extern "C" wq_status gptq_linear(const uint16_t* x, int64_t m, const int32_t* qw
                                                 (cudaStream_t)stream));
     if (!x || !qweight || !scales || !workspace || (!sym && !qzeros)) return WQ_ERR_NULL_PTR;
     if (workspace_bytes < gptq_linear_workspace_bytes(m, n)) return WQ_ERR_WORKSPACE_TOO_SMALL;
-    if (!wqh::aligned16(x) || !wqh::aligned_to(qweight, 4) || !wqh::aligned_to(scales, 2) ||
+    if (!wqh::aligned16(x) || !wqh::aligned16(qweight) || !wqh::aligned_to(scales, 2) ||
         (!sym && !wqh::aligned_to(qzeros, 4)) || !wqh::aligned_to(out, 4) ||
         !wqh::aligned_to(workspace, 256))
         return WQ_ERR_MISALIGNED;
