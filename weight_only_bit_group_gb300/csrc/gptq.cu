@@ -2,17 +2,18 @@
 // (export_gptq_cpu.py: pack_int32, quantize_sym, quantize_asym; module docstring
 // for the uint4b8 dequant rule).
 //
-// Quantize.  A warp owns a tile of 16 output channels (rows of w) x 128 input
-// channels (256 for group 256); lane h*16 + r owns row n0 + r and half h of the
-// tile's input channels.  Tiles are numbered K-fastest, so the warps that run at
-// the same time sweep long contiguous stretches of the same rows.  A tile
-// arrives in shared memory through a two-stage per-warp TMA pipeline: one lane
-// arms the stage's mbarrier and issues 2D tensor-map loads of 16 x 64 bf16
-// boxes with the 128-byte swizzle, which makes the per-lane 16-byte reads bank
-// conflict free; the next tile streams in while the current one is coded.  The
-// group max/min is a bf16x2 reduction inside the lane (plus one shuffle when a
-// group spans both halves); scale and zero point use true IEEE divisions once
-// per group.  Per element pair, with packed binary32 pairs (f32x2): the clamp
+// Quantize.  For groups up to 128 a warp owns a tile of 32 output channels (rows
+// of w) x 128 input channels and lane r owns row n0 + r, so each group lies in
+// one lane; for group 256 the tile is 16 rows x 256 channels and lane h*16 + r
+// owns half h of row n0 + r.  Tiles are numbered K-fastest, so the warps that
+// run at the same time sweep long contiguous stretches of the same rows.  A
+// tile arrives in shared memory through a two-stage per-warp TMA pipeline: one
+// lane arms the stage's mbarrier and issues 2D tensor-map loads of (32 or 16) x
+// 64 bf16 boxes with the 128-byte swizzle, which makes the per-lane 16-byte
+// reads bank conflict free; the next tile streams in while the current one is
+// coded.  The group max/min is a bf16x2 reduction inside the lane (plus one
+// shuffle when a group spans both halves); scale and zero point use true IEEE
+// divisions once per group (warp-uniformly through the rare large-scale path).  Per element pair, with packed binary32 pairs (f32x2): the clamp
 // to the code range is applied to w itself, in bf16x2, with bounds bf16(lo*s)
 // and bf16(hi*s) (exact, see bound2); the quotient by the scale is a correctly
 // rounded reciprocal plus one FMA correction step (bit-identical to IEEE
@@ -42,21 +43,21 @@ constexpr float kRcp15 = 1.0f / 15.0f;  // RN(1/15), correctly rounded by the co
 template <int G>
 struct QTile {
     static constexpr int KT = G > 128 ? G : 128;      // input channels per warp tile
-    static constexpr int R = 16;                       // output channels per warp tile
-    static constexpr int HALF = KT / 2;                // input channels per lane
+    static constexpr int P = G > 128 ? 2 : 1;          // lanes per row
+    static constexpr int R = 32 / P;                   // output channels per warp tile
+    static constexpr int HALF = KT / P;                // input channels per lane
     static constexpr int GL = G < HALF ? G : HALF;     // group elements one lane holds
     static constexpr int LPG = G / GL;                 // lanes per group (1 or 2)
-    static constexpr int NB = KT / 64;                 // TMA boxes (16 rows x 64 bf16) per tile
+    static constexpr int NB = KT / 64;                 // TMA boxes (R rows x 64 bf16) per tile
     static constexpr int BOXB = R * 128;               // bytes per box
-    static constexpr int STAGE = NB * BOXB;            // one stage of one warp
+    static constexpr int STAGE = NB * BOXB;            // one stage of one warp (8 KB)
     static constexpr int NS = 2;                       // pipeline stages
     static constexpr int WARPS = 4;                    // warps per CTA
     static constexpr int THREADS = 32 * WARPS;
     static constexpr int BARS = WARPS * NS * 8;        // mbarriers after the stages
     static constexpr int SMEM = NS * WARPS * STAGE + BARS + 1024;  // + room to align to 1 KB
-    // CTAs per SM: shared memory allows 6 (3 for 256-wide tiles); with the SNR
-    // sums the code needs more than the 80 registers that 6 CTAs leave
-    static constexpr int minb(bool snr) { return KT > 128 ? 3 : (snr ? 4 : 6); }
+    // CTAs per SM: shared memory allows 3
+    static constexpr int minb(bool) { return 3; }
 };
 
 // Per-group constants of the code computation.
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int row = lane & 15, half = lane >> 4;
+    const int row = lane % T::R, half = lane / T::R;  // half: which part of the row (P = 2 only)
     unsigned char* wsm = smem + warp * (T::NS * T::STAGE);
     const uint32_t wsm_s = (uint32_t)__cvta_generic_to_shared(wsm);
     const uint32_t bar_s = (uint32_t)__cvta_generic_to_shared(smem + T::WARPS * T::NS * T::STAGE) + warp * T::NS * 8;
@@ -177,7 +178,8 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
     // (the swizzle permutes the 16-byte chunks of each 128-byte box row by row % 8)
     uint32_t roff8[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) roff8[c] = (uint32_t)(half * (T::NB / 2) * T::BOXB + row * 128 + 16 * (c ^ (row & 7)));
+    for (int c = 0; c < 8; ++c)
+        roff8[c] = (uint32_t)(half * (T::NB / T::P) * T::BOXB + row * 128 + 16 * (c ^ (row & 7)));
 #define WQ_CHUNK(c) (*reinterpret_cast<const uint4*>(stage + roff8[(c) & 7] + ((c) >> 3) * T::BOXB))
 
     unsigned inflight = 0;  // bit i: a load into stage i has been issued and not yet waited for
@@ -235,7 +237,8 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
             const bool gval = kg < k;
             constexpr int GC = T::GL / 8;  // chunks per group part
             const int c0 = g * GC;
-            float s, zp;
+            float s, zp, rcp;
+            bool big;  // warp-uniform: some lane's scale is beyond 2^100 (IEEE divisions then)
             if (SYM) {
                 uint32_t m = 0;
 #pragma unroll
@@ -248,6 +251,8 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
                 const float amax = wq::bf_to_f(max(m & 0xffffu, m >> 16));
                 s = fmaxf(__fmul_rn(amax, 0.125f), 1e-9f);  // amax / 8: exact for any bf16 amax
                 zp = 8.0f;
+                big = __any_sync(0xffffffffu, s > 0x1p100f);
+                rcp = big ? 0.0f : __frcp_rn(s);
             } else {
                 const uint4 v0 = WQ_CHUNK(c0);
                 uint32_t mx = v0.x, mn = v0.x;
@@ -265,9 +270,21 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
                 const float wmin = fminf(wq::bf_lo(mn), wq::bf_hi(mn));
                 const float range = fmaxf(__fsub_rn(wmax, wmin), 1e-9f);
                 // range / 15 and -wmin / s as IEEE quotients: reciprocal + one FMA
-                // correction (exact while the operands stay in the normal range)
-                s = range <= 0x1p120f ? wq::div_by_recip(range, 15.0f, kRcp15) : __fdiv_rn(range, 15.0f);
-                const float q = s <= 0x1p100f ? wq::div_by_recip(-wmin, s, __frcp_rn(s)) : __fdiv_rn(-wmin, s);
+                // correction (exact while the operands stay in the normal range:
+                // range <= 2^100 keeps s, 1/s and the quotients there); a warp with
+                // a larger range anywhere takes true divisions on every lane, so
+                // that no lane branches around them alone
+                big = __any_sync(0xffffffffu, range > 0x1p100f);
+                float q;
+                if (!big) {
+                    s = wq::div_by_recip(range, 15.0f, kRcp15);
+                    rcp = __frcp_rn(s);
+                    q = wq::div_by_recip(-wmin, s, rcp);
+                } else {
+                    s = __fdiv_rn(range, 15.0f);
+                    rcp = 0.0f;
+                    q = __fdiv_rn(-wmin, s);
+                }
                 zp = fminf(fmaxf(rintf(q), 0.0f), 15.0f);
             }
             if (gval) {
@@ -277,9 +294,8 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
                 gc.lo2 = bound2(__fmul_rn(-zp, s));
                 gc.hi2 = bound2(__fmul_rn(15.0f - zp, s));
                 wq::f2_t sw2 = wq::f2(0.0f, 0.0f), se2 = sw2;
-                if (s <= 0x1p100f) {  // 1/s normal: the reciprocal + correction step is exact
-                    const float r = __frcp_rn(s);
-                    const wq::f2_t R2 = wq::f2(r, r), NS2 = wq::f2(-s, -s);
+                if (!big) {  // 1/s normal: the reciprocal + correction step is exact
+                    const wq::f2_t R2 = wq::f2(rcp, rcp), NS2 = wq::f2(-s, -s);
                     const uint32_t cg = (uint32_t)((int)zp - 0x4B400000) * 0x11111111u;
                     int32_t* qc = qp + (int64_t)c0 * n;
 #pragma unroll
@@ -289,14 +305,14 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
                         if (rowv) *qc = (int32_t)word;
                         qc += n;
                     }
-                } else {  // astronomically large scales: plain IEEE division
+                } else {  // astronomically large scales somewhere in the warp: IEEE division
                     const float lo = -zp, hi = 15.0f - zp;
                     float sw = 0.f, se = 0.f;
 #pragma unroll 1
                     for (int c = 0; c < GC; ++c) {
                         const int cc = c0 + c;
                         const uint4 v = *reinterpret_cast<const uint4*>(
-                            stage + half * (T::NB / 2) * T::BOXB + (cc >> 3) * T::BOXB + row * 128 +
+                            stage + half * (T::NB / T::P) * T::BOXB + (cc >> 3) * T::BOXB + row * 128 +
                             16 * ((cc & 7) ^ (row & 7)));
                         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
                         uint32_t word = 0;
@@ -326,7 +342,7 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
             const bool owner = T::LPG == 1 || half == 0;  // one lane writes per group
             if (gval && rowv && owner) scales[gi * n + col] = __half_as_ushort(__float2half_rn(s));
             if (qzeros) {
-                // zero points of 8 consecutive rows (lanes h*16 + r, r = 0..7 or 8..15)
+                // zero points of 8 consecutive rows (8 consecutive lanes of one part)
                 uint32_t zw = SYM ? 0x77777777u : ((uint32_t)zp << (4 * (row & 7)));
                 if (!SYM) {
                     zw |= __shfl_xor_sync(0xffffffffu, zw, 1);
@@ -375,14 +391,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Tensor map of w [n, k] bf16 (row-major): boxes of 16 rows x 64 values with the
+// Tensor map of w [n, k] bf16 (row-major): boxes of box_rows rows x 64 values with the
 // 128-byte swizzle; reads outside the tensor return zeros.
-wq_status weight_map(const uint16_t* w, int64_t n, int64_t k, CUtensorMap* map) {
+wq_status weight_map(const uint16_t* w, int64_t n, int64_t k, int box_rows, CUtensorMap* map) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return wqh::cuda_status(cudaErrorNotSupported);
     const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)n};
     const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
-    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(w), dims, strides,
                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -404,7 +420,7 @@ wq_status launch_quant(const uint16_t* w, int64_t n, int64_t k, int32_t* qweight
         attr_set = true;
     }
     CUtensorMap map;
-    wq_status s = weight_map(w, n, k, &map);
+    wq_status s = weight_map(w, n, k, T::R, &map);
     if (s != WQ_OK) return s;
     const int64_t warp_tiles = ((n + T::R - 1) / T::R) * ((k + T::KT - 1) / T::KT);
     const int grid = wqh::grid_for(fn, T::THREADS, T::SMEM, (warp_tiles + T::WARPS - 1) / T::WARPS,
