@@ -96,7 +96,11 @@ __device__ __forceinline__ wq::f2_t bf2_to_f2_fma(uint32_t u) {
 // per-group constant cg = (zp - bits(1.5*2^23)) * 0x11111111 (mod 2^32).
 // SNR terms as the page forms them: deq = RN((code - zp) * s), e = RN(w - deq)
 // (one mixed FMA reading w's bf16 half), e^2 and w^2 (mixed FMA) summed.
-template <bool SYM, bool SNR>
+// LO: apply the lower clamp.  rint(w/s) + zp < 0 needs w/s below -zp - 1/2; as
+// the quotients round monotonically and rint(RN(wmin/s)) = -rint(RN(-wmin/s)),
+// that happens only when the zero point was clamped down from above 15 (an
+// all-negative group), so callers request the clamp only then (and sym never).
+template <bool LO, bool SNR>
 __device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst& gc, const wq::f2_t R2,
                                                 const wq::f2_t NS2, uint32_t cg, wq::f2_t& sw2,
                                                 wq::f2_t& se2) {
@@ -106,7 +110,7 @@ __device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst&
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
         uint32_t uc = wq::bmin2(u[p], gc.hi2);
-        if (!SYM) uc = wq::bmax2(uc, gc.lo2);  // sym: w/s >= -8 always
+        if (LO) uc = wq::bmax2(uc, gc.lo2);
         const wq::f2_t x = bf2_to_f2_fma(uc);
         const wq::f2_t qa = wq::mul2(x, R2);
         const wq::f2_t rem = wq::fma2(qa, NS2, x);                          // x - qa*s, exact
@@ -156,8 +160,11 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
     using T = QTile<G>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // the 128-byte swizzle needs 1 KB aligned boxes
-    unsigned char* smem = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    // pointer arithmetic on the shared array (no integer round trip) keeps the
+    // shared address space visible, so the chunk reads below compile to 32-bit
+    // shared loads
+    unsigned char* smem =
+        smem_raw + ((1024u - ((uint32_t)__cvta_generic_to_shared(smem_raw) & 1023u)) & 1023u);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int row = lane % T::R, half = lane / T::R;  // half: which part of the row (P = 2 only)
     unsigned char* wsm = smem + warp * (T::NS * T::STAGE);
@@ -239,6 +246,7 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
             const int c0 = g * GC;
             float s, zp, rcp;
             bool big;  // warp-uniform: some lane's scale is beyond 2^100 (IEEE divisions then)
+            bool need_lo = false;  // asym: this lane's zero point was clamped from above 15
             if (SYM) {
                 uint32_t m = 0;
 #pragma unroll
@@ -285,8 +293,12 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
                     rcp = 0.0f;
                     q = __fdiv_rn(-wmin, s);
                 }
-                zp = fminf(fmaxf(rintf(q), 0.0f), 15.0f);
+                const float zr = rintf(q);
+                need_lo = zr > 15.0f;
+                zp = fminf(fmaxf(zr, 0.0f), 15.0f);
             }
+            // warp-uniform: the lower clamp only where a zero point was clamped from above
+            const bool lo_any = !SYM && __any_sync(0xffffffffu, need_lo);
             if (gval) {
                 GroupConst gc;
                 gc.s = s;
@@ -298,12 +310,22 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
                     const wq::f2_t R2 = wq::f2(rcp, rcp), NS2 = wq::f2(-s, -s);
                     const uint32_t cg = (uint32_t)((int)zp - 0x4B400000) * 0x11111111u;
                     int32_t* qc = qp + (int64_t)c0 * n;
+                    if (lo_any) {
 #pragma unroll
-                    for (int c = 0; c < GC; ++c) {
-                        const uint4 v = WQ_CHUNK(c0 + c);
-                        const uint32_t word = quant_chunk<SYM, SNR>(v, gc, R2, NS2, cg, sw2, se2);
-                        if (rowv) *qc = (int32_t)word;
-                        qc += n;
+                        for (int c = 0; c < GC; ++c) {
+                            const uint4 v = WQ_CHUNK(c0 + c);
+                            const uint32_t word = quant_chunk<true, SNR>(v, gc, R2, NS2, cg, sw2, se2);
+                            if (rowv) *qc = (int32_t)word;
+                            qc += n;
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < GC; ++c) {
+                            const uint4 v = WQ_CHUNK(c0 + c);
+                            const uint32_t word = quant_chunk<false, SNR>(v, gc, R2, NS2, cg, sw2, se2);
+                            if (rowv) *qc = (int32_t)word;
+                            qc += n;
+                        }
                     }
                 } else {  // astronomically large scales somewhere in the warp: IEEE division
                     const float lo = -zp, hi = 15.0f - zp;
@@ -330,7 +352,7 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
                     sw2 = wq::f2(sw, 0.f);
                     se2 = wq::f2(se, 0.f);
                 }
-                if (SNR && rowv) {
+                if (SNR) {  // rows past n hold zeros (the tensor map fills them): zero terms
                     float a0, a1, b0, b1;
                     wq::f2u(sw2, a0, a1);
                     wq::f2u(se2, b0, b1);
