@@ -77,18 +77,6 @@ __device__ __forceinline__ uint32_t bound2(float v) {
     return b | (b << 16);
 }
 
-// bf16 pair -> two binary32 values through mixed-precision FMAs (w * 1 - 0, exact)
-// that read the bf16 halves in place: the unpacking runs on the FMA pipe, not on
-// the integer pipe that the clamps and the nibble pack already keep busy.
-__device__ __forceinline__ wq::f2_t bf2_to_f2_fma(uint32_t u) {
-    float lo, hi;
-    asm("{\n\t.reg .b16 l, h, one;\n\tmov.b32 {l, h}, %2;\n\tmov.b16 one, 0x3F80;\n\t"
-        "fma.rn.f32.bf16 %0, l, one, %3;\n\tfma.rn.f32.bf16 %1, h, one, %3;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(u), "f"(-0.0f));
-    return wq::f2(lo, hi);
-}
-
 // Codes of one 8-value chunk (one qweight word) and the SNR terms, on packed
 // binary32 pairs.  Per value: clamp (bf16x2, on w), q = RN(w/s) by reciprocal +
 // correction, t = rint(q) + 1.5*2^23 from the binary32 adder; the low bits of
@@ -111,7 +99,9 @@ __device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst&
     for (int p = 0; p < 4; ++p) {
         uint32_t uc = wq::bmin2(u[p], gc.hi2);
         if (LO) uc = wq::bmax2(uc, gc.lo2);
-        const wq::f2_t x = bf2_to_f2_fma(uc);
+        // bf16 pair -> binary32 pair on the integer pipe (byte permute, mask): the
+        // FMA pipe already carries the packed quotient and SNR arithmetic
+        const wq::f2_t x = wq::f2(__uint_as_float(__byte_perm(uc, 0u, 0x1044)), __uint_as_float(uc & 0xffff0000u));
         const wq::f2_t qa = wq::mul2(x, R2);
         const wq::f2_t rem = wq::fma2(qa, NS2, x);                          // x - qa*s, exact
         const wq::f2_t tq = wq::add2(wq::fma2(rem, R2, qa), M2);            // rint(RN(x/s)) + 1.5*2^23
@@ -297,6 +287,11 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
                 need_lo = zr > 15.0f;
                 zp = fminf(fmaxf(zr, 0.0f), 15.0f);
             }
+            // the coding pass reads the chunks from shared memory again: holding all
+            // of the group's chunks in registers between the two passes left too few
+            // registers to interleave the per-pair chains (measured: sym 74.2 -> 68.2 us
+            // on a 16384 x 8192 weight together with the integer-pipe unpacking)
+            asm volatile("" ::: "memory");
             // warp-uniform: the lower clamp only where a zero point was clamped from above
             const bool lo_any = !SYM && __any_sync(0xffffffffu, need_lo);
             if (gval) {
