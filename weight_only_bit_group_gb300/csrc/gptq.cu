@@ -82,13 +82,20 @@ __device__ __forceinline__ uint32_t bound2(float v) {
 // correction, t = rint(q) + 1.5*2^23 from the binary32 adder; the low bits of
 // t hold rint(q), and the word is sum over i of bits(t_i) << 4i plus the
 // per-group constant cg = (zp - bits(1.5*2^23)) * 0x11111111 (mod 2^32).
-// SNR terms as the page forms them: deq = RN((code - zp) * s), e = RN(w - deq)
-// (one mixed FMA reading w's bf16 half), e^2 and w^2 (mixed FMA) summed.
-// LO: apply the lower clamp.  rint(w/s) + zp < 0 needs w/s below -zp - 1/2; as
-// the quotients round monotonically and rint(RN(wmin/s)) = -rint(RN(-wmin/s)),
-// that happens only when the zero point was clamped down from above 15 (an
-// all-negative group), so callers request the clamp only then (and sym never).
-template <bool LO, bool SNR>
+// SNR terms as the page forms them: deq = RN((code - zp) * s), e = RN(w - deq),
+// e^2 and w^2 summed (each a single-rounding FMA).
+// CLAMP selects the clamps applied to w before the division:
+//   0  none: every code of the warp's groups is already in [0, 15], so the
+//      unpacked x is w itself and the SNR terms come from it in f32x2
+//   1  the upper one (sym: the positive extreme amax / s = 8 rounds to code 16)
+//   2  both (asym groups whose extreme codes leave [0, 15]).  rint(w/s) + zp < 0
+//      needs w/s below -zp - 1/2; as the quotients round monotonically and
+//      rint(RN(wmin/s)) = -rint(RN(-wmin/s)), that happens only when the zero
+//      point was clamped down from above 15 (an all-negative group); the upper
+//      end, rint(RN(wmax/s)) + zp > 15, is tested exactly per group
+// With a clamp, x may differ from w, so e and w^2 read w's bf16 halves by
+// mixed-precision FMAs instead.
+template <int CLAMP, bool SNR>
 __device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst& gc, const wq::f2_t R2,
                                                 const wq::f2_t NS2, uint32_t cg, wq::f2_t& sw2,
                                                 wq::f2_t& se2) {
@@ -97,8 +104,9 @@ __device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst&
     uint32_t word = cg;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        uint32_t uc = wq::bmin2(u[p], gc.hi2);
-        if (LO) uc = wq::bmax2(uc, gc.lo2);
+        uint32_t uc = u[p];
+        if (CLAMP >= 1) uc = wq::bmin2(uc, gc.hi2);
+        if (CLAMP == 2) uc = wq::bmax2(uc, gc.lo2);
         // bf16 pair -> binary32 pair on the integer pipe (byte permute, mask): the
         // FMA pipe already carries the packed quotient and SNR arithmetic
         const wq::f2_t x = wq::f2(__uint_as_float(__byte_perm(uc, 0u, 0x1044)), __uint_as_float(uc & 0xffff0000u));
@@ -109,7 +117,12 @@ __device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst&
         wq::f2u(tq, t0, t1);
         word += (uint32_t)__float_as_int(t0) << (8 * p);
         word += (uint32_t)__float_as_int(t1) << (8 * p + 4);
-        if (SNR) {
+        if (SNR && CLAMP == 0) {
+            const wq::f2_t nd = wq::mul2(wq::add2(tq, NM2), NS2);  // -deq = -RN((code - zp) * s)
+            const wq::f2_t e = wq::add2(x, nd);                    // RN(w - deq)
+            se2 = wq::fma2(e, e, se2);
+            sw2 = wq::fma2(x, x, sw2);
+        } else if (SNR) {
             const wq::f2_t nd = wq::mul2(wq::add2(tq, NM2), NS2);  // -deq = -RN((code - zp) * s)
             float e0, e1, w0, w1;
             asm("{\n\t.reg .b16 l, h, one;\n\tmov.b32 {l, h}, %4;\n\tmov.b16 one, 0x3F80;\n\t"
@@ -236,7 +249,7 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
             const int c0 = g * GC;
             float s, zp, rcp;
             bool big;  // warp-uniform: some lane's scale is beyond 2^100 (IEEE divisions then)
-            bool need_lo = false;  // asym: this lane's zero point was clamped from above 15
+            bool need_clamp = false;  // asym: some code of this lane's group leaves [0, 15]
             if (SYM) {
                 uint32_t m = 0;
 #pragma unroll
@@ -284,16 +297,19 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
                     q = __fdiv_rn(-wmin, s);
                 }
                 const float zr = rintf(q);
-                need_lo = zr > 15.0f;
                 zp = fminf(fmaxf(zr, 0.0f), 15.0f);
+                // the largest code is the one of wmax (the same correctly rounded
+                // quotient as the coding pass; ignored on the IEEE-division path)
+                const float cmax = big ? 0.0f : __fadd_rn(rintf(wq::div_by_recip(wmax, s, rcp)), zp);
+                need_clamp = zr > 15.0f || cmax > 15.0f;
             }
             // the coding pass reads the chunks from shared memory again: holding all
             // of the group's chunks in registers between the two passes left too few
             // registers to interleave the per-pair chains (measured: sym 74.2 -> 68.2 us
             // on a 16384 x 8192 weight together with the integer-pipe unpacking)
             asm volatile("" ::: "memory");
-            // warp-uniform: the lower clamp only where a zero point was clamped from above
-            const bool lo_any = !SYM && __any_sync(0xffffffffu, need_lo);
+            // warp-uniform: asym clamps only in warps where some group needs it
+            const bool clamp_any = !SYM && __any_sync(0xffffffffu, need_clamp);
             if (gval) {
                 GroupConst gc;
                 gc.s = s;
@@ -305,19 +321,20 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
                     const wq::f2_t R2 = wq::f2(rcp, rcp), NS2 = wq::f2(-s, -s);
                     const uint32_t cg = (uint32_t)((int)zp - 0x4B400000) * 0x11111111u;
                     int32_t* qc = qp + (int64_t)c0 * n;
-                    if (lo_any) {
-#pragma unroll
+                    if (SYM || clamp_any) {
+#pragma unroll(SYM ? GC : 8)
                         for (int c = 0; c < GC; ++c) {
                             const uint4 v = WQ_CHUNK(c0 + c);
-                            const uint32_t word = quant_chunk<true, SNR>(v, gc, R2, NS2, cg, sw2, se2);
+                            const uint32_t word =
+                                quant_chunk<SYM ? 1 : 2, SNR>(v, gc, R2, NS2, cg, sw2, se2);
                             if (rowv) *qc = (int32_t)word;
                             qc += n;
                         }
                     } else {
-#pragma unroll
+#pragma unroll 8
                         for (int c = 0; c < GC; ++c) {
                             const uint4 v = WQ_CHUNK(c0 + c);
-                            const uint32_t word = quant_chunk<false, SNR>(v, gc, R2, NS2, cg, sw2, se2);
+                            const uint32_t word = quant_chunk<0, SNR>(v, gc, R2, NS2, cg, sw2, se2);
                             if (rowv) *qc = (int32_t)word;
                             qc += n;
                         }
