@@ -44,9 +44,12 @@ constexpr int X_BYTES = BT * BK * 2;       // x tile, bf16, 128-byte swizzle
 constexpr int Q_BYTES = (BK / 8) * BM * 4; // raw qweight rows
 constexpr int STAGE = X_BYTES + Q_BYTES;    // the A operand lives in TMEM
 constexpr int BAR_OFF = NS * STAGE;
-// barriers: full[NS] aready[NS] empty[NS] tfull[2] tempty[2] done; then the TMEM
-// address slot and the abort flag
-constexpr int N_BARS = 3 * NS + 5;
+// barriers: full[NS] (one per K block stage), aready[NS / 2] and empty[NS / 2]
+// (one per pair of stages: the MMA thread consumes K blocks two at a time),
+// tfull[2] tempty[2] done; then the TMEM address slot and the abort flag
+constexpr int NP = NS / 2;                 // stage pairs
+constexpr int N_BARS = NS + 2 * NP + 5;
+static_assert(NS % 2 == 0, "stages are consumed in pairs");
 constexpr int SLOT_OFF = BAR_OFF + 8 * N_BARS;
 constexpr int SMEM = SLOT_OFF + 16 + 1024;  // + slack to align the tiles to 1024 bytes
 constexpr int DQ_WARPS = 8;                // dequant warps: two per feature row
@@ -238,11 +241,13 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     auto q_at = [&](int s) { return smem + s * STAGE + X_BYTES; };
     const uint32_t bar0 = sbase + BAR_OFF;
     auto full = [&](int s) { return bar0 + 8 * s; };
-    auto aready = [&](int s) { return bar0 + 8 * (NS + s); };
-    auto empty = [&](int s) { return bar0 + 8 * (2 * NS + s); };
-    auto tfull = [&](int b) { return bar0 + 8 * (3 * NS + b); };
-    auto tempty = [&](int b) { return bar0 + 8 * (3 * NS + 2 + b); };
-    const uint32_t done = bar0 + 8 * (3 * NS + 4);
+    // pair barriers of K blocks kb, kb + 1 (kb even): slot (kb / 2) % NP, used once
+    // per NS K blocks, so a wait's parity is (kb / NS) & 1 as for the stages
+    auto aready = [&](int kb) { return bar0 + 8 * (NS + (kb >> 1) % NP); };
+    auto empty = [&](int kb) { return bar0 + 8 * (NS + NP + (kb >> 1) % NP); };
+    auto tfull = [&](int b) { return bar0 + 8 * (NS + 2 * NP + b); };
+    auto tempty = [&](int b) { return bar0 + 8 * (NS + 2 * NP + 2 + b); };
+    const uint32_t done = bar0 + 8 * (NS + 2 * NP + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SLOT_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SLOT_OFF + 4);
 
@@ -264,10 +269,10 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     const int ngroups = UX ? 1 : k / G;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            wq::mbar_init(full(s), 1);
-            wq::mbar_init(aready(s), DQ_WARPS);
-            wq::mbar_init(empty(s), 1);
+        for (int s = 0; s < NS; ++s) wq::mbar_init(full(s), 1);
+        for (int q = 0; q < NP; ++q) {
+            wq::mbar_init(aready(2 * q), DQ_WARPS);
+            wq::mbar_init(empty(2 * q), 1);
         }
         for (int b = 0; b < 2; ++b) {
             wq::mbar_init(tfull(b), 1);
@@ -290,7 +295,8 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             for (int kb = 0; kb < nkb; ++kb) {
                 const int s = kb % NS;
                 const uint32_t u = (uint32_t)(kb / NS);
-                if (!wait_bar(empty(s), (u & 1u) ^ 1u, abort_flag)) break;
+                // both stages of a pair are released together
+                if ((kb & 1) == 0 && !wait_bar(empty(kb), (u & 1u) ^ 1u, abort_flag)) break;
                 wq::mbar_expect_tx(full(s), UX ? X_BYTES : X_BYTES + Q_BYTES);
                 wq::tma_load_2d(x_at(s), &xmap, kb * BK, t0, full(s));
                 if (UX == 0)
@@ -320,14 +326,9 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                     tc_mma_ta(tmem + b * BT, da + (uint32_t)(ks * 8), db + (uint64_t)(ks * 2), kIdesc,
                               (fresh && ks == ks0) ? 0u : 1u);
             };
-            bool ok = true;
-            for (int kb = 0; kb < nkb && ok; ++kb) {
+            // MMAs of one K block; false when a wait for a free accumulator gave up
+            auto block = [&](int kb) -> bool {
                 const int s = kb % NS;
-                const uint32_t par = (uint32_t)(kb / NS) & 1u;
-                if (!wait_bar(full(s), par, abort_flag, mma_slices) ||
-                    !wait_bar(aready(s), par, abort_flag, mma_slices))
-                    break;
-                tc_fence_after();
                 const uint32_t da = tmem + (uint32_t)(A_COL0 + s * (BK / 2));
                 const uint64_t db = db0 + (uint64_t)((s * STAGE) >> 4);
                 if constexpr (UX != 0) {
@@ -341,7 +342,8 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                     const uint32_t b = (uint32_t)g & 1u;
                     const bool gstart = (kb & (BPG - 1)) == 0;
                     if (gstart) {
-                        if (!wait_bar(tempty(b), ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag, mma_slices)) break;
+                        if (!wait_bar(tempty(b), ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag, mma_slices))
+                            return false;
                         tc_fence_after();
                     }
                     mmas(da, db, b, 0, BK / 16, gstart);
@@ -350,19 +352,27 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                     // G == 32: groups 2kb (accumulator 0, K steps 0-1) and 2kb+1
                     // (accumulator 1, K steps 2-3; absent in a half-full last block)
                     const int halves = (k - kb * BK) >= BK ? 2 : 1;
-                    for (int hh = 0; hh < halves && ok; ++hh) {
+                    for (int hh = 0; hh < halves; ++hh) {
                         const int g = 2 * kb + hh;
                         if (!wait_bar(tempty((uint32_t)hh), ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag,
-                                      mma_slices)) {
-                            ok = false;
-                            break;
-                        }
+                                      mma_slices))
+                            return false;
                         tc_fence_after();
                         mmas(da, db, (uint32_t)hh, 2 * hh, 2 * hh + 2, true);
                         tc_commit(tfull((uint32_t)hh));
                     }
                 }
-                tc_commit(empty(s));
+                return true;
+            };
+            // K blocks two at a time: one wait, one fence and one stage release per
+            // pair.  aready completes only after every dequant warp saw both stages'
+            // copies land (it waits on full first), so it orders the x tiles too.
+            for (int kb = 0; kb < nkb; kb += 2) {
+                if (!wait_bar(aready(kb), (uint32_t)(kb / NS) & 1u, abort_flag, mma_slices)) break;
+                tc_fence_after();
+                if (!block(kb)) break;
+                if (kb + 1 < nkb && !block(kb + 1)) break;
+                tc_commit(empty(kb));
             }
             // every MMA issued has completed before TMEM can be freed
             tc_commit(done);
@@ -468,7 +478,8 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(aready(s));
+            // one arrival per pair of K blocks (or for a last, unpaired block)
+            if (lane == 0 && ((kb & 1) || kb + 1 == nkb)) mbar_arrive(aready(kb & ~1));
         }
       } else {
         // ---------------------------------------------------------- dequant
@@ -523,10 +534,7 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(aready(kb % NS));
-                if (two) mbar_arrive(aready((kb + 1) % NS));
-            }
+            if (lane == 0) mbar_arrive(aready(kb));
         }
       }
     } else {
