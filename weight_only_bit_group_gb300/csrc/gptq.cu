@@ -25,7 +25,9 @@
 // out records WQ_ERR_DEVICE_TIMEOUT in a device status word (read by
 // wq_device_status) and the kernel finishes without touching the stage again.
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 #include <atomic>
+#include <type_traits>
 #include <mutex>
 
 #include "wq_common.cuh"
@@ -408,6 +410,316 @@ __global__ void __launch_bounds__(QTile<G>::THREADS, QTile<G>::minb(SNR)) gptq_q
 }
 #undef WQ_CHUNK
 
+// ------------------------------------------------------------------ fp16 / fp32 weights
+// export_gptq_cpu.py quantizes w.float(): an fp16 or fp32 weight takes the same
+// binary32 steps with more significant bits, so the bf16 kernel's shortcuts
+// (bf16x2 clamps on w, exact squares) do not carry over.  Same warp-tile
+// pipeline: a warp stage is 8 KB, i.e. R rows x KT channels with R = 32 (fp16)
+// or 16 (fp32) for KT = 128; a row spans P = 32 / R lanes.  The clamp acts on
+// the rounded quotient t = rint(RN(w/s)) + 1.5*2^23 (exact for |w/s| < 2^22,
+// which the per-group test below guarantees), and only in warps where some
+// group's extreme code leaves [0, 15].
+template <int DT, int G>
+struct WTile {
+    static constexpr int ES = DT == WQ_DTYPE_F32 ? 4 : 2;  // element bytes
+    static constexpr int BI = 128 / ES;                     // elements per 128-byte box row
+    static constexpr int KT = G > 128 ? G : 128;            // input channels per warp tile
+    static constexpr int R = 8192 / (KT * ES);              // output channels per warp tile
+    static constexpr int P = 32 / R;                        // lanes per row
+    static constexpr int HALF = KT / P;                     // input channels per lane
+    static constexpr int GL = G < HALF ? G : HALF;          // group elements one lane holds
+    static constexpr int LPG = G / GL;                      // lanes per group
+    static constexpr int NB = KT / BI;                      // TMA boxes (R rows x 128 B) per tile
+    static constexpr int BOXB = R * 128;
+    static constexpr int STAGE = NB * BOXB;
+    static constexpr int CPW = ES / 2;                      // 16-byte chunks per qweight word
+    static constexpr int PPC = 4 / CPW;                     // binary32 pairs per chunk
+    static constexpr int NS = 2, WARPS = 4, THREADS = 32 * WARPS;
+    static constexpr int SMEM = NS * WARPS * STAGE + WARPS * NS * 8 + 1024;
+    static_assert(STAGE == 8192 && R >= 8 && R <= 32 && HALF % BI == 0, "warp tile");
+};
+
+// The 16-byte chunk `c` of w values held by this lane, as binary32 pairs
+// (fp16 widens exactly): two pairs per chunk for fp32, four for fp16.
+template <int DT>
+__device__ __forceinline__ void chunk_pairs(const uint4 v, wq::f2_t (&x)[4]) {
+    if (DT == WQ_DTYPE_F32) {
+        x[0] = wq::f2(__uint_as_float(v.x), __uint_as_float(v.y));
+        x[1] = wq::f2(__uint_as_float(v.z), __uint_as_float(v.w));
+    } else {
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+            x[i] = wq::f2(f.x, f.y);
+        }
+    }
+}
+
+// Codes (4 bits each, added into `word` from nibble `nib`) and SNR terms of one
+// binary32 pair.  CLAMP: 0 none, 1 the upper end, 2 both.
+template <int CLAMP, bool SNR>
+__device__ __forceinline__ void wide_pair(const wq::f2_t x, const wq::f2_t R2, const wq::f2_t NS2, float tlo,
+                                          float thi, uint32_t& word, int nib, wq::f2_t& sw2, wq::f2_t& se2) {
+    const wq::f2_t qa = wq::mul2(x, R2);
+    const wq::f2_t rem = wq::fma2(qa, NS2, x);                                 // x - qa*s, exact
+    const wq::f2_t tq = wq::add2(wq::fma2(rem, R2, qa), wq::f2(kMagic, kMagic));  // rint(RN(x/s)) + 1.5*2^23
+    float t0, t1;
+    wq::f2u(tq, t0, t1);
+    if (CLAMP >= 1) { t0 = fminf(t0, thi); t1 = fminf(t1, thi); }
+    if (CLAMP == 2) { t0 = fmaxf(t0, tlo); t1 = fmaxf(t1, tlo); }
+    word += (uint32_t)__float_as_int(t0) << (4 * nib);
+    word += (uint32_t)__float_as_int(t1) << (4 * nib + 4);
+    if (SNR) {
+        // deq = RN((code - zp) * s), e = RN(w - deq); squares summed by FMAs
+        const wq::f2_t nd = wq::mul2(wq::add2(wq::f2(t0, t1), wq::f2(-kMagic, -kMagic)), NS2);
+        const wq::f2_t e = wq::add2(x, nd);
+        se2 = wq::fma2(e, e, se2);
+        sw2 = wq::fma2(x, x, sw2);
+    }
+}
+
+template <bool SYM, int DT, int G, bool SNR>
+__global__ void __launch_bounds__(WTile<DT, G>::THREADS, 3) gptq_quant_wide_kernel(
+    const __grid_constant__ CUtensorMap wmap, int64_t n, int64_t k, int32_t* __restrict__ qweight,
+    int32_t* __restrict__ qzeros, uint16_t* __restrict__ scales, int32_t* __restrict__ g_idx,
+    float4* __restrict__ slots, unsigned* __restrict__ counter, double* __restrict__ snr_db,
+    unsigned max_polls) {
+    using T = WTile<DT, G>;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned char* smem =
+        smem_raw + ((1024u - ((uint32_t)__cvta_generic_to_shared(smem_raw) & 1023u)) & 1023u);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int row = lane % T::R, part = lane / T::R;
+    unsigned char* wsm = smem + warp * (T::NS * T::STAGE);
+    const uint32_t wsm_s = (uint32_t)__cvta_generic_to_shared(wsm);
+    const uint32_t bar_s =
+        (uint32_t)__cvta_generic_to_shared(smem + T::WARPS * T::NS * T::STAGE) + warp * T::NS * 8;
+    const int tn = (int)((n + T::R - 1) / T::R), tk = (int)((k + T::KT - 1) / T::KT);
+    const int gwarp = blockIdx.x * T::WARPS + warp;
+    const int nwarps = gridDim.x * T::WARPS;
+    const int dn = nwarps / tk, dk = nwarps % tk;
+    if (lane == 0) {
+        for (int i = 0; i < T::NS; ++i) wq::mbar_init(bar_s + 8 * i, 1);
+        wq::mbar_fence_init();
+    }
+    __syncwarp();
+    // chunk c of this lane's part of its row: box part * (HALF / BI) + c / 8, with
+    // the 128-byte swizzle permuting the 16-byte chunks of each box row by row % 8
+    uint32_t roff8[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        roff8[c] = (uint32_t)(part * (T::HALF / T::BI) * T::BOXB + row * 128 + 16 * (c ^ (row & 7)));
+#define WQ_WCHUNK(c) (*reinterpret_cast<const uint4*>(stage + roff8[(c) & 7] + ((c) >> 3) * T::BOXB))
+
+    unsigned inflight = 0;
+    auto issue = [&](int nb, int kb, int st) {
+        if (nb < tn) {
+            if (lane == 0) {
+                const uint32_t bar = bar_s + 8 * st, dst = wsm_s + st * T::STAGE;
+                wq::mbar_expect_tx(bar, T::STAGE);
+#pragma unroll
+                for (int b = 0; b < T::NB; ++b)
+                    wq::tma_load_2d(dst + b * T::BOXB, &wmap, kb * T::KT + T::BI * b, nb * T::R, bar);
+            }
+            inflight |= 1u << st;
+        }
+    };
+    wq::KSum ksw, kse;
+    bool ok = true;
+    int nb = gwarp / tk, kb = gwarp % tk;
+    int na = nb, ka = kb;
+    auto step = [&](int& x, int& y) {
+        x += dn;
+        y += dk;
+        if (y >= tk) { y -= tk; ++x; }
+    };
+    issue(na, ka, 0);
+    step(na, ka);
+    int st = 0, ahead = 1;
+    uint32_t parity = 0;
+    constexpr int GC = T::GL * T::ES / 16;  // chunks per group part
+    constexpr unsigned FULL = 0xffffffffu;
+    for (; nb < tn;) {
+        issue(na, ka, ahead);
+        step(na, ka);
+        ahead ^= 1;
+        if (!wait_stage(bar_s + 8 * st, parity, max_polls)) {
+            atomicExch(&g_device_status, (unsigned)WQ_ERR_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+        }
+        inflight &= ~(1u << st);
+        const int64_t n0 = (int64_t)nb * T::R, k0 = (int64_t)kb * T::KT;
+        const int64_t col = n0 + row;
+        const bool rowv = col < n;
+        const int64_t kl = k0 + part * T::HALF;
+        const unsigned char* stage = wsm + st * T::STAGE;
+        int32_t* qp = qweight + (kl / 8) * n + col;
+#pragma unroll
+        for (int g = 0; g < T::HALF / T::GL; ++g) {
+            const int64_t kg = kl + g * T::GL;
+            const bool gval = kg < k;
+            const int c0 = g * GC;
+            // group statistics (exact: fp16 pairs by half2 max / min, fp32 values
+            // one by one)
+            float wmax = -INFINITY, wmin = INFINITY;
+            if (DT == WQ_DTYPE_F16) {
+                const uint4 v0 = WQ_WCHUNK(c0);
+                __half2 mx = *reinterpret_cast<const __half2*>(&v0.x), mn = mx;
+#pragma unroll
+                for (int c = 0; c < GC; ++c) {
+                    const uint4 v = WQ_WCHUNK(c0 + c);
+                    const __half2* h = reinterpret_cast<const __half2*>(&v);
+                    mx = __hmax2(mx, __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3])));
+                    mn = __hmin2(mn, __hmin2(__hmin2(h[0], h[1]), __hmin2(h[2], h[3])));
+                }
+                const float2 fx = __half22float2(mx), fn = __half22float2(mn);
+                wmax = fmaxf(fx.x, fx.y);
+                wmin = fminf(fn.x, fn.y);
+            } else {
+#pragma unroll
+                for (int c = 0; c < GC; ++c) {
+                    wq::f2_t x[4];
+                    chunk_pairs<DT>(WQ_WCHUNK(c0 + c), x);
+#pragma unroll
+                    for (int i = 0; i < T::PPC; ++i) {
+                        wmax = fmaxf(wmax, fmaxf(x[i].x, x[i].y));
+                        wmin = fminf(wmin, fminf(x[i].x, x[i].y));
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = T::R; o < T::R * T::LPG; o <<= 1) {
+                wmax = fmaxf(wmax, __shfl_xor_sync(FULL, wmax, o));
+                wmin = fminf(wmin, __shfl_xor_sync(FULL, wmin, o));
+            }
+            float s, zp, rcp = 0.0f, q0 = 0.0f;
+            bool big, need = false;
+            if (SYM) {
+                const float amax = fmaxf(wmax, -wmin);
+                s = fmaxf(__fmul_rn(amax, 0.125f), 1e-9f);  // amax / 8: exact
+                zp = 8.0f;
+                big = __any_sync(FULL, s > 0x1p100f);
+                if (!big) rcp = __frcp_rn(s);
+            } else {
+                const float range = fmaxf(__fsub_rn(wmax, wmin), 1e-9f);
+                // the fast path needs normal quotients and |w / s| < 2^22 (the
+                // adder rounding): range <= 2^100 and |w| <= 2^16 range
+                big = __any_sync(FULL, range > 0x1p100f || fmaxf(wmax, -wmin) > __fmul_rn(range, 0x1p16f));
+                if (!big) {
+                    s = wq::div_by_recip(range, 15.0f, kRcp15);
+                    rcp = __frcp_rn(s);
+                    q0 = wq::div_by_recip(-wmin, s, rcp);
+                } else {
+                    s = __fdiv_rn(range, 15.0f);
+                    q0 = __fdiv_rn(-wmin, s);
+                }
+                const float zr = rintf(q0);
+                zp = fminf(fmaxf(zr, 0.0f), 15.0f);
+                // the extreme codes: wmin's is -rint(q0) + zp (< 0 only when zp was
+                // clamped down), wmax's from the same quotient as the coding pass
+                const float cmax = big ? 0.0f : __fadd_rn(rintf(wq::div_by_recip(wmax, s, rcp)), zp);
+                need = zr > 15.0f || cmax > 15.0f;
+            }
+            asm volatile("" ::: "memory");  // the coding pass reads the chunks again
+            const bool clamp_any = !SYM && __any_sync(FULL, need);
+            if (gval) {
+                wq::f2_t sw2 = wq::f2(0.0f, 0.0f), se2 = sw2;
+                if (!big) {
+                    const wq::f2_t R2 = wq::f2(rcp, rcp), NS2 = wq::f2(-s, -s);
+                    const float tlo = __fsub_rn(kMagic, zp), thi = __fadd_rn(kMagic, __fsub_rn(15.0f, zp));
+                    const uint32_t cg = (uint32_t)((int)zp - 0x4B400000) * 0x11111111u;
+                    int32_t* qc = qp + (int64_t)(c0 / T::CPW) * n;
+                    auto code = [&](auto clamp_tag) {
+                        constexpr int CL = decltype(clamp_tag)::value;
+#pragma unroll(SYM ? GC / T::CPW : 8)
+                        for (int wd = 0; wd < GC / T::CPW; ++wd) {
+                            uint32_t word = cg;
+#pragma unroll
+                            for (int h = 0; h < T::CPW; ++h) {
+                                wq::f2_t x[4];
+                                chunk_pairs<DT>(WQ_WCHUNK(c0 + wd * T::CPW + h), x);
+#pragma unroll
+                                for (int i = 0; i < T::PPC; ++i)
+                                    wide_pair<CL, SNR>(x[i], R2, NS2, tlo, thi, word, 2 * (h * T::PPC + i),
+                                                       sw2, se2);
+                            }
+                            if (rowv) *qc = (int32_t)word;
+                            qc += n;
+                        }
+                    };
+                    if (SYM) code(std::integral_constant<int, 1>());
+                    else if (clamp_any) code(std::integral_constant<int, 2>());
+                    else code(std::integral_constant<int, 0>());
+                } else {  // astronomical ratios somewhere in the warp: IEEE division
+                    const float lo = -zp, hi = 15.0f - zp;
+                    float sw = 0.f, se = 0.f;
+#pragma unroll 1
+                    for (int wd = 0; wd < GC / T::CPW; ++wd) {
+                        uint32_t word = 0;
+                        for (int h = 0; h < T::CPW; ++h) {
+                            const int cc = c0 + wd * T::CPW + h;
+                            const uint4 v = *reinterpret_cast<const uint4*>(
+                                stage + part * (T::HALF / T::BI) * T::BOXB + (cc >> 3) * T::BOXB + row * 128 +
+                                16 * ((cc & 7) ^ (row & 7)));
+                            wq::f2_t x[4];
+                            chunk_pairs<DT>(v, x);
+                            for (int i = 0; i < T::PPC; ++i) {
+                                const float xv[2] = {x[i].x, x[i].y};
+                                for (int e = 0; e < 2; ++e) {
+                                    const float rq = rintf(fminf(fmaxf(__fdiv_rn(xv[e], s), lo), hi));
+                                    const int nibble = 2 * (h * T::PPC + i) + e;
+                                    word |= (uint32_t)((int)rq + (int)zp) << (4 * nibble);
+                                    const float dd = __fsub_rn(xv[e], __fmul_rn(rq, s));
+                                    sw = __fmaf_rn(xv[e], xv[e], sw);
+                                    se = __fmaf_rn(dd, dd, se);
+                                }
+                            }
+                        }
+                        if (rowv) qp[(int64_t)(c0 / T::CPW + wd) * n] = (int32_t)word;
+                    }
+                    sw2 = wq::f2(sw, 0.f);
+                    se2 = wq::f2(se, 0.f);
+                }
+                if (SNR) {  // rows past n hold zeros (the tensor map fills them): zero terms
+                    float a0, a1, b0, b1;
+                    wq::f2u(sw2, a0, a1);
+                    wq::f2u(se2, b0, b1);
+                    ksw.add(__fadd_rn(a0, a1));
+                    kse.add(__fadd_rn(b0, b1));
+                }
+            }
+            const int64_t gi = kg / G;
+            const bool owner = part % T::LPG == 0;  // one lane writes per group
+            if (gval && rowv && owner) scales[gi * n + col] = __half_as_ushort(__float2half_rn(s));
+            if (qzeros) {
+                uint32_t zw = SYM ? 0x77777777u : ((uint32_t)zp << (4 * (row & 7)));
+                if (!SYM) {
+                    zw |= __shfl_xor_sync(FULL, zw, 1);
+                    zw |= __shfl_xor_sync(FULL, zw, 2);
+                    zw |= __shfl_xor_sync(FULL, zw, 4);
+                }
+                if (gval && rowv && owner && (row & 7) == 0) qzeros[gi * (n / 8) + col / 8] = (int32_t)zw;
+            }
+        }
+        if (g_idx && n0 == 0) {
+            for (int i = lane; i < T::KT; i += 32)
+                if (k0 + i < k) g_idx[k0 + i] = (int32_t)((k0 + i) / G);
+        }
+        __syncwarp();
+        step(nb, kb);
+        if (++st == T::NS) { st = 0; parity ^= 1u; }
+    }
+    if (!ok && lane == 0) {
+        for (int i = 0; i < T::NS; ++i)
+            if ((inflight >> i) & 1u) wait_stage(bar_s + 8 * i, i >= st ? parity : parity ^ 1u, kMaxPolls);
+    }
+    __syncwarp();
+    if (SNR) wq::finish_snr(wq::ff_of(ksw), wq::ff_of(kse), slots, counter, snr_db, nullptr);
+}
+#undef WQ_WCHUNK
+
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
 // (no link-time dependency on the driver library).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -462,6 +774,67 @@ wq_status launch_quant(const uint16_t* w, int64_t n, int64_t k, int32_t* qweight
     gptq_quant_kernel<SYM, G, SNR><<<grid, T::THREADS, T::SMEM, st>>>(
         map, n, k, qweight, qzeros, scales, g_idx, slots, counter, snr_db, g_stage_polls.load());
     return wqh::check_launch();
+}
+
+// Tensor map of an fp16 / fp32 weight [n, k]: boxes of box_rows rows x 128 bytes
+// with the 128-byte swizzle; reads outside the tensor return zeros.
+wq_status wide_map(const void* w, int dt, int64_t n, int64_t k, int box_rows, CUtensorMap* map) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return wqh::cuda_status(cudaErrorNotSupported);
+    const int es = dt == WQ_DTYPE_F32 ? 4 : 2;
+    const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)n};
+    const cuuint64_t strides[1] = {(cuuint64_t)k * es};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, dt == WQ_DTYPE_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           2, const_cast<void*>(w), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? WQ_OK : wqh::cuda_status(cudaErrorInvalidValue);
+}
+
+template <bool SYM, int DT, int G, bool SNR>
+wq_status launch_wide(const void* w, int64_t n, int64_t k, int32_t* qweight, int32_t* qzeros,
+                      uint16_t* scales, int32_t* g_idx, float4* slots, unsigned* counter, double* snr_db,
+                      cudaStream_t st) {
+    using T = WTile<DT, G>;
+    const void* fn = (const void*)gptq_quant_wide_kernel<SYM, DT, G, SNR>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        wq_status s = wqh::cuda_status(
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM));
+        if (s != WQ_OK) return s;
+        attr_set = true;
+    }
+    CUtensorMap map;
+    wq_status s = wide_map(w, DT, n, k, T::R, &map);
+    if (s != WQ_OK) return s;
+    const int64_t warp_tiles = ((n + T::R - 1) / T::R) * ((k + T::KT - 1) / T::KT);
+    const int grid = wqh::grid_for(fn, T::THREADS, T::SMEM, (warp_tiles + T::WARPS - 1) / T::WARPS,
+                                   wqh::kMaxPartials);
+    gptq_quant_wide_kernel<SYM, DT, G, SNR><<<grid, T::THREADS, T::SMEM, st>>>(
+        map, n, k, qweight, qzeros, scales, g_idx, slots, counter, snr_db, g_stage_polls.load());
+    return wqh::check_launch();
+}
+
+template <bool SYM, int DT>
+wq_status wide_group(int group, bool snr, const void* w, int64_t n, int64_t k, int32_t* qweight,
+                     int32_t* qzeros, uint16_t* scales, int32_t* g_idx, float4* slots, unsigned* counter,
+                     double* snr_db, cudaStream_t st) {
+#define WQ_WIDE_CASE(GG)                                                                                   \
+    case GG:                                                                                               \
+        return snr ? launch_wide<SYM, DT, GG, true>(w, n, k, qweight, qzeros, scales, g_idx, slots, counter, \
+                                                    snr_db, st)                                            \
+                   : launch_wide<SYM, DT, GG, false>(w, n, k, qweight, qzeros, scales, g_idx, slots,       \
+                                                     counter, snr_db, st);
+    switch (group) {
+        WQ_WIDE_CASE(32)
+        WQ_WIDE_CASE(64)
+        WQ_WIDE_CASE(128)
+        WQ_WIDE_CASE(256)
+        default: return WQ_ERR_UNSUPPORTED;
+    }
+#undef WQ_WIDE_CASE
 }
 
 template <bool SYM>
@@ -745,4 +1118,30 @@ extern "C" wq_status wq_device_status(void) {
 
 namespace wqh {
 unsigned gptq_stage_polls_exchange(unsigned polls) { return g_stage_polls.exchange(polls); }
+}  // namespace wqh
+
+namespace wqh {
+// GPTQ quantization of an fp16 / fp32 weight (arguments checked by the caller;
+// the workspace, when snr_db is given, holds the SNR's counter and partials).
+wq_status gptq_quantize_wide(const void* w, int dt, int64_t n, int64_t k, int group, bool sym,
+                             int32_t* qweight, int32_t* qzeros, uint16_t* scales, int32_t* g_idx,
+                             double* snr_db, void* ws, cudaStream_t st) {
+    if (n > INT32_MAX || k > INT32_MAX) return WQ_ERR_BAD_SHAPE;  // TMA coordinates are 32-bit
+    unsigned* counter = snr_db ? (unsigned*)ws : nullptr;
+    float4* slots = snr_db ? (float4*)((char*)ws + wqh::kCtrlBytes) : nullptr;
+    if (snr_db) {
+        const wq_status s0 = wqh::cuda_status(cudaMemsetAsync(counter, 0, sizeof(unsigned), st));
+        if (s0 != WQ_OK) return s0;
+    }
+    const bool snr = snr_db != nullptr;
+    if (dt == WQ_DTYPE_F32)
+        return sym ? wide_group<true, WQ_DTYPE_F32>(group, snr, w, n, k, qweight, qzeros, scales, g_idx, slots,
+                                                    counter, snr_db, st)
+                   : wide_group<false, WQ_DTYPE_F32>(group, snr, w, n, k, qweight, qzeros, scales, g_idx, slots,
+                                                     counter, snr_db, st);
+    return sym ? wide_group<true, WQ_DTYPE_F16>(group, snr, w, n, k, qweight, qzeros, scales, g_idx, slots,
+                                                counter, snr_db, st)
+               : wide_group<false, WQ_DTYPE_F16>(group, snr, w, n, k, qweight, qzeros, scales, g_idx, slots,
+                                                 counter, snr_db, st);
+}
 }  // namespace wqh

@@ -2,13 +2,10 @@
 //
 // export_gptq_cpu.py (quantize_sym, quantize_asym) and quantize_dflash_mxfp4.py
 // (quantize_mxfp4) both start from w.float(): an fp16 or fp32 weight reaches
-// the same binary32 arithmetic as a bf16 one, only with more significant bits,
-// so the shortcuts of the bf16 kernels (exact bf16x2 max/min, exact squares)
-// do not apply and these kernels take each binary32 step as written: IEEE
-// divisions (per element as a correctly rounded reciprocal plus one FMA
-// correction, which gives the same quotient), round half to even, compensated
-// sums of the rounded squares for the SNR.  bf16 weights go to the tuned bf16
-// kernels.
+// the same binary32 arithmetic as a bf16 one, only with more significant bits.
+// GPTQ: argument checks here, the warp-tiled TMA kernel in gptq.cu
+// (gptq_quant_wide_kernel).  MXFP4: one thread per 32-value block, below.
+// bf16 weights go to the bf16 kernels.
 #include <cuda_fp16.h>
 
 #include "wq_common.cuh"
@@ -36,86 +33,6 @@ __device__ __forceinline__ void load8(const void* base, int64_t idx, float (&v)[
             v[2 * i + 1] = f.y;
         }
     }
-}
-
-// One thread per (weight row c, group g): the group's G values are a contiguous
-// run of row c; work items (column block, group) are spread over a grid of at
-// most wqh::kMaxPartials CTAs so that the SNR partials fit the workspace.
-template <bool SYM, int DT, bool SNR>
-__global__ void __launch_bounds__(kWideThreads)
-gptq_quant_wide_kernel(const void* __restrict__ w, int64_t n, int64_t k, int G, int32_t* __restrict__ qweight,
-                       int32_t* __restrict__ qzeros, uint16_t* __restrict__ scales, int32_t* __restrict__ g_idx,
-                       float4* __restrict__ slots, unsigned* __restrict__ counter, double* __restrict__ snr_db) {
-    const int lane = threadIdx.x & 31;
-    const int64_t ncb = (n + kWideThreads - 1) / kWideThreads, ng = k / G;
-    wq::KSum ksw, kse;
-    for (int64_t it = blockIdx.x; it < ncb * ng; it += gridDim.x) {
-        const int64_t g = it / ncb, c = (it - g * ncb) * kWideThreads + threadIdx.x;
-        const bool valid = c < n;
-        const int64_t row0 = c * k + g * G;
-        float v[8];
-        // group statistics over binary32 values
-        float amax = 0.f, wmax = -INFINITY, wmin = INFINITY;
-        if (valid) {
-            for (int j = 0; j < G; j += 8) {
-                load8<DT>(w, row0 + j, v);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    amax = fmaxf(amax, fabsf(v[i]));
-                    wmax = fmaxf(wmax, v[i]);
-                    wmin = fminf(wmin, v[i]);
-                }
-            }
-        }
-        float s, z;
-        if (SYM) {
-            s = fmaxf(__fdiv_rn(amax, 8.0f), 1e-9f);  // scale = (amax / 8).clamp(min=1e-9)
-            z = 8.0f;
-        } else {
-            s = __fdiv_rn(fmaxf(__fsub_rn(wmax, wmin), 1e-9f), 15.0f);      // (wmax - wmin).clamp / 15
-            z = fminf(fmaxf(rintf(__fdiv_rn(-wmin, s)), 0.0f), 15.0f);      // (-wmin / s).round().clamp
-        }
-        if (!valid) s = 1.0f, z = 8.0f;
-        // codes, packed 8 per word along K (low nibble first).  x / s as the
-        // correctly rounded reciprocal plus one FMA correction (exact while s,
-        // 1/s and the quotient are normal; a subnormal quotient rounds to code zp
-        // either way); IEEE division for scales above 2^100.
-        const bool fast = s <= 0x1p100f;
-        const float rs = __frcp_rn(s);
-        if (valid) {
-            for (int j = 0; j < G; j += 8) {
-                load8<DT>(w, row0 + j, v);
-                uint32_t word = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float qt = fast ? wq::div_by_recip(v[i], s, rs) : __fdiv_rn(v[i], s);
-                    const float q = fminf(fmaxf(__fadd_rn(rintf(qt), z), 0.0f), 15.0f);
-                    word |= (uint32_t)q << (4 * i);
-                    if (SNR) {
-                        const float e = __fsub_rn(v[i], __fmul_rn(__fsub_rn(q, z), s));
-                        ksw.add(__fmul_rn(v[i], v[i]));
-                        kse.add(__fmul_rn(e, e));
-                    }
-                }
-                qweight[(g * G + j) / 8 * n + c] = (int32_t)word;
-            }
-            scales[g * n + c] = __half_as_ushort(__float2half_rn(s));
-        }
-        if (qzeros) {
-            // eight neighbouring columns' zero points in one word (all lanes shuffle)
-            uint32_t zw = SYM ? 0x77777777u : (uint32_t)z << (4 * (lane & 7));
-            if (!SYM) {
-                zw |= __shfl_xor_sync(0xffffffffu, zw, 1);
-                zw |= __shfl_xor_sync(0xffffffffu, zw, 2);
-                zw |= __shfl_xor_sync(0xffffffffu, zw, 4);
-            }
-            if (valid && (c & 7) == 0) qzeros[g * (n / 8) + c / 8] = (int32_t)zw;
-        }
-    }
-    if (g_idx)
-        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < k; i += (int64_t)gridDim.x * blockDim.x)
-            g_idx[i] = (int32_t)(i / G);
-    if (SNR) wq::finish_snr(wq::ff_of(ksw), wq::ff_of(kse), slots, counter, snr_db, nullptr);
 }
 
 // Two binary32 values -> two e2m1 nibbles (round half to even, saturating at
@@ -199,28 +116,8 @@ wq_status gptq_quantize_ex(const void* w, int w_dtype, int64_t n, int64_t k, int
         (qzeros && !wqh::aligned_to(qzeros, 4)) || (g_idx && !wqh::aligned_to(g_idx, 4)) ||
         (snr_db && !wqh::aligned_to(workspace, 256)))
         return WQ_ERR_MISALIGNED;
-    cudaStream_t st = (cudaStream_t)stream;
-    unsigned* counter = snr_db ? (unsigned*)workspace : nullptr;
-    float4* slots = snr_db ? (float4*)((char*)workspace + wqh::kCtrlBytes) : nullptr;
-    if (snr_db) {
-        const wq_status s0 = wqh::cuda_status(cudaMemsetAsync(counter, 0, sizeof(unsigned), st));
-        if (s0 != WQ_OK) return s0;
-    }
-    const int64_t items = ((n + kWideThreads - 1) / kWideThreads) * (k / group);
-    const int grid = (int)(items < wqh::kMaxPartials ? items : wqh::kMaxPartials);
-#define WQ_WIDE(S, D, R)                                                                                      \
-    gptq_quant_wide_kernel<S, D, R><<<grid, kWideThreads, 0, st>>>(w, n, k, group, qweight, qzeros, scales,    \
-                                                                   g_idx, slots, counter, snr_db)
-    const bool f32 = w_dtype == WQ_DTYPE_F32, snr = snr_db != nullptr;
-    if (sym) {
-        if (f32) { if (snr) WQ_WIDE(true, WQ_DTYPE_F32, true); else WQ_WIDE(true, WQ_DTYPE_F32, false); }
-        else { if (snr) WQ_WIDE(true, WQ_DTYPE_F16, true); else WQ_WIDE(true, WQ_DTYPE_F16, false); }
-    } else {
-        if (f32) { if (snr) WQ_WIDE(false, WQ_DTYPE_F32, true); else WQ_WIDE(false, WQ_DTYPE_F32, false); }
-        else { if (snr) WQ_WIDE(false, WQ_DTYPE_F16, true); else WQ_WIDE(false, WQ_DTYPE_F16, false); }
-    }
-#undef WQ_WIDE
-    return wqh::check_launch();
+    return wqh::gptq_quantize_wide(w, w_dtype, n, k, group, sym != 0, qweight, qzeros, scales, g_idx, snr_db,
+                                   workspace, (cudaStream_t)stream);
 }
 
 wq_status mxfp4_quantize_ex(const void* w, int w_dtype, int64_t n, int64_t k, int tie_mode, uint8_t* packed,

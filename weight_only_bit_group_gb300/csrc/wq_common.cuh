@@ -312,6 +312,11 @@ int grid_for(const void* kernel, int threads, size_t smem, int64_t work_items, i
 wq_status cuda_status(cudaError_t e);
 wq_status check_launch();
 
+// GPTQ quantization of an fp16 / fp32 weight (gptq.cu; arguments already checked).
+wq_status gptq_quantize_wide(const void* w, int dt, int64_t n, int64_t k, int group, bool sym,
+                             int32_t* qweight, int32_t* qzeros, uint16_t* scales, int32_t* g_idx,
+                             double* snr_db, void* ws, cudaStream_t st);
+
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 inline bool aligned_to(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
