@@ -9,9 +9,9 @@
 // Grid: ceil(N/128) column blocks x S slices along K.  A CTA is 4 warps over the
 // same 128 output columns; lane = 4 adjacent columns, so one 16-byte piece of a
 // qweight row holds the 8 codes of each of its 4 columns.  Each warp walks
-// `batches` batches of 8 qweight rows (64 input channels) through a 4-stage
+// `batches` batches of 8 qweight rows (64 input channels) through a 3-stage
 // cp.async pipeline of its own: the codes (16 bytes per lane and row) and the
-// batch's x rows land in shared memory three batches ahead of their use, so
+// batch's x rows land in shared memory two batches ahead of their use, so
 // the loads stream while earlier batches are computed.  The group scales and
 // zero points of the next batch are read into registers one batch ahead.
 // Per qweight word the 8 codes become bf16 128 + c by byte permutes (two codes
@@ -32,7 +32,7 @@ namespace {
 constexpr int kThreads = 128;   // 4 warps
 constexpr int kCols = 128;      // output columns per CTA (4 per lane)
 constexpr int kRPW = 8;         // qweight rows per warp batch
-constexpr int kNST = 4;         // pipeline stages per warp
+constexpr int kNST = 3;         // pipeline stages per warp
 constexpr int kMaxSlices = 64;
 constexpr int kMaxM = 8;
 
