@@ -160,12 +160,23 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
     return r;
 }
 
-__device__ __forceinline__ void e2m1x2_to_f(uint32_t byte, float& lo, float& hi) {
+// Two e2m1 nibbles of one byte -> their values as f16x2 (exact).
+__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
     uint32_t h2;
     uint16_t in = (uint16_t)byte;
     asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "h"(in));
-    lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
-    hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+    return h2;
+}
+
+// (m - v) for the f16x2 grid values m and the binary32 pair v, by mixed-precision
+// subtractions that read the f16 halves in place (exact: see awq_err).
+__device__ __forceinline__ wq::f2_t grid_minus(uint32_t h2, wq::f2_t v) {
+    float d0, d1;
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "sub.rn.f32.f16 %0, lo, %3;\n\tsub.rn.f32.f16 %1, hi, %4;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(h2), "f"(v.x), "f"(v.y));
+    return wq::f2(d0, d1);
 }
 
 // e2m1 rounding of (lo, hi) straight back to f16x2 values (round half even,
@@ -195,7 +206,7 @@ __device__ __forceinline__ uint32_t page_tie(uint32_t nib, float v) {
 // only by the rounding of ws and of the final products (relative 1e-7), far
 // inside the 1e-4 agreement required of the errors.
 template <int TIE>
-__global__ void __launch_bounds__(kThreads) awq_err(const uint16_t* __restrict__ w, int64_t k,
+__global__ void __launch_bounds__(kThreads, 2) awq_err(const uint16_t* __restrict__ w, int64_t k,
                                                     int64_t rows, int64_t row_stride, int n_alpha,
                                                     AlphaList al, const float* __restrict__ s_tab,
                                                     const float* __restrict__ q_tab,
@@ -230,16 +241,24 @@ __global__ void __launch_bounds__(kThreads) awq_err(const uint16_t* __restrict__
             wf[q][2] = wq::bf2_to_f2(u.z);
             wf[q][3] = wq::bf2_to_f2(u.w);
         }
+        // the column tables of alpha i + 1 are read while alpha i is evaluated (their
+        // L2 latency was the kernel's main stall)
+        auto tables = [&](int i, float4 (&t)[4]) {
+            const int64_t off = (int64_t)i * k + (cval ? col : 0);
+            t[0] = __ldg(reinterpret_cast<const float4*>(s_tab + off));
+            t[1] = __ldg(reinterpret_cast<const float4*>(s_tab + off) + 1);
+            t[2] = cval ? __ldg(reinterpret_cast<const float4*>(q_tab + off)) : make_float4(0, 0, 0, 0);
+            t[3] = cval ? __ldg(reinterpret_cast<const float4*>(q_tab + off) + 1) : make_float4(0, 0, 0, 0);
+        };
+        float4 tn[4];
+        tables(0, tn);
 #pragma unroll
         for (int i = 0; i < kMaxAlpha; ++i) {
             if (i >= n_alpha) break;
             wq::f2_t S[4], Q[4];
             {
-                const int64_t off = (int64_t)i * k + (cval ? col : 0);
-                const float4 s0 = __ldg(reinterpret_cast<const float4*>(s_tab + off));
-                const float4 s1 = __ldg(reinterpret_cast<const float4*>(s_tab + off) + 1);
-                const float4 q0 = cval ? __ldg(reinterpret_cast<const float4*>(q_tab + off)) : make_float4(0, 0, 0, 0);
-                const float4 q1 = cval ? __ldg(reinterpret_cast<const float4*>(q_tab + off) + 1) : make_float4(0, 0, 0, 0);
+                const float4 s0 = tn[0], s1 = tn[1], q0 = tn[2], q1 = tn[3];
+                if (i + 1 < n_alpha) tables(i + 1, tn);
                 S[0] = wq::f2(s0.x, s0.y); S[1] = wq::f2(s0.z, s0.w);
                 S[2] = wq::f2(s1.x, s1.y); S[3] = wq::f2(s1.z, s1.w);
                 Q[0] = wq::f2(q0.x, q0.y); Q[1] = wq::f2(q0.z, q0.w);
@@ -258,24 +277,34 @@ __global__ void __launch_bounds__(kThreads) awq_err(const uint16_t* __restrict__
                 float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));  // a tree: short chain
                 amax = fmaxf(amax, wq::shfl_xor(amax, 1));
                 amax = fmaxf(amax, wq::shfl_xor(amax, 2));
-                const int ex = exp_from_f32(amax);
-                const float inv = __uint_as_float((uint32_t)(127 - ex) << 23);  // 2^-exp, normal
-                const float sc = __uint_as_float(ex == -127 ? 0x00400000u : (uint32_t)(ex + 127) << 23);
+                // 2^-exp and 2^exp.  With amax >= 2^-124 (every lane of the warp)
+                // exp = floor(log2 amax) - 2 >= -126 and both are bit arithmetic on
+                // the exponent field of amax; otherwise the clamped general form
+                float inv, sc;
+                const uint32_t ab = __float_as_uint(amax);
+                if (__all_sync(0xffffffffu, ab >= 0x01800000u)) {
+                    const uint32_t pe = ab & 0x7F800000u;         // 2^floor(log2 amax)
+                    inv = __uint_as_float(0x80000000u - pe);      // 2^(2 - floor(log2 amax))
+                    sc = __uint_as_float(pe - 0x01000000u);       // 2^(floor(log2 amax) - 2)
+                } else {
+                    const int ex = exp_from_f32(amax);
+                    inv = __uint_as_float((uint32_t)(127 - ex) << 23);  // 2^-exp, normal
+                    sc = __uint_as_float(ex == -127 ? 0x00400000u : (uint32_t)(ex + 127) << 23);
+                }
                 const wq::f2_t INV = wq::f2(inv, inv);
                 wq::f2_t loc = wq::f2(0.0f, 0.0f);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const wq::f2_t v = wq::mul2(ws[j], INV);
-                    wq::f2_t m;
+                    uint32_t h2;  // the e2m1 grid values of v as f16x2
                     if (TIE == WQ_TIE_PAGE_LITERAL) {
                         uint32_t b = e2m1x2(v.x, v.y);
                         b = page_tie(b & 15u, v.x) | (page_tie(b >> 4, v.y) << 4);
-                        e2m1x2_to_f(b, m.x, m.y);
+                        h2 = e2m1x2_to_h2(b);
                     } else {
-                        const uint32_t h2 = e2m1_round2(v.x, v.y);
-                        m = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+                        h2 = e2m1_round2(v.x, v.y);
                     }
-                    const wq::f2_t d = wq::fma2(v, wq::f2(-1.0f, -1.0f), m);  // m - v, exact
+                    const wq::f2_t d = grid_minus(h2, v);  // m - v, exact
                     loc = wq::fma2(wq::mul2(d, d), Q[j], loc);
                 }
                 part = __fadd_rn(part, __fmul_rn(__fmul_rn(__fadd_rn(loc.x, loc.y), sc), sc));
