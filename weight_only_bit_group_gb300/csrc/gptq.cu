@@ -120,7 +120,7 @@ __device__ __forceinline__ uint32_t quant_chunk(const uint4 v, const GroupConst&
         word += (uint32_t)__float_as_int(t0) << (8 * p);
         word += (uint32_t)__float_as_int(t1) << (8 * p + 4);
         if (SNR && CLAMP == 0) {
-            const wq::f2_t nd = wq::mul2(wq::add2(tq, NM2), NS2);  // -deq = -RN((code - zp) * s)
+            const wq::f2_t nd = wq::mul2_kept(wq::add2(tq, NM2), NS2);  // -deq = -RN((code - zp) * s)
             const wq::f2_t e = wq::add2(x, nd);                    // RN(w - deq)
             se2 = wq::fma2(e, e, se2);
             sw2 = wq::fma2(x, x, sw2);
@@ -472,7 +472,7 @@ __device__ __forceinline__ void wide_pair(const wq::f2_t x, const wq::f2_t R2, c
     word += (uint32_t)__float_as_int(t1) << (4 * nib + 4);
     if (SNR) {
         // deq = RN((code - zp) * s), e = RN(w - deq); squares summed by FMAs
-        const wq::f2_t nd = wq::mul2(wq::add2(wq::f2(t0, t1), wq::f2(-kMagic, -kMagic)), NS2);
+        const wq::f2_t nd = wq::mul2_kept(wq::add2(wq::f2(t0, t1), wq::f2(-kMagic, -kMagic)), NS2);
         const wq::f2_t e = wq::add2(x, nd);
         se2 = wq::fma2(e, e, se2);
         sw2 = wq::fma2(x, x, sw2);

@@ -175,6 +175,13 @@ __device__ __forceinline__ void f2u(f2_t v, float& lo, float& hi) {
     hi = v.y;
 }
 __device__ __forceinline__ f2_t mul2(f2_t a, f2_t b) { return __fmul2_rn(a, b); }
+// RN(a * b) for a product that is then added to something: a packed multiply
+// followed by a packed add was fused into one FMA by the code generator (one
+// rounding instead of two, measured in the instruction mix), so the product is
+// formed as fma(a, b, +0), which equals RN(a * b) whenever the product is not
+// -0 (then +0: the sign of a zero term is irrelevant to the sums it enters) and
+// which no rewrite may merge with the following add.
+__device__ __forceinline__ f2_t mul2_kept(f2_t a, f2_t b) { return __ffma2_rn(a, b, make_float2(0.0f, 0.0f)); }
 __device__ __forceinline__ f2_t add2(f2_t a, f2_t b) { return __fadd2_rn(a, b); }
 __device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c) { return __ffma2_rn(a, b, c); }
 // The two bf16 of a packed word as a binary32 pair (exact).
