@@ -425,17 +425,37 @@ gptq_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             uint32_t sh[4][NSH];
             uint32_t sc, zp;
         };
+        // With n k % 256 == 0 every shard length and base is a multiple of 32 bytes,
+        // so a thread's 32 codes of a K block (32 aligned bytes per shard) never
+        // straddle a chunk boundary: two 16-byte loads per shard and one bit offset
+        const bool whole = numel % 256 == 0;
         auto fetch = [&](int kb, Raw& o) {
             // positions advance by 64 elements per K block (wrapping into the next chunk)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            if (whole) {
 #pragma unroll
                 for (int i = 0; i < NSH; ++i) {
-                    int64_t p = pos[i] + 8 * j;
-                    int c = chunk[i];
-                    while (p >= L[i]) { p -= L[i]; ++c; }
-                    o.sh[j][i] = (uint32_t)(c * kbits[i]);
-                    o.w[j][i] = rv ? __ldg(reinterpret_cast<const unsigned long long*>(ux_packed + base[i] + p)) : 0ull;
+                    const uint4* src = reinterpret_cast<const uint4*>(ux_packed + base[i] + pos[i]);
+                    const uint4 a = rv ? __ldg(src) : make_uint4(0, 0, 0, 0);
+                    const uint4 b = rv ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
+                    o.w[0][i] = (uint64_t)a.x | ((uint64_t)a.y << 32);
+                    o.w[1][i] = (uint64_t)a.z | ((uint64_t)a.w << 32);
+                    o.w[2][i] = (uint64_t)b.x | ((uint64_t)b.y << 32);
+                    o.w[3][i] = (uint64_t)b.z | ((uint64_t)b.w << 32);
+                    const uint32_t sh = (uint32_t)(chunk[i] * kbits[i]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) o.sh[j][i] = sh;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                    for (int i = 0; i < NSH; ++i) {
+                        int64_t p = pos[i] + 8 * j;
+                        int c = chunk[i];
+                        while (p >= L[i]) { p -= L[i]; ++c; }
+                        o.sh[j][i] = (uint32_t)(c * kbits[i]);
+                        o.w[j][i] = rv ? __ldg(reinterpret_cast<const unsigned long long*>(ux_packed + base[i] + p)) : 0ull;
+                    }
                 }
             }
             const int gi = (kb * BK + 32 * h) / ux_group;
