@@ -171,6 +171,7 @@ class Workload:
         # the products a caller takes home live in one buffer per projection
         # (typed views at 256-byte offsets), so that they travel home in one copy
         self.product_bufs = []
+        self.product_regions = []
         for name, w in self.layer:
             n, k = w.shape
             g = k // GROUP_GPTQ
@@ -190,6 +191,10 @@ class Workload:
                 total = (total + nbytes + 255) // 256 * 256
             buf = torch.empty(total, dtype=torch.uint8, device=device)
             self.product_bufs.append(buf)
+            # byte ranges of each format's products (asym, sym, mxfp4 + its error,
+            # uintx): each can travel home as soon as its quantize call is done
+            starts = [offs[0], offs[4], offs[8], offs[12]]
+            self.product_regions.append([(a, b) for a, b in zip(starts, starts[1:] + [total])])
             o = {"asym": {}, "sym": {}, "mx": {}, "snr": {}, "ux": {}}
             for (tag, key, shape, dt), off in zip(specs, offs):
                 nbytes = int(torch.Size(shape).numel()) * torch.empty((), dtype=dt).element_size()
@@ -724,9 +729,13 @@ def run_e2e(args, wl, dev, dist, world):
     copies the layer from pinned host memory to the device and copies the
     quantized products back, inside the timed region.  The copies in run one
     after another on one stream; each projection is then one chain on its own
-    stream (every row of the path, then one copy home of the projection's product
-    buffer), so the copies of one projection overlap the kernels and copies of
-    the others; the AWQ search starts once gate and up have landed."""
+    stream: its four quantize calls, each followed at once by the copy home of
+    that format's products, then its four dequantize calls.  The device-to-host
+    direction is the critical path on this link (it carries 462 MB against the
+    436 MB coming in and can only start once a projection's first products
+    exist), so products leave as early as they are ready; the copies of one
+    projection overlap the kernels and copies of the others.  The AWQ search
+    starts once gate and up have landed."""
     host_flat = wl.flat.cpu().pin_memory()
     dev_flat = torch.empty_like(wl.flat)
     host_in = wl.views(host_flat, wl.layer)
@@ -734,9 +743,12 @@ def run_e2e(args, wl, dev, dist, world):
     phases = wl.phases(dev_in, wl.gate_up_view(dev_flat))
     per_proj, awq_outs = wl.results()
     host_awq = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in awq_outs]
-    # chain of projection i: every phase's call, then one copy home of the
-    # projection's product buffer (all its quantized tensors and scalars)
-    chains = [[ph[5][i] for ph in phases if ph[5] is not None] for i in range(len(dev_in))]
+    # chain of projection i: the quantize calls (each with the index of the
+    # product region it fills), then the dequantize calls
+    region_of = {"gptq_quantize_asym": 0, "gptq_quantize_sym": 1, "mxfp4_quantize+err": 2, "uintx_quantize": 3}
+    chains = [[(ph[5][i], region_of[ph[0]]) for ph in phases if ph[5] is not None and ph[0] in region_of]
+              + [(ph[5][i], None) for ph in phases if ph[5] is not None and ph[0] not in region_of]
+              for i in range(len(dev_in))]
     host_bufs = [torch.empty(b.shape, dtype=b.dtype, pin_memory=True) for b in wl.product_bufs]
     awq_fn = [ph[1] for ph in phases if ph[5] is None]
     names = [name for name, _ in wl.layer]
@@ -767,9 +779,11 @@ def run_e2e(args, wl, dev, dist, world):
             st = wl.streams[i]
             st.wait_event(landed[i])
             with torch.cuda.stream(st):
-                for f in chains[i]:
+                for f, r in chains[i]:
                     f()
-                host_bufs[i].copy_(wl.product_bufs[i], non_blocking=True)
+                    if r is not None:
+                        a, b = wl.product_regions[i][r]
+                        host_bufs[i][a:b].copy_(wl.product_bufs[i][a:b], non_blocking=True)
             e = torch.cuda.Event()
             e.record(st)
             joins.append(e)
