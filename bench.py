@@ -1073,7 +1073,7 @@ def main():
     ap.add_argument("--wdtype", choices=["bf16", "f16", "f32"], default="bf16",
                     help="weight type for --kernel gptq_quantize_* / mxfp4_quantize")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--awq-after", default="gptq_dequantize_sym",
+    ap.add_argument("--awq-after", default="mxfp4_quantize+err",
                     help="fork the AWQ search's side stream at the step's start or after this phase")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
