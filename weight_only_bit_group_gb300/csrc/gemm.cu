@@ -19,8 +19,9 @@
 //   warp 16     TMA: x tile [128 tokens x 64] (128-byte swizzle) and qweight
 //               rows [8 x 128 features]; owns the TMEM allocation
 //   warp 17     MMA: one thread issues tcgen05.mma (A from TMEM, x from shared
-//               memory; M 128, N 128, K 16) per 16 values of K, commits to the
-//               stage and group barriers
+//               memory; M 128, N 128, K 16) per 16 values of K, taking K blocks
+//               in pairs (one wait, one fence and one stage release per pair),
+//               and commits to the stage-pair and group barriers
 // Keeping A out of shared memory matters: an N = 128 MMA reading both operands
 // from shared memory uses all of its bandwidth by itself.
 // Every wait is bounded; on a timeout the CTA records WQ_ERR_DEVICE_TIMEOUT in
@@ -175,9 +176,9 @@ __device__ __forceinline__ bool poll_bar(uint32_t bar, uint32_t parity, uint32_t
 // One non-blocking test of the phase with parity `parity`.  A completed phase is
 // the common case in the pipeline's steady state, and mbarrier.try_wait with a
 // suspend hint costs a few hundred cycles even then (measured with clock64
-// stamps in the MMA-issuing thread: ~300 cycles per wait, three waits per K
-// block, against ~220 cycles to issue the block's MMAs), so every wait tries
-// this first.
+// stamps in the MMA-issuing thread: ~300 cycles per wait on a completed phase,
+// against ~250 cycles to issue a K block's four MMAs), so every wait tries this
+// first.
 __device__ __forceinline__ bool test_bar(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(

@@ -13,17 +13,21 @@
 // reads bank conflict free; the next tile streams in while the current one is
 // coded.  The group max/min is a bf16x2 reduction inside the lane (plus one
 // shuffle when a group spans both halves); scale and zero point use true IEEE
-// divisions once per group (warp-uniformly through the rare large-scale path).  Per element pair, with packed binary32 pairs (f32x2): the clamp
-// to the code range is applied to w itself, in bf16x2, with bounds bf16(lo*s)
-// and bf16(hi*s) (exact, see bound2); the quotient by the scale is a correctly
-// rounded reciprocal plus one FMA correction step (bit-identical to IEEE
-// division); round-half-even comes from the binary32 adder (q + 1.5*2^23); the
-// nibble pack is one multiply-add per code.  The eight codes along k of one row
-// are one qweight word, so the [K/8, N] transpose costs nothing.  The optional
-// reconstruction SNR is accumulated from the same registers and reduced by the
-// last CTA to finish.  Every wait on an mbarrier is bounded: a wait that runs
-// out records WQ_ERR_DEVICE_TIMEOUT in a device status word (read by
-// wq_device_status) and the kernel finishes without touching the stage again.
+// divisions once per group (warp-uniformly through the rare large-scale path).
+// Per element pair, with packed binary32 pairs (f32x2): where a clamp to the
+// code range can act (always for sym; for asym only in warps where some group's
+// extreme code leaves [0, 15], tested exactly per group) it is applied to w
+// itself, in bf16x2, with bounds bf16(lo*s) and bf16(hi*s) (exact, see bound2);
+// the quotient by the scale is a correctly rounded reciprocal plus one FMA
+// correction step (bit-identical to IEEE division); round-half-even comes from
+// the binary32 adder (q + 1.5*2^23); the nibble pack is one shift-add per code.
+// The eight codes along k of one row are one qweight word, so the [K/8, N]
+// transpose costs nothing.  The optional reconstruction SNR is accumulated from
+// the same registers and reduced by the last CTA to finish.  fp16 and fp32
+// weights take the same pipeline with their own kernel (gptq_quant_wide_kernel,
+// below).  Every wait on an mbarrier is bounded: a wait that runs out records
+// WQ_ERR_DEVICE_TIMEOUT in a device status word (read by wq_device_status) and
+// the kernel finishes without touching the stage again.
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <atomic>
