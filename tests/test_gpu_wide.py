@@ -65,6 +65,57 @@ def test_gptq_wide_hand_groups_tiled():
         assert np.all(r["qweight"].cpu().numpy() == word)
 
 
+def degenerate_weight(dtype, group, seed):
+    """Rows of groups that take every special path of the fp16 / fp32 kernel:
+    constant groups (range 0, scale from the 1e-9 floor), narrow all-positive and
+    all-negative groups (zero point clamped to 0 / 15, so codes leave [0, 15]
+    before the clamp), values far beyond 2^16 x the range (the IEEE-division
+    path), a single outlier, exact zeros and (fp32) subnormals, next to ordinary
+    groups in the same warp tile."""
+    g = torch.Generator().manual_seed(seed)
+    n, k = 64, 4 * max(group, 128)
+    w = torch.randn(n, k, generator=g) * 0.02
+    big = 1e12 if dtype == torch.float32 else 3.0e4  # squares and their sums stay finite
+    tiny = 1e-40 if dtype == torch.float32 else 1e-7
+    for r in range(n):
+        kind = r % 8
+        for g0 in range(0, k, group):
+            seg = slice(g0, g0 + group)
+            u = torch.rand(group, generator=g)
+            if kind == 0:
+                w[r, seg] = 0.3 if (g0 // group) % 2 == 0 else -2.0   # constant groups
+            elif kind == 1:
+                w[r, seg] = 1.0 + 1e-3 * u                            # narrow, all positive
+            elif kind == 2:
+                w[r, seg] = -1.0 - 1e-3 * u                           # narrow, all negative
+            elif kind == 3:
+                w[r, seg] = big * (1.0 + 1e-6 * u)                    # |w| far beyond 2^16 range
+            elif kind == 4:
+                w[r, seg] = 0.0
+                w[r, g0 + 3] = 5.0                                    # one outlier among zeros
+            elif kind == 5:
+                w[r, seg] = tiny * (u - 0.5)                          # tiny / subnormal values
+    return w.to(dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16])
+@pytest.mark.parametrize("group", [32, 128])
+@pytest.mark.parametrize("sym", [True, False])
+def test_gptq_wide_degenerate_groups(dtype, group, sym):
+    w = degenerate_weight(dtype, group, 60 + group)
+    fn = wq.gptq_quantize_sym if sym else wq.gptq_quantize_asym
+    r = fn(w.to(DEV), group, True)
+    qw, qz, sc, gi, snr = oracle.gptq_quantize_f32(w.float().numpy(), group, sym)
+    assert np.array_equal(r["qweight"].cpu().numpy(), qw), "qweight"
+    assert np.array_equal(r["scales"].cpu().view(torch.int16).numpy().view(np.uint16), sc), "scales"
+    assert np.array_equal(r["qzeros"].cpu().numpy(), qz), "qzeros"
+    # the large groups' errors dominate both norms here, so the SNR can sit near
+    # 0 dB: 1e-4 relative to it, or 1e-4 dB
+    got = float(r["snr_db"])
+    assert np.isfinite(snr) and abs(got - snr) <= REL * max(abs(snr), 1.0), (got, snr)
+    assert wq.device_status() == 0
+
+
 def check_mx(w, tie):
     p, e = wq.mxfp4_quantize(w.to(DEV), tie)
     rp, re = oracle.mxfp4_quantize_f32(w.float().numpy(), tie)
