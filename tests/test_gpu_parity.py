@@ -124,6 +124,46 @@ def test_gptq_degenerate_groups():
         assert np.array_equal(npy(res["qzeros"]), qz)
 
 
+@pytest.mark.parametrize("group", [32, 128])
+def test_gptq_degenerate_groups_mixed_warps_with_snr(group):
+    """Degenerate groups (constant, narrow all-positive / all-negative so that the
+    zero point clamps, a lone outlier, zeros, tiny values, large values) in every
+    eighth row, ordinary groups in the rest: warps mix lanes that need the clamps
+    with lanes that need none, and the fused SNR runs through both coding paths.
+    Codes bit for bit; the SNR to 1e-4 relative (1e-4 dB when it is near 0)."""
+    g = torch.Generator().manual_seed(70 + group)
+    n, k = 96, 512
+    w = torch.randn(n, k, generator=g) * 0.02
+    for r in range(0, n, 8):
+        kind = (r // 8) % 6
+        for g0 in range(0, k, group):
+            seg = slice(g0, g0 + group)
+            u = torch.rand(group, generator=g)
+            if kind == 0:
+                w[r, seg] = 0.3
+            elif kind == 1:
+                w[r, seg] = 1.0 + 0.01 * u
+            elif kind == 2:
+                w[r, seg] = -1.0 - 0.01 * u
+            elif kind == 3:
+                w[r, seg] = 0.0
+                w[r, g0 + 5] = 4.0
+            elif kind == 4:
+                w[r, seg] = 1e-30 * (u - 0.5)
+            else:
+                w[r, seg] = 1e12 * (1.0 + 0.5 * u)
+    w = w.to(torch.bfloat16)
+    for sym in (True, False):
+        fn = wq.gptq_quantize_sym if sym else wq.gptq_quantize_asym
+        res = fn(w.to(DEV), group=group, snr=True)
+        qw, qz, sc, gi, snr = oracle.gptq_quantize(w, group, sym)
+        assert np.array_equal(npy(res["qweight"]), qw)
+        assert np.array_equal(u16(res["scales"]), sc)
+        assert np.array_equal(npy(res["qzeros"]), qz)
+        got = float(res["snr_db"])
+        assert np.isfinite(snr) and abs(got - snr) <= REL * max(abs(snr), 1.0), (got, snr)
+
+
 def test_gptq_layer_full_size_asym():
     """The seven projections of one layer (218,103,808 weights, outlier columns)
     at full size, asym group 128 -- the configuration the benchmark times."""
