@@ -66,6 +66,14 @@ def test_gptq_gemm_partial_last_k_block():
         check(acts(40, k, 94), qw, qz, sc, n, k, 32, sym)
 
 
+def test_gptq_gemm_odd_number_of_k_blocks():
+    # k = 17 blocks of 64 with group 64: the MMA thread's last pair holds one block
+    n, k = 136, 1088
+    for sym in (True, False):
+        qw, qz, sc = quantized(n, k, 64, sym, 97)
+        check(acts(70, k, 98), qw, qz, sc, n, k, 64, sym)
+
+
 @pytest.mark.parametrize("shape", [(4096, 4096), (14336, 4096), (4096, 14336)])
 def test_gptq_gemm_layer_shapes_prefill(shape):
     n, k = shape
@@ -164,3 +172,11 @@ def test_uintx_gemm_layer_shape():
     y1 = check_ux(x, packed, sc, zp, deq, n, k, 4, 64)
     y2 = wq.uintx_gemm(x.to(DEV), packed, sc, zp, n, k, 4, 64)
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("nbits", [3, 5])
+def test_uintx_gemm_odd_number_of_k_blocks(nbits):
+    # k = 15 blocks of 64: the last pair of K blocks holds one block
+    n, k = 136, 960
+    packed, sc, zp, deq = uintx_inputs(n, k, nbits, 64, 119 + nbits)
+    check_ux(acts(70, k, 120), packed, sc, zp, deq, n, k, nbits, 64)
